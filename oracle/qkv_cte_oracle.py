@@ -1,0 +1,258 @@
+"""Oracle for the fused QKV context-encoding projection (test infrastructure).
+
+THIS IS TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH. Only the tests, the
+package's ``smoke()`` check and the benchmark's CPU-baseline / reference leg may
+import it. It shares no code with the CUDA library: it decodes every FP8, UE8M0
+and bf16 bit pattern itself and computes in float64.
+
+What it computes is the method of the ``qkv_cte`` kernel reference page
+("Kernel reference: qkv_cte - Wan2.2 additions to the NKI Library QKV CTE MXFP8
+projection", vllm-omni-neuron docs, kernels/qkv-cte), cited below as [qkv_cte]
+with the page's own section headings:
+
+  1. O[S, I] = A[S, H] @ W[H, I] (+ bias), I = (n_q + 2 n_kv) * d_head
+     ([qkv_cte] "Upstream behavior", first bullet), with ROW_MX activations
+     (per-row FP8 codes plus one fp32 dequant scale per row) and MXFP8 weights
+     ([qkv_cte] "Upstream behavior", quantization-modes bullet; "Interface"
+     argument table, rows packed_hidden / weight / weight_scales / bias).
+  2. Across-heads RMSNorm of Q and of K: a per-token sum(x^2) over the whole
+     un-normalised Q (and K) segment, inv_rms = rsqrt(sum / (n_heads * d_head * tp)
+     + eps), then multiplication by the segment-wide per-channel gamma
+     ([qkv_cte] "Design", "1) Across-heads QK RMSNorm with a single cross-rank
+     AllReduce", steps a, b, c).
+  3. Rotate-half RoPE after the norm, pairing lanes (i, i + d/2) within each head,
+     with position-only cos/sin tables broadcast over heads:
+     out = y * cos + [-y_hi, y_lo] * sin ([qkv_cte] "Design", "2) Bundled
+     rotate-half RoPE in the same pass").
+  4. V is never normalised ([qkv_cte] "Design" 1, step c); with n_kv_heads = 0 the
+     whole projection is one segment, normalised as Q ([qkv_cte] "Design",
+     "5) Individual QKV projections for cross-attention").
+
+Readings of points the page leaves open (each also listed in the design notes):
+
+  * MX block: one UE8M0 scale per 32 consecutive H elements of each weight row
+    (the OCP MX block); the page only says "MXFP8" / "MX weight".
+  * weight_scales [1, I] fp32 ("Interface" table) is an optional per-output-column
+    multiplier applied with the activation row scale; absent means 1.
+  * The activation carries no MX block scale of its own: its only scale is the
+    per-row fp32 dequant scale (ROW_MX, "Interface" table, packed_hidden row).
+  * sum(x^2) is taken over the bias-included, un-normalised projection before any
+    rounding ("Design" 1, step a: the sum of the output copied out of the matmul).
+  * tp = 1: this call holds every head of the segment.
+  * gamma multiplies before the rotation, and inv_rms folds into it:
+    y = x * inv_rms * gamma, then the rotate-half combination ("Design" 1 step c
+    with "Design" 2).
+  * norm off leaves gamma unused (gamma belongs to the norm); RoPE off leaves y.
+
+Pins: every function here is checked in tests/test_oracle_pins.py against
+something other than itself - an exhaustive comparison with torch's float8 codecs,
+exact rational brute force on tiny shapes, torch's fp64 rms_norm, the complex
+closed form of the rotation, and the invariants the method implies. No function
+is parity-unpinned.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SEG_Q, SEG_K, SEG_V = 0, 1, 2
+
+
+# ---------------------------------------------------------------------------
+# codecs
+# ---------------------------------------------------------------------------
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 ("fn": no infinities) bit patterns -> float64.
+
+    Layout s.eeee.mmm with exponent bias 7. e == 0 encodes subnormals
+    m * 2^-9; e == 15 with m == 7 is NaN; every other pattern is
+    (1 + m/8) * 2^(e-7). This is the FP8 element type of both the packed
+    activation codes and the MX weight ([qkv_cte] "Interface" table).
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = m * 2.0 ** -9
+    mag = np.where(e == 0, sub, normal)
+    mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+def decode_ue8m0(codes: np.ndarray) -> np.ndarray:
+    """UE8M0 block-scale bytes -> float64: 2^(e - 127); 0xFF is NaN."""
+    e = np.asarray(codes, dtype=np.uint8).astype(np.float64)
+    return np.where(e == 255, np.nan, np.exp2(e - 127.0))
+
+
+def decode_bf16(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64 (exact: bf16 is the top half of fp32)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# step 1: the projection
+# ---------------------------------------------------------------------------
+
+def dequant_activations(A: np.ndarray, a_scale: np.ndarray) -> np.ndarray:
+    """ROW_MX activations: a[t, h] = e4m3(A[t, h]) * a_scale[t].
+
+    [qkv_cte] "Upstream behavior" (packed H + 4 layout: per-row FP8 codes plus a
+    4-byte fp32 dequant scale) and "Interface" table, packed_hidden row.
+    """
+    return decode_e4m3(A) * np.asarray(a_scale, dtype=np.float64)[:, None]
+
+
+def dequant_weights(W: np.ndarray, w_sf: np.ndarray) -> np.ndarray:
+    """MXFP8 weights: w[i, h] = e4m3(W[i, h]) * 2^(w_sf[i, h // 32] - 127).
+
+    W is stored K-major as [I, H] (row i = output channel i); w_sf is [I, H/32].
+    [qkv_cte] "Upstream behavior" (MXFP8 quantization mode) and "Design" 3
+    (nc_matmul_mx applies the MX scales inside the matmul).
+    """
+    I, H = W.shape
+    scale = decode_ue8m0(w_sf)                       # [I, H/32]
+    block = np.arange(H) // 32                       # the block each h belongs to
+    return decode_e4m3(W) * scale[:, block]
+
+
+def project(A, a_scale, W, w_sf, w_col_scale=None, bias=None) -> np.ndarray:
+    """O = A @ W (+ bias) in float64: o[t, i] = sum_h a[t, h] * w[i, h] * cs[i] + b[i].
+
+    [qkv_cte] "Upstream behavior", first bullet; weight_scales and bias from the
+    "Interface" table (cs = weight_scales, 1 when absent; b = bias, 0 when absent).
+    """
+    a = dequant_activations(A, a_scale)
+    w = dequant_weights(W, w_sf)
+    o = a @ w.T
+    if w_col_scale is not None:
+        o = o * np.asarray(w_col_scale, dtype=np.float64)[None, :]
+    if bias is not None:
+        o = o + decode_bf16(bias)[None, :]
+    return o
+
+
+# ---------------------------------------------------------------------------
+# step 2: across-heads RMSNorm
+# ---------------------------------------------------------------------------
+
+def segments(n_q_heads: int, n_kv_heads: int, d_head: int):
+    """Column ranges of the Q, K and V segments of O: I = (n_q + 2 n_kv) * d_head.
+
+    With n_kv_heads == 0 there is one segment and it is treated as Q
+    ([qkv_cte] "Design" 5).
+    """
+    q = (0, n_q_heads * d_head)
+    k = (q[1], q[1] + n_kv_heads * d_head)
+    v = (k[1], k[1] + n_kv_heads * d_head)
+    return q, k, v
+
+
+def segment_sumsq(o: np.ndarray, n_q_heads: int, n_kv_heads: int, d_head: int) -> np.ndarray:
+    """Per-token sum(x^2) over the whole un-normalised Q segment and K segment.
+
+    Returns [rows, 2] (column 1 is 0 when there is no K segment).
+    [qkv_cte] "Design" 1, step a (accumulate).
+    """
+    q, k, _ = segments(n_q_heads, n_kv_heads, d_head)
+    ss = np.zeros((o.shape[0], 2), dtype=np.float64)
+    ss[:, SEG_Q] = np.sum(o[:, q[0]:q[1]] ** 2, axis=1)
+    if n_kv_heads > 0:
+        ss[:, SEG_K] = np.sum(o[:, k[0]:k[1]] ** 2, axis=1)
+    return ss
+
+
+def inv_rms(sumsq: np.ndarray, n_q_heads: int, n_kv_heads: int, d_head: int, eps: float,
+            tp: int = 1) -> np.ndarray:
+    """inv_rms = 1 / sqrt(sumsq / (n_heads * d_head * tp) + eps), per token and segment.
+
+    [qkv_cte] "Design" 1, step b (reduce). With one GPU holding every head, tp = 1
+    and the cross-rank AllReduce is the identity. The K column is 0 when the call
+    has no K segment (its rsqrt is skipped, "Design" 5).
+    """
+    out = np.zeros_like(sumsq)
+    out[:, SEG_Q] = 1.0 / np.sqrt(sumsq[:, SEG_Q] / (n_q_heads * d_head * tp) + eps)
+    if n_kv_heads > 0:
+        out[:, SEG_K] = 1.0 / np.sqrt(sumsq[:, SEG_K] / (n_kv_heads * d_head * tp) + eps)
+    return out
+
+
+# ---------------------------------------------------------------------------
+# step 3: norm apply + rotate-half RoPE on one segment
+# ---------------------------------------------------------------------------
+
+def rotate_half(y: np.ndarray, d_head: int) -> np.ndarray:
+    """[-y_hi, y_lo] per head: lane i pairs with lane i + d/2 ([qkv_cte] "Design" 2)."""
+    rows, width = y.shape
+    h = y.reshape(rows, width // d_head, d_head)
+    lo = h[:, :, : d_head // 2]
+    hi = h[:, :, d_head // 2:]
+    return np.concatenate([-hi, lo], axis=2).reshape(rows, width)
+
+
+def apply_norm_rope(x: np.ndarray, inv: np.ndarray, gamma, cos, sin, d_head: int,
+                    norm: int, rope: int) -> np.ndarray:
+    """One segment (all its heads) of one set of tokens.
+
+    y = x * inv_rms * gamma when the norm is on ("Design" 1, step c), else y = x;
+    out = y * cos + rotate_half(y) * sin when RoPE is on ("Design" 2), where cos/sin
+    are the per-position [rows, d_head] tables broadcast over the heads.
+    """
+    rows, width = x.shape
+    y = x
+    if norm:
+        y = x * inv[:, None] * decode_bf16(gamma)[None, :]
+    if rope:
+        heads = width // d_head
+        c = np.tile(np.asarray(cos, dtype=np.float64), (1, heads))
+        s = np.tile(np.asarray(sin, dtype=np.float64), (1, heads))
+        y = y * c + rotate_half(y, d_head) * s
+    return y
+
+
+# ---------------------------------------------------------------------------
+# the whole path
+# ---------------------------------------------------------------------------
+
+def qkv_cte(A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, *, n_q_heads: int,
+            n_kv_heads: int, d_head: int, norm: int, rope: int, eps: float,
+            w_col_scale=None, rows=None):
+    """The fused projection for the given rows (all rows when ``rows`` is None).
+
+    Rows are independent, so a row subset gives exactly the rows of the full
+    result. Returns a dict of float64 arrays: O [rows, I] (Q/K normalised and
+    rotated, V as projected), sumsq [rows, 2], inv_rms [rows, 2] (zeros when the
+    norm is off).
+    """
+    if rows is not None:
+        rows = np.asarray(rows)
+        A = A[rows]
+        a_scale = a_scale[rows]
+        if cos is not None:
+            cos = cos[rows]
+            sin = sin[rows]
+    o = project(A, a_scale, W, w_sf, w_col_scale, bias)
+    ss = segment_sumsq(o, n_q_heads, n_kv_heads, d_head)
+    inv = inv_rms(ss, n_q_heads, n_kv_heads, d_head, eps) if norm else np.zeros_like(ss)
+    out = o.copy()
+    q, k, _ = segments(n_q_heads, n_kv_heads, d_head)
+    out[:, q[0]:q[1]] = apply_norm_rope(o[:, q[0]:q[1]], inv[:, SEG_Q], gamma_q, cos, sin,
+                                        d_head, norm, rope)
+    if n_kv_heads > 0:
+        out[:, k[0]:k[1]] = apply_norm_rope(o[:, k[0]:k[1]], inv[:, SEG_K], gamma_k, cos, sin,
+                                            d_head, norm, rope)
+    return dict(O=out, sumsq=ss, inv_rms=inv, projected=o)
+
+
+def qkv_cte_from_inputs(call, inp, rows=None):
+    """Convenience wrapper over :func:`qkv_cte` for a ``workloads.Call`` and its inputs."""
+    from workloads import as_numpy_bits
+
+    n = {k: as_numpy_bits(v) for k, v in inp.items()}
+    return qkv_cte(n["A"], n["a_scale"], n["W"], n["w_sf"], n["bias"], n["gamma_q"],
+                   n["gamma_k"], n["cos"], n["sin"], n_q_heads=call.n_q_heads,
+                   n_kv_heads=call.n_kv_heads, d_head=call.d_head, norm=call.norm,
+                   rope=call.rope, eps=call.eps, w_col_scale=n["w_col_scale"], rows=rows)

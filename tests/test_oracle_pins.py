@@ -1,0 +1,521 @@
+"""Pins of the float64 oracle to things other than itself (CPU only).
+
+Every oracle function is checked against an independent source:
+  * the FP8 / UE8M0 / bf16 codecs exhaustively against torch's own dtypes and the
+    OFP8 specification's code points (tests/golden/ofp8_e4m3_values.txt);
+  * the whole path against an exact brute force written with pure-Python loops and
+    rational arithmetic on tiny shapes, and against a hand-worked closed-form case
+    (tests/golden/hand_example.json);
+  * the across-heads norm against torch's fp64 ``rms_norm`` over the whole segment;
+  * the rotate-half RoPE against the complex-multiplication closed form;
+  * invariants from the qkv_cte page's definitions: unit-RMS rows for an all-ones
+    gamma with zero angle, per-pair norm preservation, V equal to the plain
+    dequantised projection, the separate-mode Q call equal to the fused Q slice,
+    and row subsets equal to the rows of the full result.
+
+``test_planted_mistakes_are_caught`` plants plausible mistakes in the oracle (on the
+CPU, through monkeypatch) and checks that at least one pin fails for each.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import qkv_cte_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# helpers (independent decoders from torch)
+# ---------------------------------------------------------------------------
+
+def _torch_e4m3(codes):
+    return torch.from_numpy(np.asarray(codes, dtype=np.uint8).copy()).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy()
+
+
+def _torch_bf16(bits):
+    return torch.from_numpy(np.asarray(bits, dtype=np.uint16).view(np.int16).copy()).view(
+        torch.bfloat16).to(torch.float64).numpy()
+
+
+def _rand_codes(rng, shape):
+    c = rng.integers(0, 254, size=shape).astype(np.uint8)
+    c[c == 0x7F] = 0x7E   # no NaN codes
+    return c
+
+
+def _rand_bf16_bits(rng, shape, mean=0.0, std=1.0):
+    x = torch.from_numpy(rng.normal(mean, std, size=shape).astype(np.float32)).to(torch.bfloat16)
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
+def _tiny_case(seed=0, T=3, H=96, nq=2, nkv=1, d=4, col_scale=True, distinct_halves=True):
+    rng = np.random.default_rng(seed)
+    I = (nq + 2 * nkv) * d
+    c = dict(
+        A=_rand_codes(rng, (T, H)),
+        a_scale=rng.uniform(0.01, 0.2, size=T).astype(np.float32),
+        W=_rand_codes(rng, (I, H)),
+        w_sf=rng.integers(118, 136, size=(I, H // 32)).astype(np.uint8),
+        w_col_scale=(rng.uniform(0.5, 2.0, size=I).astype(np.float32) if col_scale else None),
+        bias=_rand_bf16_bits(rng, I, 0.0, 0.5),
+        gamma_q=_rand_bf16_bits(rng, nq * d, 1.0, 0.3),
+        gamma_k=_rand_bf16_bits(rng, nkv * d, 1.0, 0.3) if nkv else None,
+    )
+    ang = rng.uniform(-math.pi, math.pi, size=(T, d))
+    if not distinct_halves:
+        ang[:, d // 2:] = ang[:, : d // 2]
+    c["cos"] = np.cos(ang).astype(np.float32)
+    c["sin"] = np.sin(ang).astype(np.float32)
+    shape = dict(n_q_heads=nq, n_kv_heads=nkv, d_head=d)
+    return c, shape
+
+
+def _run(c, shape, norm=1, rope=1, eps=1e-6, rows=None):
+    return O.qkv_cte(c["A"], c["a_scale"], c["W"], c["w_sf"], c["bias"], c["gamma_q"],
+                     c["gamma_k"], c["cos"] if rope else None, c["sin"] if rope else None,
+                     norm=norm, rope=rope, eps=eps, w_col_scale=c["w_col_scale"], rows=rows,
+                     **shape)
+
+
+def _brute_force(c, nq, nkv, d, norm, rope, eps):
+    """The whole path with Python loops: exact rationals for the projection and the
+    sums of squares, floats for rsqrt and the rotation. Decoders come from torch."""
+    A = _torch_e4m3(c["A"])
+    W = _torch_e4m3(c["W"])
+    T, H = A.shape
+    I = W.shape[0]
+    sf = [[Fraction(2) ** (int(e) - 127) for e in row] for row in c["w_sf"]]
+    bias = _torch_bf16(c["bias"])
+    cs = c["w_col_scale"]
+    o = []
+    for t in range(T):
+        row = []
+        for i in range(I):
+            acc = Fraction(0)
+            for h in range(H):
+                acc += Fraction(float(A[t, h])) * Fraction(float(W[i, h])) * sf[i][h // 32]
+            acc *= Fraction(float(c["a_scale"][t]))
+            if cs is not None:
+                acc *= Fraction(float(cs[i]))
+            acc += Fraction(float(bias[i]))
+            row.append(acc)
+        o.append(row)
+    segs = [(0, nq * d, _torch_bf16(c["gamma_q"]), nq)]
+    if nkv:
+        segs.append((nq * d, (nq + nkv) * d, _torch_bf16(c["gamma_k"]), nkv))
+    out = [[float(v) for v in row] for row in o]
+    ss = [[0.0, 0.0] for _ in range(T)]
+    inv = [[0.0, 0.0] for _ in range(T)]
+    for t in range(T):
+        for s_idx, (lo, hi, gamma, nh) in enumerate(segs):
+            exact = sum((o[t][i] ** 2 for i in range(lo, hi)), Fraction(0))
+            ss[t][s_idx] = float(exact)
+            r = 1.0 / math.sqrt(float(exact / (nh * d)) + eps) if norm else 0.0
+            inv[t][s_idx] = r
+            y = []
+            for i in range(lo, hi):
+                v = float(o[t][i])
+                y.append(v * r * float(gamma[i - lo]) if norm else v)
+            for head in range(nh):
+                base = head * d
+                for j in range(d):
+                    yj = y[base + j]
+                    if rope:
+                        if j < d // 2:
+                            partner = -y[base + j + d // 2]
+                        else:
+                            partner = y[base + j - d // 2]
+                        val = yj * float(c["cos"][t][j]) + partner * float(c["sin"][t][j])
+                    else:
+                        val = yj
+                    out[t][lo + base + j] = val
+    return np.array(out), np.array(ss), np.array(inv)
+
+
+def _close(a, b, rel=1e-12, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} vs {b.shape}"
+    err = np.abs(a - b)
+    tol = rel * (np.abs(b) + np.max(np.abs(b)) * 1e-3 + 1e-300)
+    assert np.all(err <= tol), f"{what}: max err {err.max():.3e}"
+
+
+# ---------------------------------------------------------------------------
+# pins (plain functions so the planted-mistake test can run them all)
+# ---------------------------------------------------------------------------
+
+def pin_e4m3_exhaustive():
+    codes = np.arange(256, dtype=np.uint8)
+    got = O.decode_e4m3(codes)
+    ref = _torch_e4m3(codes)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert np.array_equal(np.signbit(got[ok]), np.signbit(ref[ok]))
+
+
+def pin_e4m3_spec_values():
+    with open(os.path.join(GOLDEN, "ofp8_e4m3_values.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            code, value = line.split()[:2]
+            got = float(O.decode_e4m3(np.array([int(code, 16)], dtype=np.uint8))[0])
+            if value == "nan":
+                assert math.isnan(got), code
+            else:
+                want = float(eval(value))  # exact expressions such as 7*2**-9
+                assert got == want, (code, got, want)
+                if value.startswith("-"):
+                    assert math.copysign(1.0, got) < 0, code
+
+
+def pin_ue8m0_exhaustive():
+    codes = np.arange(256, dtype=np.uint8)
+    got = O.decode_ue8m0(codes)
+    for e in range(255):
+        assert got[e] == math.ldexp(1.0, e - 127), e
+    assert math.isnan(got[255])
+    if hasattr(torch, "float8_e8m0fnu"):
+        ref = torch.from_numpy(codes.copy()).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+        assert np.array_equal(got[:255], ref[:255])
+
+
+def pin_bf16_exhaustive():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = O.decode_bf16(bits)
+    ref = _torch_bf16(bits)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def pin_full_bruteforce():
+    for seed, (norm, rope) in enumerate([(1, 1), (1, 0), (0, 1), (0, 0)]):
+        c, shape = _tiny_case(seed=seed)
+        res = _run(c, shape, norm=norm, rope=rope)
+        out, ss, inv = _brute_force(c, shape["n_q_heads"], shape["n_kv_heads"], shape["d_head"],
+                                    norm, rope, 1e-6)
+        _close(res["O"], out, what=f"O norm={norm} rope={rope}")
+        _close(res["sumsq"], ss, what="sumsq")
+        if norm:
+            _close(res["inv_rms"], inv, what="inv_rms")
+
+
+def pin_separate_bruteforce():
+    c, shape = _tiny_case(seed=7, nq=3, nkv=0, d=4, col_scale=False)
+    res = _run(c, shape, norm=1, rope=0)
+    out, ss, inv = _brute_force(c, 3, 0, 4, 1, 0, 1e-6)
+    _close(res["O"], out, what="separate O")
+    _close(res["sumsq"], ss, what="separate sumsq")
+    _close(res["inv_rms"], inv, what="separate inv")
+
+
+def pin_hand_example():
+    with open(os.path.join(GOLDEN, "hand_example.json")) as f:
+        g = json.load(f)
+    H = g["hidden"]
+    I = (g["n_q_heads"] + 2 * g["n_kv_heads"]) * g["d_head"]
+    hx = lambda xs: np.array([int(x, 16) for x in xs], dtype=np.uint16)
+    res = O.qkv_cte(
+        np.full((1, H), int(g["A_code"], 16), dtype=np.uint8),
+        np.array([g["a_scale"]], dtype=np.float32),
+        np.full((I, H), int(g["W_code"], 16), dtype=np.uint8),
+        np.repeat(np.array(g["w_sf"], dtype=np.uint8)[:, None], H // 32, axis=1),
+        hx(g["bias_bf16"]), hx(g["gamma_q_bf16"]), hx(g["gamma_k_bf16"]),
+        np.array([g["cos"]], dtype=np.float32), np.array([g["sin"]], dtype=np.float32),
+        n_q_heads=g["n_q_heads"], n_kv_heads=g["n_kv_heads"], d_head=g["d_head"], norm=1, rope=1,
+        eps=g["eps"])
+    ev = lambda xs: np.array([eval(x, {"math": math}) for x in xs], dtype=np.float64)
+    _close(res["sumsq"][0], ev(g["expected"]["sumsq"]), rel=1e-15, what="hand sumsq")
+    _close(res["inv_rms"][0], ev(g["expected"]["inv_rms"]), rel=1e-14, what="hand inv")
+    _close(res["O"][0], ev(g["expected"]["O"]), rel=1e-14, what="hand O")
+
+
+def pin_norm_vs_torch_rms_norm():
+    c, shape = _tiny_case(seed=3, T=5, H=64, nq=3, nkv=2, d=8)
+    res = _run(c, shape, norm=1, rope=0, eps=1e-3)
+    o = torch.from_numpy(res["projected"])
+    for lo, hi, g in ((0, 24, c["gamma_q"]), (24, 40, c["gamma_k"])):
+        ref = torch.nn.functional.rms_norm(o[:, lo:hi], (hi - lo,),
+                                           weight=torch.from_numpy(_torch_bf16(g)), eps=1e-3)
+        _close(res["O"][:, lo:hi], ref.numpy(), rel=1e-12, what="rms_norm")
+    _close(res["O"][:, 40:], res["projected"][:, 40:], rel=0, what="V untouched")
+
+
+def pin_rope_complex_closed_form():
+    rng = np.random.default_rng(11)
+    rows, heads, d = 4, 3, 16
+    y = rng.normal(size=(rows, heads * d))
+    ang = rng.uniform(-10, 10, size=(rows, d // 2))
+    cos = np.concatenate([np.cos(ang)] * 2, axis=1)
+    sin = np.concatenate([np.sin(ang)] * 2, axis=1)
+    got = O.apply_norm_rope(y, None, None, cos, sin, d, norm=0, rope=1)
+    h = y.reshape(rows, heads, d)
+    z = (h[:, :, : d // 2] + 1j * h[:, :, d // 2:]) * np.exp(1j * ang)[:, None, :]
+    ref = np.concatenate([z.real, z.imag], axis=2).reshape(rows, heads * d)
+    _close(got, ref, rel=1e-13, what="rope closed form")
+
+
+def pin_unit_rms_invariant():
+    c, shape = _tiny_case(seed=5, T=4, H=64, nq=2, nkv=2, d=8, distinct_halves=False)
+    c["gamma_q"] = np.full(16, 0x3F80, dtype=np.uint16)
+    c["gamma_k"] = np.full(16, 0x3F80, dtype=np.uint16)
+    c["cos"] = np.ones_like(c["cos"])
+    c["sin"] = np.zeros_like(c["sin"])
+    eps = 1e-2
+    res = _run(c, shape, norm=1, rope=1, eps=eps)
+    for lo, hi, col in ((0, 16, 0), (16, 32, 1)):
+        ms = res["sumsq"][:, col] / 16
+        rms = np.sqrt(np.mean(res["O"][:, lo:hi] ** 2, axis=1))
+        _close(rms, np.sqrt(ms / (ms + eps)), rel=1e-13, what="unit rms")
+
+
+def pin_pair_norm_invariant():
+    c, shape = _tiny_case(seed=6, T=4, H=64, nq=2, nkv=1, d=8, distinct_halves=False)
+    # float64 tables: the invariant needs cos^2 + sin^2 == 1 to rounding of fp64
+    ang = np.random.default_rng(60).uniform(-math.pi, math.pi, size=(4, 4))
+    c["cos"] = np.cos(np.concatenate([ang, ang], axis=1))
+    c["sin"] = np.sin(np.concatenate([ang, ang], axis=1))
+    normed = _run(c, shape, norm=1, rope=0)["O"]
+    roped = _run(c, shape, norm=1, rope=1)["O"]
+    for lo, hi in ((0, 16), (16, 24)):
+        a = normed[:, lo:hi].reshape(4, -1, 8)
+        b = roped[:, lo:hi].reshape(4, -1, 8)
+        na = a[:, :, :4] ** 2 + a[:, :, 4:] ** 2
+        nb = b[:, :, :4] ** 2 + b[:, :, 4:] ** 2
+        _close(nb, na, rel=1e-12, what="pair norm")
+
+
+def pin_v_is_plain_projection():
+    c, shape = _tiny_case(seed=8, T=2, H=64, nq=1, nkv=2, d=4)
+    res = _run(c, shape, norm=1, rope=1)
+    out, _, _ = _brute_force(dict(c), 1, 2, 4, 0, 0, 1e-6)   # plain projection
+    _close(res["O"][:, 12:], out[:, 12:], what="V")
+
+
+def pin_separate_equals_fused_slice():
+    c, shape = _tiny_case(seed=9, T=3, H=64, nq=2, nkv=2, d=8, distinct_halves=False)
+    fused = _run(c, shape, norm=1, rope=1)
+    q = 16
+    sep = dict(c, W=c["W"][:q], w_sf=c["w_sf"][:q], bias=c["bias"][:q],
+               w_col_scale=c["w_col_scale"][:q], gamma_k=None)
+    res = _run(sep, dict(n_q_heads=2, n_kv_heads=0, d_head=8), norm=1, rope=1)
+    _close(res["O"], fused["O"][:, :q], rel=1e-14, what="separate vs fused")
+    _close(res["inv_rms"][:, 0], fused["inv_rms"][:, 0], rel=1e-14, what="separate inv")
+
+
+def pin_rows_subset():
+    c, shape = _tiny_case(seed=10, T=6, H=64, nq=1, nkv=1, d=8)
+    full = _run(c, shape)
+    rows = np.array([0, 3, 5])
+    sub = _run(c, shape, rows=rows)
+    for k in ("O", "sumsq", "inv_rms"):
+        _close(sub[k], full[k][rows], rel=0, what=k)
+
+
+PINS = [pin_e4m3_exhaustive, pin_e4m3_spec_values, pin_ue8m0_exhaustive, pin_bf16_exhaustive,
+        pin_full_bruteforce, pin_separate_bruteforce, pin_hand_example, pin_norm_vs_torch_rms_norm,
+        pin_rope_complex_closed_form, pin_unit_rms_invariant, pin_pair_norm_invariant,
+        pin_v_is_plain_projection, pin_separate_equals_fused_slice, pin_rows_subset]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
+def test_pin(pin):
+    pin()
+
+
+# ---------------------------------------------------------------------------
+# planted mistakes: each must make at least one pin fail
+# ---------------------------------------------------------------------------
+
+_orig = {name: getattr(O, name) for name in
+         ("decode_e4m3", "decode_ue8m0", "decode_bf16", "dequant_activations", "dequant_weights",
+          "project", "segments", "segment_sumsq", "inv_rms", "rotate_half", "apply_norm_rope",
+          "qkv_cte")}
+
+
+def _e4m3_bias8(codes):
+    return _orig["decode_e4m3"](codes) * 0.5
+
+
+def _e4m3_subnormal_as_normal(codes):
+    c = np.asarray(codes, dtype=np.uint8)
+    v = _orig["decode_e4m3"](c)
+    sub = ((c >> 3) & 0xF) == 0
+    return np.where(sub & ((c & 7) > 0), np.sign(v + 0.0) * (1 + (c & 7) / 8.0) * 2.0 ** -6, v)
+
+
+def _e4m3_unsigned(codes):
+    return np.abs(_orig["decode_e4m3"](codes))
+
+
+def _ue8m0_bias128(codes):
+    return _orig["decode_ue8m0"](codes) * 0.5
+
+
+def _bf16_wrong_shift(bits):
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 15
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def _weights_block16(W, w_sf):
+    I, H = W.shape
+    scale = O.decode_ue8m0(w_sf)
+    return O.decode_e4m3(W) * scale[:, np.minimum(np.arange(H) // 16, H // 32 - 1)]
+
+
+def _weights_block_transposed(W, w_sf):
+    I, H = W.shape
+    scale = O.decode_ue8m0(w_sf)
+    return O.decode_e4m3(W) * scale[:, np.arange(H) % (H // 32)]
+
+
+def _act_scale_ignored(A, a_scale):
+    return O.decode_e4m3(A)
+
+
+def _project_no_bias(A, a_scale, W, w_sf, w_col_scale=None, bias=None):
+    return _orig["project"](A, a_scale, W, w_sf, w_col_scale, None)
+
+
+def _project_no_colscale(A, a_scale, W, w_sf, w_col_scale=None, bias=None):
+    return _orig["project"](A, a_scale, W, w_sf, None, bias)
+
+
+def _project_transposed(A, a_scale, W, w_sf, w_col_scale=None, bias=None):
+    a = O.dequant_activations(A, a_scale)
+    w = O.dequant_weights(W, w_sf)
+    o = a @ w[:, ::-1].T          # output columns reversed (a wrong index map)
+    if w_col_scale is not None:
+        o = o * np.asarray(w_col_scale, dtype=np.float64)[None, :]
+    if bias is not None:
+        o = o + O.decode_bf16(bias)[None, :]
+    return o
+
+
+def _sumsq_mean(o, nq, nkv, d):
+    ss = _orig["segment_sumsq"](o, nq, nkv, d)
+    ss[:, 0] /= nq * d
+    return ss
+
+
+def _sumsq_k_includes_v(o, nq, nkv, d):
+    ss = _orig["segment_sumsq"](o, nq, nkv, d)
+    if nkv:
+        ss[:, 1] = np.sum(o[:, nq * d:] ** 2, axis=1)
+    return ss
+
+
+def _inv_eps_outside(ss, nq, nkv, d, eps, tp=1):
+    out = _orig["inv_rms"](ss, nq, nkv, d, 0.0, tp)
+    return out + eps
+
+
+def _inv_heads_only(ss, nq, nkv, d, eps, tp=1):
+    out = np.zeros_like(ss)
+    out[:, 0] = 1.0 / np.sqrt(ss[:, 0] / nq + eps)
+    if nkv:
+        out[:, 1] = 1.0 / np.sqrt(ss[:, 1] / nkv + eps)
+    return out
+
+
+def _inv_k_uses_nq(ss, nq, nkv, d, eps, tp=1):
+    out = _orig["inv_rms"](ss, nq, nkv, d, eps, tp)
+    if nkv:
+        out[:, 1] = 1.0 / np.sqrt(ss[:, 1] / (nq * d) + eps)
+    return out
+
+
+def _rotate_sign(y, d):
+    return -_orig["rotate_half"](y, d)
+
+
+def _rotate_interleaved(y, d):
+    rows, width = y.shape
+    h = y.reshape(rows, width // 2, 2)
+    return np.stack([-h[:, :, 1], h[:, :, 0]], axis=2).reshape(rows, width)
+
+
+def _gamma_after_rope(x, inv, gamma, cos, sin, d, norm, rope):
+    y = _orig["apply_norm_rope"](x, inv, None, cos, sin, d, 0, rope)
+    if norm:
+        y = y * inv[:, None] * O.decode_bf16(gamma)[None, :]
+    return y
+
+
+def _cos_sin_swapped(x, inv, gamma, cos, sin, d, norm, rope):
+    return _orig["apply_norm_rope"](x, inv, gamma, sin, cos, d, norm, rope)
+
+
+def _gamma_ignored(x, inv, gamma, cos, sin, d, norm, rope):
+    ones = np.full(x.shape[1], 0x3F80, dtype=np.uint16)
+    return _orig["apply_norm_rope"](x, inv, ones, cos, sin, d, norm, rope)
+
+
+def _v_normalised(*args, **kw):
+    res = _orig["qkv_cte"](*args, **kw)
+    nq, nkv, d = kw["n_q_heads"], kw["n_kv_heads"], kw["d_head"]
+    if nkv and kw["norm"]:
+        v = res["projected"][:, (nq + nkv) * d:]
+        res["O"][:, (nq + nkv) * d:] = v / np.sqrt(np.mean(v ** 2, axis=1, keepdims=True) + kw["eps"])
+    return res
+
+
+def _k_uses_gamma_q(*args, **kw):
+    args = list(args)
+    if args[6] is not None:
+        args[6] = args[5][: len(args[6])]
+    return _orig["qkv_cte"](*args, **kw)
+
+
+MUTANTS = {
+    "e4m3_bias8": ("decode_e4m3", _e4m3_bias8),
+    "e4m3_subnormal_as_normal": ("decode_e4m3", _e4m3_subnormal_as_normal),
+    "e4m3_unsigned": ("decode_e4m3", _e4m3_unsigned),
+    "ue8m0_bias128": ("decode_ue8m0", _ue8m0_bias128),
+    "bf16_wrong_shift": ("decode_bf16", _bf16_wrong_shift),
+    "weights_block16": ("dequant_weights", _weights_block16),
+    "weights_block_transposed": ("dequant_weights", _weights_block_transposed),
+    "act_scale_ignored": ("dequant_activations", _act_scale_ignored),
+    "project_no_bias": ("project", _project_no_bias),
+    "project_no_colscale": ("project", _project_no_colscale),
+    "project_column_map": ("project", _project_transposed),
+    "sumsq_mean": ("segment_sumsq", _sumsq_mean),
+    "sumsq_k_includes_v": ("segment_sumsq", _sumsq_k_includes_v),
+    "inv_eps_outside": ("inv_rms", _inv_eps_outside),
+    "inv_heads_only": ("inv_rms", _inv_heads_only),
+    "inv_k_uses_nq": ("inv_rms", _inv_k_uses_nq),
+    "rotate_sign": ("rotate_half", _rotate_sign),
+    "rotate_interleaved": ("rotate_half", _rotate_interleaved),
+    "gamma_after_rope": ("apply_norm_rope", _gamma_after_rope),
+    "cos_sin_swapped": ("apply_norm_rope", _cos_sin_swapped),
+    "gamma_ignored": ("apply_norm_rope", _gamma_ignored),
+    "v_normalised": ("qkv_cte", _v_normalised),
+    "k_uses_gamma_q": ("qkv_cte", _k_uses_gamma_q),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistakes_are_caught(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(O, attr, fn)
+    failed = []
+    for pin in PINS:
+        try:
+            pin()
+        except Exception:  # any failure (assertion, shape error) counts as caught
+            failed.append(pin.__name__)
+    assert failed, f"planted mistake {name} passed every pin"
