@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark: fused QKV context-encoding projection on GB300, one JSON line.
+
+A step is one pass of the whole path through the C ABI (scale-factor prep, the
+tcgen05 MXFP8 GEMM with its fused epilogue, the norm + RoPE pass) over the Wan2.2
+480p self-attention shape: T = 32760 tokens (21x30x52 latent grid), H = 5120,
+40 Q + 40 KV heads of 128 (I = 15360), synthetic seeded inputs. The metric is the
+projection's algorithmic FP8 TFLOP/s (2*T*H*I per step).
+
+Timing: W untimed warm-up steps, then exactly K timed steps, each bracketed by CUDA
+events on the launching stream; L2 is flushed (a 256 MB write) between timed steps,
+outside the events. A barrier and a device synchronise bracket the timed region and
+the step time is the maximum over ranks. Under torchrun each rank runs its own
+replica of the workload (the path has no exchange step on one GPU), so `value` is
+the work of all ranks divided by that time.
+
+`--impl reference` times the float64 CPU oracle, as it stands, on this host's cores
+(rank 0 only), on a bounded row sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused QKV-CTE FP8 TFLOP/s and % of dense FP8 peak at Wan 480p self-attn shape"
+NOMINAL_FP8_TFLOPS = 4500.0        # GB300 dense FP8 tensor peak, nominal
+FP8_PER_BF16 = 2.0                  # nominal dense FP8 / BF16 tensor rate ratio
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="wan480p")
+    p.add_argument("--tile-n", type=int, default=0)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
+    p.add_argument("--cpu-rows", type=int, default=4096, help="oracle row sample for cpu_baseline")
+    p.add_argument("--ref-rows", type=int, default=256, help="oracle row sample per reference step")
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), float(m["bf16_tflops"]), float(m.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 0.0, "fallback"
+
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n)), "threadpoolctl"
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var]), var
+    return os.cpu_count(), "cpu_count (BLAS default: all cores)"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms during the timed region."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) == len(self.FIELDS):
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                 r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def _k1_traffic(workload, tile_n):
+    """DRAM bytes per K1 launch from the committed ncu summary, if it was taken on the
+    current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "k1_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for fn in rec["sources"]:
+            with open(os.path.join(ROOT, fn), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["source_sha256"]:
+            return None
+        if rec.get("workload") != workload or int(rec.get("tile_n", -1)) != tile_n:
+            return None
+        return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: a bounded row sample per step."""
+    import numpy as np
+
+    import workloads as wl
+    from oracle import qkv_cte_oracle as O
+
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    call = wl.workload(args.workload)[0]
+    inp = wl.make_inputs(call)
+    rows = wl.sample_rows(call, args.ref_rows).numpy()
+    flops = 2.0 * len(rows) * call.hidden * call.width
+    for _ in range(args.warmup):
+        O.qkv_cte_from_inputs(call, inp, rows=rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        O.qkv_cte_from_inputs(call, inp, rows=rows)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    cores, how = _blas_threads()
+    sample = (f"{len(rows)} seeded rows of {call.tokens} per step (rows are independent); "
+              f"float64 numpy oracle, BLAS threads via {how}")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(call, 0, flushed=False),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def _config(call, tile_n, flushed=True):
+    return {
+        "workload": (f"{call.name}: Wan2.2-style fused QKV self-attention projection, T={call.tokens} "
+                     f"H={call.hidden} n_q={call.n_q_heads} n_kv={call.n_kv_heads} d_head={call.d_head} "
+                     f"I={call.width}, across-heads Q/K RMSNorm + 3D-grid rotate-half RoPE"),
+        "tokens": call.tokens, "hidden": call.hidden, "width": call.width,
+        "n_q_heads": call.n_q_heads, "n_kv_heads": call.n_kv_heads, "d_head": call.d_head,
+        "tile_n": tile_n,
+        "l2": "flushed between timed steps (256 MB write, outside the step events)" if flushed
+        else "not flushed",
+    }
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import workloads as wl
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_PROFILE, QkvCte
+    from rope_tcgen05_mxfp8_gb300 import build as b
+
+    world, rank, local = _dist()
+    b.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    call = wl.workload(args.workload)[0]
+    inp = wl.make_inputs(call)
+    g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
+                rope=call.rope, eps=call.eps, tile_n=args.tile_n, flags=QKV_CTE_FLAG_PROFILE, device=dev)
+    tile_n = op.desc.tile_n if op.desc.tile_n else 256
+    out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=dev)
+    sumsq = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        op(g["A"], g["a_scale"], g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"],
+           out=out, sumsq=sumsq, stream=stream)
+
+    for _ in range(max(args.warmup, 0)):
+        if not args.no_flush:
+            flush.zero_()
+        step()
+    op.status(stream)
+
+    gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    sampler = ClockSampler(gpu_uuid)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    passes = []
+    barrier()
+    sampler.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        if not args.no_flush:
+            flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        passes.append(op.pass_times())
+    barrier()
+    clocks = sampler.stop()
+    op.status(stream)
+    step_ms = [s.elapsed_time(e) for s, e in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        import torch.distributed as dist
+
+        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops = call.flops
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    prep_ms = statistics.mean(p[0] for p in passes)
+    gemm_ms = statistics.mean(p[1] for p in passes)
+    norm_ms = statistics.mean(p[2] for p in passes)
+    hbm_gbs, bf16, bf16_sus, peak_src = _peaks()
+    fp8_peak = bf16 * FP8_PER_BF16
+    k1_achieved = flops / (gemm_ms * 1e-3) / 1e12
+    # norm + RoPE algorithmic bytes: read + write the Q and K columns (bf16), read the
+    # fp32 cos/sin rows and the fp32 [T, 2] sums of squares
+    qk_cols = (call.n_q_heads + call.n_kv_heads) * call.d_head
+    k2_bytes = 2 * 2 * call.tokens * qk_cols + 2 * 4 * call.tokens * call.d_head + 8 * call.tokens
+    k2_gbs = k2_bytes / (norm_ms * 1e-3) / 1e9 if norm_ms > 0 else None
+
+    e2e = None
+    if not args.no_e2e:
+        A_h = inp["A"].pin_memory()
+        s_h = inp["a_scale"].pin_memory()
+        O_h = torch.empty(call.tokens, call.width, dtype=torch.bfloat16).pin_memory()
+        e2e_ev = []
+        for i in range(args.warmup + args.steps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            if not args.no_flush:
+                flush.zero_()
+            e0.record(stream)
+            g["A"].copy_(A_h, non_blocking=True)
+            g["a_scale"].copy_(s_h, non_blocking=True)
+            step()
+            O_h.copy_(out, non_blocking=True)
+            e1.record(stream)
+            if i >= args.warmup:
+                e2e_ev.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        e2e_ms = sum(a.elapsed_time(b2) for a, b2 in e2e_ev)
+        if world > 1:
+            import torch.distributed as dist
+
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(A_h.numel() * A_h.element_size() + s_h.numel() * s_h.element_size()),
+               "d2h_bytes_per_step": int(O_h.numel() * O_h.element_size()),
+               "ms_per_step": e2e_ms / args.steps,
+               "note": "pinned host A codes + row scales in, full bf16 O out, through the C ABI"}
+        op.status(stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import qkv_cte_oracle as O
+
+        rows = wl.sample_rows(call, args.cpu_rows).numpy()
+        t0 = time.perf_counter()
+        O.qkv_cte_from_inputs(call, inp, rows=rows)
+        dt = time.perf_counter() - t0
+        cores, how = _blas_threads()
+        cpu = {"value": 2.0 * len(rows) * call.hidden * call.width / dt / 1e12, "unit": "TFLOP/s",
+               "cores": cores, "kind": "oracle",
+               "sample": (f"{len(rows)} seeded rows of the {call.tokens}-token workload in one oracle call "
+                          f"({dt:.2f} s; float64 numpy, BLAS threads via {how})")}
+
+    traffic = _k1_traffic(args.workload, tile_n)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; Wan2.2 480p shapes and distributions)",
+        "config": _config(call, tile_n, flushed=not args.no_flush),
+        "pct_nominal_dense_fp8_peak": 100.0 * value / (world * NOMINAL_FP8_TFLOPS),
+        "pct_measured_fp8_peak": 100.0 * value / (world * fp8_peak),
+        "passes_ms": {"prep": prep_ms, "gemm_epilogue": gemm_ms, "norm_rope": norm_ms},
+        "norm_rope": {"GB/s": k2_gbs, "bytes": k2_bytes,
+                      "frac_of_hbm": (k2_gbs / hbm_gbs) if k2_gbs else None, "peak_GB/s": hbm_gbs},
+        "roofline": {"bound": "tensor", "kernel": f"qkv_gemm_mxf8_kernel<{tile_n}>", "achieved": k1_achieved,
+                     "peak": fp8_peak, "unit": "TFLOP/s", "frac": k1_achieved / fp8_peak,
+                     "traffic": traffic,
+                     "peak_source": (f"{peak_src} bf16 burst {bf16:.1f} TFLOP/s x nominal fp8/bf16 ratio "
+                                     f"{FP8_PER_BF16:g}")},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,148 @@
+/*
+ * qkv_cte.h - C ABI of the GB300 (sm_103a) fused QKV context-encoding projection.
+ *
+ * The operation is the one described on the `qkv_cte` kernel reference page
+ * ("Kernel reference: qkv_cte - Wan2.2 additions to the NKI Library QKV CTE MXFP8
+ * projection", vllm-omni-neuron docs, kernels/qkv-cte), cited below as [qkv_cte]
+ * with the page's section headings:
+ *
+ *   O[T, I] = dequant(A_fp8[T, H] @ W_fp8[H, I]) (+ bias),  I = (n_q + 2 n_kv) * d_head
+ *             ([qkv_cte] "Upstream behavior", first bullet; "Interface" argument table)
+ *   Q, K   : across-heads RMSNorm - one RMS per token over the whole Q (or K) segment,
+ *            inv_rms = 1/sqrt(sum(o^2) / (n_heads * d_head) + eps), times a segment-wide
+ *            per-channel gamma ([qkv_cte] "Design" 1, steps a-c), then rotate-half RoPE
+ *            out = y*cos + [-y_hi, y_lo]*sin with position-only cos/sin tables broadcast
+ *            over heads ([qkv_cte] "Design" 2)
+ *   V      : left as projected ([qkv_cte] "Design" 1, step c)
+ *   n_kv_heads == 0: one segment, normalised as Q - the separate Q / K / V calls of
+ *            cross-attention ([qkv_cte] "Design" 5)
+ *
+ * Number formats
+ *   A      : FP8 e4m3 ("fn") codes, one fp32 dequant scale per row (ROW_MX activations).
+ *   W      : FP8 e4m3 codes with one UE8M0 scale (2^(e-127)) per 32 consecutive H
+ *            elements of each output channel (MXFP8 weights).
+ *   bias, gamma : bfloat16 bit patterns. cos/sin : fp32. O : bfloat16 bit patterns,
+ *            round-to-nearest-even. sumsq / inv_rms : fp32.
+ *
+ * Memory and ownership
+ *   Every tensor pointer is a DEVICE pointer owned by the caller; the library never
+ *   frees or keeps it past the call. The plan owns only host-side state. The workspace
+ *   is caller-allocated device memory of the size qkv_cte_plan reports; it holds the
+ *   per-call scratch (repacked weight scales, the sum-of-squares accumulator and a
+ *   device status word) and must not be shared by calls that overlap on the GPU.
+ *   qkv_cte_run is stream-ordered and asynchronous: it never synchronises. Q and K are
+ *   normalised in place in O, so O must not alias any input.
+ *
+ * Errors
+ *   Every entry point returns 0 on success or a negative QKV_CTE_ERR_* code, never
+ *   throws, and records a message readable with qkv_cte_last_error() (thread-local).
+ *   Argument checks happen before any launch: a call that returns an error launched
+ *   nothing. Device-side waits are bounded; a wait that runs out sets the workspace's
+ *   status word and the kernel returns. qkv_cte_status() reports it.
+ */
+#ifndef QKV_CTE_H
+#define QKV_CTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QKV_CTE_ABI_VERSION 1
+
+#define QKV_CTE_OK 0
+#define QKV_CTE_ERR_INVALID (-1)        /* null / inconsistent argument, mode-segment mismatch */
+#define QKV_CTE_ERR_UNSUPPORTED (-2)    /* shape, layout or alignment this build does not take */
+#define QKV_CTE_ERR_CUDA (-3)           /* a CUDA runtime / launch error */
+#define QKV_CTE_ERR_ARCH (-4)           /* current device is not sm_103 */
+#define QKV_CTE_ERR_DEVICE_TIMEOUT (-5) /* a bounded device wait ran out (see qkv_cte_status) */
+
+enum { QKV_CTE_MODE_FUSED = 0, QKV_CTE_MODE_SEPARATE = 1 };
+enum { QKV_CTE_LAYOUT_BSD = 0, QKV_CTE_LAYOUT_NBSD = 1 };
+
+/* Test hook: the GEMM's load warp issues nothing, so every bounded wait downstream
+ * runs out and the kernel exits through its error path (status word set). */
+#define QKV_CTE_FLAG_TEST_STALL 0x1u
+/* Record CUDA events between the launches of each run so qkv_cte_pass_times() can
+ * report per-pass device times. */
+#define QKV_CTE_FLAG_PROFILE 0x2u
+
+/* Problem description ([qkv_cte] "Interface" argument table, flattened to scalars). */
+typedef struct {
+    int64_t tokens;        /* T = B*S rows; 0 is allowed (nothing is launched); <= INT32_MAX */
+    int32_t hidden;        /* H, contraction length; multiple of 128 */
+    int32_t n_q_heads;     /* Q heads in this call (>= 1) */
+    int32_t n_kv_heads;    /* K/V heads; 0 for a single-segment (separate) call */
+    int32_t d_head;        /* head dim; multiple of 16 */
+    int32_t mode;          /* QKV_CTE_MODE_FUSED (n_kv >= 1) or QKV_CTE_MODE_SEPARATE (n_kv == 0) */
+    int32_t norm;          /* 1: across-heads RMSNorm on Q (and K); 0: none */
+    int32_t rope;          /* 1: rotate-half RoPE on Q (and K); needs cos/sin */
+    int32_t output_layout; /* QKV_CTE_LAYOUT_BSD ([T, I]); NBSd is not built yet (-2) */
+    float eps;             /* norm epsilon, >= 0 */
+    uint32_t flags;        /* 0 or QKV_CTE_FLAG_* bits */
+    int32_t tile_n;        /* GEMM N tile: 0 = automatic, else 128, 192, 240 or 256 */
+    int32_t reserved;      /* must be 0 */
+} qkv_cte_desc;
+
+typedef struct qkv_cte_plan_s* qkv_cte_plan_t;
+
+/* Validate `desc` (host only, no CUDA call) and create a plan.
+ * out            : receives the plan (set to NULL on error).
+ * workspace_bytes: receives the device workspace size qkv_cte_run needs.
+ * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values) or
+ * -2 (H % 128, d_head % 16, T > INT32_MAX, NBSd layout, unknown tile_n). */
+int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes);
+
+/* Run the whole path on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *
+ * A          : uint8  [T, H]      e4m3 codes, row-major; 16-byte aligned
+ * a_scale    : fp32   [T]         per-row dequant scale
+ * W          : uint8  [I, H]      e4m3 codes, K-major (row i = output channel i); 16-byte aligned
+ * w_sf       : uint8  [I, H/32]   UE8M0 block scales, row-major; 4-byte aligned
+ * w_col_scale: fp32   [I] or NULL per-output-channel multiplier ("weight_scales"); 16-byte aligned
+ * bias       : bf16   [I] or NULL; 16-byte aligned
+ * gamma_q    : bf16   [n_q*d_head] segment-wide Q gamma; required iff norm; 16-byte aligned
+ * gamma_k    : bf16   [n_kv*d_head] K gamma; required iff norm and n_kv > 0, else NULL
+ * cos_table, sin_table: fp32 [T, d_head] rotate-half tables; required iff rope, else NULL;
+ *              16-byte aligned
+ * O          : bf16   [T, I] (BSD) output; 16-byte aligned; must not alias any input
+ * sumsq      : fp32   [T, 2] or NULL: per-token sum of o^2 over the un-normalised Q and K
+ *              segments ([qkv_cte] "Design" 1 step a; column 1 is 0 when n_kv == 0)
+ * inv_rms    : fp32   [T, 2] or NULL: the rsqrt factors of step b (written iff norm)
+ * workspace  : device scratch of at least the planned size; 256-byte aligned
+ * Returns 0 or -1/-2/-3/-4 (nothing launched on -1/-2/-4). */
+int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, const uint8_t* W,
+                const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias,
+                const uint16_t* gamma_q, const uint16_t* gamma_k, const float* cos_table,
+                const float* sin_table, uint16_t* O, float* sumsq, float* inv_rms,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the device status word in `workspace`.
+ * Each run clears the word before its kernels start, so this reports the most recent
+ * run that used `workspace`. Returns 0, -5 if one of its bounded device waits ran out
+ * (the message names the wait), or -3 on a CUDA error. */
+int qkv_cte_status(void* workspace, void* stream);
+
+/* Device time in milliseconds of each pass of the most recent run of `plan`, which
+ * must have been created with QKV_CTE_FLAG_PROFILE: ms[0] = prep (scale repack and
+ * clears), ms[1] = GEMM with its fused epilogue, ms[2] = norm + RoPE (0 when the call
+ * has neither). Blocks until that run has finished. Returns 0, -1 (no flag, never run,
+ * null pointer) or -3. */
+int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms);
+
+/* Release a plan. NULL is a no-op. */
+void qkv_cte_destroy(qkv_cte_plan_t plan);
+
+/* Message for the last non-zero return on this thread ("" if none). */
+const char* qkv_cte_last_error(void);
+
+/* QKV_CTE_ABI_VERSION of the loaded library. */
+int qkv_cte_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKV_CTE_H */

@@ -1,0 +1,127 @@
+// Kernel K2: in-place across-heads RMSNorm apply + rotate-half RoPE over the Q and K
+// columns of O; V is never read.
+//
+// Follows the `qkv_cte` kernel reference page, "Design" 1 (steps b and c: finish
+// inv_rms = 1/sqrt(sum(o^2) / (n_heads * d_head) + eps) per token and segment, re-read
+// each token's Q and K, multiply by the segment-wide gamma) and "Design" 2 (RoPE in
+// the same pass, inv_rms folded into it, out = y*cos + [-y_hi, y_lo]*sin with
+// position-only cos/sin broadcast over the heads).
+//
+// On one GPU every head is local, so the page's cross-rank AllReduce of the sums is
+// the identity: K1 already summed over every column tile of the row. This pass is
+// HBM-bound: each thread moves two 16-byte vectors of O (8 lanes of the low half of
+// a head and the 8 partner lanes d/2 away), with the per-position cos/sin and the
+// gamma vectors served from L1/L2.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace qkvcte {
+
+namespace {
+
+__device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+    w[j] = *reinterpret_cast<uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__global__ void __launch_bounds__(256) qk_norm_rope_kernel(const NormRopeArgs p) {
+  const int chunks = p.d_head / 16;  // 8-lane chunks in the low half of one head
+  const int half = p.d_head / 2;
+  const long long per_row = static_cast<long long>(p.n_q + p.n_kv) * chunks;
+  const long long total = static_cast<long long>(p.T) * per_row;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long it = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; it < total;
+       it += stride) {
+    const int t = static_cast<int>(it / per_row);
+    const int rem = static_cast<int>(it - static_cast<long long>(t) * per_row);
+    const int hg = rem / chunks;
+    const int c = rem - hg * chunks;
+    const int seg = hg >= p.n_q ? 1 : 0;
+    const int h = seg ? hg - p.n_q : hg;
+    const int n_heads = seg ? p.n_kv : p.n_q;
+    const int off = h * p.d_head + c * 8;  // column inside the segment
+    uint16_t* row = p.O + static_cast<size_t>(t) * p.I + (seg ? p.n_q * p.d_head : 0);
+
+    float lo[8], hi[8];
+    unpack8(*reinterpret_cast<const uint4*>(row + off), lo);
+    unpack8(*reinterpret_cast<const uint4*>(row + off + half), hi);
+
+    float inv = 1.0f;
+    if (p.norm) {
+      const float ss = p.sumsq[2 * static_cast<size_t>(t) + seg];
+      inv = 1.0f / sqrtf(ss / static_cast<float>(n_heads * p.d_head) + p.eps);
+      const uint16_t* gamma = seg ? p.gamma_k : p.gamma_q;
+      float glo[8], ghi[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off)), glo);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off + half)), ghi);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        lo[j] = lo[j] * inv * glo[j];
+        hi[j] = hi[j] * inv * ghi[j];
+      }
+      if (p.inv_rms != nullptr && h == 0 && c == 0) {
+        p.inv_rms[2 * static_cast<size_t>(t) + seg] = inv;
+        if (p.n_kv == 0) p.inv_rms[2 * static_cast<size_t>(t) + 1] = 0.0f;
+      }
+    }
+    if (p.rope) {
+      const float* cr = p.cos_t + static_cast<size_t>(t) * p.d_head + c * 8;
+      const float* sr = p.sin_t + static_cast<size_t>(t) * p.d_head + c * 8;
+      float cl[8], ch[8], sl[8], sh[8];
+      load8f(cr, cl);
+      load8f(cr + half, ch);
+      load8f(sr, sl);
+      load8f(sr + half, sh);
+      float olo[8], ohi[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        olo[j] = lo[j] * cl[j] - hi[j] * sl[j];
+        ohi[j] = hi[j] * ch[j] + lo[j] * sh[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        lo[j] = olo[j];
+        hi[j] = ohi[j];
+      }
+    }
+    *reinterpret_cast<uint4*>(row + off) = pack8(lo);
+    *reinterpret_cast<uint4*>(row + off + half) = pack8(hi);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms) {
+  if (!a.norm && !a.rope) return cudaSuccess;
+  const long long total = static_cast<long long>(a.T) * (a.n_q + a.n_kv) * (a.d_head / 16);
+  if (total == 0) return cudaSuccess;
+  long long blocks = (total + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms) * 8;
+  if (blocks > cap) blocks = cap;
+  qk_norm_rope_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace qkvcte

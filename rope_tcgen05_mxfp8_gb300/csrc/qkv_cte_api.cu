@@ -1,0 +1,324 @@
+// C-ABI front end: plan validation, workspace layout, TMA descriptors and the launch
+// sequence prep -> K1 (GEMM + epilogue) -> K2 (norm + RoPE) on the caller's stream.
+// The argument set follows the `qkv_cte` kernel reference page's "Interface" table,
+// with the differences listed in qkv_cte.h.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+#include "qkv_cte.h"
+
+using namespace qkvcte;
+
+struct qkv_cte_plan_s {
+  qkv_cte_desc d;
+  GemmShape g;
+  WorkspaceLayout ws;
+  int q_end, k_end;
+  // QKV_CTE_FLAG_PROFILE: events around the three launches of the latest run
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  int ev_device = -1;
+  bool ran = false;
+  bool has_norm_pass = false;
+};
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_last_error[0] = '\0';
+  return QKV_CTE_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct DeviceInfo {
+  bool init = false;
+  int major = 0, minor = 0, sms = 0;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+int device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(QKV_CTE_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return fail(QKV_CTE_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    d.init = true;
+  }
+  *out = d;
+  return QKV_CTE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D K-major uint8 operand [rows, cols], tiles of box_rows x 128 bytes, 128-byte swizzle.
+int encode_operand(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                   const char* what) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return fail(QKV_CTE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QKV_CTE_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, int(r));
+  return QKV_CTE_OK;
+}
+
+int choose_tile_n(const qkv_cte_desc& d, int I) {
+  if (d.tile_n != 0) return d.tile_n;
+  (void)I;
+  return 256;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qkv_cte_version(void) { return QKV_CTE_ABI_VERSION; }
+
+const char* qkv_cte_last_error(void) { return g_last_error; }
+
+int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes) {
+  if (out == nullptr || desc == nullptr || workspace_bytes == nullptr)
+    return fail(QKV_CTE_ERR_INVALID, "qkv_cte_plan: null argument");
+  *out = nullptr;
+  const qkv_cte_desc& d = *desc;
+  if (d.tokens < 0) return fail(QKV_CTE_ERR_INVALID, "tokens must be >= 0 (got %lld)", (long long)d.tokens);
+  if (d.tokens > INT32_MAX) return fail(QKV_CTE_ERR_UNSUPPORTED, "tokens > INT32_MAX");
+  if (d.hidden <= 0) return fail(QKV_CTE_ERR_INVALID, "hidden must be > 0");
+  if (d.hidden % 128 != 0) return fail(QKV_CTE_ERR_UNSUPPORTED, "hidden %d is not a multiple of 128", d.hidden);
+  if (d.n_q_heads < 1) return fail(QKV_CTE_ERR_INVALID, "n_q_heads must be >= 1");
+  if (d.n_kv_heads < 0) return fail(QKV_CTE_ERR_INVALID, "n_kv_heads must be >= 0");
+  if (d.d_head <= 0) return fail(QKV_CTE_ERR_INVALID, "d_head must be > 0");
+  if (d.d_head % 16 != 0) return fail(QKV_CTE_ERR_UNSUPPORTED, "d_head %d is not a multiple of 16", d.d_head);
+  if (d.mode == QKV_CTE_MODE_FUSED) {
+    if (d.n_kv_heads < 1) return fail(QKV_CTE_ERR_INVALID, "fused mode needs n_kv_heads >= 1");
+  } else if (d.mode == QKV_CTE_MODE_SEPARATE) {
+    if (d.n_kv_heads != 0) return fail(QKV_CTE_ERR_INVALID, "separate mode needs n_kv_heads == 0");
+  } else {
+    return fail(QKV_CTE_ERR_INVALID, "unknown mode %d", d.mode);
+  }
+  if (d.norm != 0 && d.norm != 1) return fail(QKV_CTE_ERR_INVALID, "norm must be 0 or 1");
+  if (d.rope != 0 && d.rope != 1) return fail(QKV_CTE_ERR_INVALID, "rope must be 0 or 1");
+  if (!(d.eps >= 0.0f) || d.eps > 1e30f) return fail(QKV_CTE_ERR_INVALID, "eps must be finite and >= 0");
+  if (d.output_layout == QKV_CTE_LAYOUT_NBSD)
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "NBSd output layout is not built in this version");
+  if (d.output_layout != QKV_CTE_LAYOUT_BSD) return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
+  if ((d.flags & ~(QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE)) != 0)
+    return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
+  if (d.reserved != 0) return fail(QKV_CTE_ERR_INVALID, "reserved must be 0");
+  const long long I = (long long)(d.n_q_heads + 2LL * d.n_kv_heads) * d.d_head;
+  if (I > INT32_MAX / 2) return fail(QKV_CTE_ERR_UNSUPPORTED, "output width too large");
+  const int tile_n = choose_tile_n(d, (int)I);
+  if (!gemm_tile_supported(tile_n)) return fail(QKV_CTE_ERR_UNSUPPORTED, "tile_n %d not built", tile_n);
+
+  qkv_cte_plan_s* p = new (std::nothrow) qkv_cte_plan_s();
+  if (p == nullptr) return fail(QKV_CTE_ERR_INVALID, "out of host memory");
+  p->d = d;
+  GemmShape& g = p->g;
+  g.T = (int)d.tokens;
+  g.H = d.hidden;
+  g.I = (int)I;
+  g.tile_n = tile_n;
+  g.m_tiles = (g.T + 127) / 128;
+  g.n_tiles = (g.I + tile_n - 1) / tile_n;
+  g.k_stages = g.H / 128;
+  g.sf_chunks = gemm_sf_chunks(tile_n);
+  p->q_end = d.n_q_heads * d.d_head;
+  p->k_end = p->q_end + d.n_kv_heads * d.d_head;
+  WorkspaceLayout& w = p->ws;
+  w.status_off = 0;
+  w.sumsq_off = 256;
+  w.sf_off = w.sumsq_off + align_up((size_t)g.T * 2 * sizeof(float), 256);
+  w.total = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
+  *workspace_bytes = w.total;
+  *out = p;
+  return ok();
+}
+
+void qkv_cte_destroy(qkv_cte_plan_t plan) {
+  if (plan == nullptr) return;
+  for (cudaEvent_t e : plan->ev)
+    if (e != nullptr) cudaEventDestroy(e);
+  delete plan;
+}
+
+int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms) {
+  if (plan == nullptr || ms == nullptr) return fail(QKV_CTE_ERR_INVALID, "null argument");
+  if (!(plan->d.flags & QKV_CTE_FLAG_PROFILE)) return fail(QKV_CTE_ERR_INVALID, "plan made without QKV_CTE_FLAG_PROFILE");
+  if (!plan->ran) return fail(QKV_CTE_ERR_INVALID, "plan has not run");
+  cudaError_t e = cudaEventSynchronize(plan->ev[3]);
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&ms[i], plan->ev[i], plan->ev[i + 1]);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "pass times: %s", cudaGetErrorString(e));
+  if (!plan->has_norm_pass) ms[2] = 0.0f;
+  return ok();
+}
+
+int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, const uint8_t* W,
+                const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias, const uint16_t* gamma_q,
+                const uint16_t* gamma_k, const float* cos_table, const float* sin_table, uint16_t* O,
+                float* sumsq, float* inv_rms, void* workspace, size_t workspace_bytes, void* stream) {
+  if (plan == nullptr) return fail(QKV_CTE_ERR_INVALID, "null plan");
+  const qkv_cte_desc& d = plan->d;
+  const GemmShape& g = plan->g;
+  if (!A || !a_scale || !W || !w_sf || !O || !workspace)
+    return fail(QKV_CTE_ERR_INVALID, "A, a_scale, W, w_sf, O and workspace are required");
+  if (d.norm && !gamma_q) return fail(QKV_CTE_ERR_INVALID, "norm needs gamma_q");
+  if (d.norm && d.n_kv_heads > 0 && !gamma_k) return fail(QKV_CTE_ERR_INVALID, "norm with a K segment needs gamma_k");
+  if (gamma_k && !(d.norm && d.n_kv_heads > 0))
+    return fail(QKV_CTE_ERR_INVALID, "gamma_k given but the call has no normalised K segment");
+  if (gamma_q && !d.norm) return fail(QKV_CTE_ERR_INVALID, "gamma_q given but norm is off");
+  if (d.rope && (!cos_table || !sin_table)) return fail(QKV_CTE_ERR_INVALID, "rope needs cos and sin tables");
+  if (!d.rope && (cos_table || sin_table)) return fail(QKV_CTE_ERR_INVALID, "cos/sin given but rope is off");
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(O, 16))
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "A, W and O must be 16-byte aligned");
+  if (!aligned(a_scale, 4) || !aligned(w_sf, 4) || (sumsq && !aligned(sumsq, 4)) || (inv_rms && !aligned(inv_rms, 4)))
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "a_scale, w_sf, sumsq and inv_rms must be 4-byte aligned");
+  if ((w_col_scale && !aligned(w_col_scale, 16)) || (bias && !aligned(bias, 16)) ||
+      (gamma_q && !aligned(gamma_q, 16)) || (gamma_k && !aligned(gamma_k, 16)) ||
+      (cos_table && !aligned(cos_table, 16)) || (sin_table && !aligned(sin_table, 16)))
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "w_col_scale, bias, gamma and cos/sin must be 16-byte aligned");
+  if (!aligned(workspace, 256)) return fail(QKV_CTE_ERR_UNSUPPORTED, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan->ws.total)
+    return fail(QKV_CTE_ERR_INVALID, "workspace of %zu bytes is smaller than the planned %zu",
+                workspace_bytes, plan->ws.total);
+  if (g.T == 0) return ok();
+
+  DeviceInfo dev;
+  int rc = device_info(&dev);
+  if (rc != QKV_CTE_OK) return rc;
+  if (!(dev.major == 10 && dev.minor == 3))
+    return fail(QKV_CTE_ERR_ARCH, "device is sm_%d%d; this library is built for sm_103a", dev.major, dev.minor);
+
+  CUtensorMap tmA, tmW;
+  if ((rc = encode_operand(&tmA, A, (uint64_t)g.T, (uint64_t)g.H, 128u, "A")) != QKV_CTE_OK) return rc;
+  if ((rc = encode_operand(&tmW, W, (uint64_t)g.I, (uint64_t)g.H, (uint32_t)g.tile_n, "W")) != QKV_CTE_OK) return rc;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws + plan->ws.status_off);
+  const bool need_ss = d.norm || sumsq != nullptr;
+  float* ss = sumsq ? sumsq : reinterpret_cast<float*>(ws + plan->ws.sumsq_off);
+  uint8_t* sf_packed = ws + plan->ws.sf_off;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool prof = (d.flags & QKV_CTE_FLAG_PROFILE) != 0;
+  cudaError_t e = cudaSuccess;
+  if (prof) {
+    int cur = 0;
+    cudaGetDevice(&cur);
+    if (plan->ev[0] != nullptr && plan->ev_device != cur)
+      return fail(QKV_CTE_ERR_INVALID, "a profiled plan must stay on one device");
+    for (int i = 0; i < 4 && plan->ev[i] == nullptr; ++i)
+      if ((e = cudaEventCreate(&plan->ev[i])) != cudaSuccess)
+        return fail(QKV_CTE_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
+    plan->ev_device = cur;
+    if ((e = cudaEventRecord(plan->ev[0], s)) != cudaSuccess)
+      return fail(QKV_CTE_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
+  }
+
+  e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0,
+                              status, s, dev.sms);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
+  if (prof) cudaEventRecord(plan->ev[1], s);
+
+  GemmArgs ga;
+  ga.a_scale = a_scale;
+  ga.w_col_scale = w_col_scale;
+  ga.bias = bias;
+  ga.sf_packed = sf_packed;
+  ga.O = O;
+  ga.sumsq = need_ss ? ss : nullptr;
+  ga.status = status;
+  ga.q_end = plan->q_end;
+  ga.k_end = plan->k_end;
+  ga.flags = d.flags;
+  e = launch_gemm(g, tmA, tmW, ga, s, dev.sms);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+  if (prof) cudaEventRecord(plan->ev[2], s);
+
+  NormRopeArgs na;
+  na.T = g.T;
+  na.I = g.I;
+  na.n_q = d.n_q_heads;
+  na.n_kv = d.n_kv_heads;
+  na.d_head = d.d_head;
+  na.norm = d.norm;
+  na.rope = d.rope;
+  na.eps = d.eps;
+  na.sumsq = ss;
+  na.gamma_q = gamma_q;
+  na.gamma_k = gamma_k;
+  na.cos_t = cos_table;
+  na.sin_t = sin_table;
+  na.O = O;
+  na.inv_rms = inv_rms;
+  e = launch_norm_rope(na, s, dev.sms);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "norm/rope launch: %s", cudaGetErrorString(e));
+  if (prof) {
+    cudaEventRecord(plan->ev[3], s);
+    plan->ran = true;
+    plan->has_norm_pass = d.norm || d.rope;
+  }
+  return ok();
+}
+
+int qkv_cte_status(void* workspace, void* stream) {
+  if (workspace == nullptr) return fail(QKV_CTE_ERR_INVALID, "null workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (word == 0) return ok();
+  const uint32_t zero = 0;
+  e = cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+  return fail(QKV_CTE_ERR_DEVICE_TIMEOUT,
+              "device wait ran out (status 0x%x:%s%s%s%s%s)", word,
+              (word & kErrProducerEmptyWait) ? " load-stage-free" : "",
+              (word & kErrMmaFullWait) ? " mma-operands-ready" : "",
+              (word & kErrMmaTmemEmptyWait) ? " mma-accumulator-free" : "",
+              (word & kErrEpilogueTmemFullWait) ? " epilogue-accumulator-ready" : "",
+              (word & kErrDrainWait) ? " drain" : "");
+}
+
+}  // extern "C"

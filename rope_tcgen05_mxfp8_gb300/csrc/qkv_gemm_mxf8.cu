@@ -1,0 +1,432 @@
+// Kernel K1: O = dequant(A_fp8 @ W_fp8^T) * a_scale[t] * w_col_scale[i] + bias[i] -> bf16,
+// plus the per-token sum of o^2 over the Q and the K columns.
+//
+// Follows the `qkv_cte` kernel reference page: the projection O[S, I] = A[S, H] @ W[H, I]
+// (+ bias) ("Upstream behavior"), dequantised, bias-added and stored as each output
+// tile leaves the accumulator, with the across-heads norm's step a (a per-token
+// sum(x^2) over the whole Q segment and K segment of the un-normalised output,
+// "Design" 1) folded into that same copy-out.
+//
+// GB300 design (not the page's Trainium schedule):
+//   * persistent grid, one CTA per SM, tiles of 128 rows x tile_n columns, walked
+//     row-panel-major so W (a few tens of MB) stays resident in L2 while A streams;
+//   * warp 0: TMA producer. Per K stage it loads a 128x128-byte A tile and a
+//     tile_n x 128-byte W tile (128-byte swizzle) plus the stage's repacked UE8M0
+//     block scales, all counted on one mbarrier;
+//   * warp 1: one thread issues tcgen05.cp for the block scales and four
+//     tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each, one UE8M0 scale per row of
+//     B per MMA, selected by the scale-factor byte id) into a TMEM fp32 accumulator;
+//   * warps 2-5: epilogue. tcgen05.ld the accumulator (one TMEM lane = one row per
+//     thread), apply the row scale / column scale / bias, store bf16, accumulate the
+//     Q and K sums of squares in fp32 and add them to sumsq[T, 2] with one atomic per
+//     row and segment. With two accumulator stages the epilogue of tile j overlaps
+//     the MMAs of tile j+1.
+//   * A carries no MX scale of its own (its only scale is the fp32 row scale), so the
+//     A-side scale factors are the constant 2^0 (UE8M0 127), copied to TMEM once.
+// Every mbarrier wait is bounded; a wait that runs out records its role in the
+// status word and the CTA unwinds, waiting for its own copies and MMAs before it
+// releases TMEM.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace qkvcte {
+
+namespace {
+
+constexpr int kBM = 128;       // rows per tile (the MMA's M)
+constexpr int kBK = 128;       // K elements (bytes of e4m3) per pipeline stage
+constexpr int kThreads = 192;  // producer warp, MMA warp, 4 epilogue warps
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kFlagTestStall = 0x1u;
+
+template <int BN>
+struct K1Cfg {
+  static constexpr int SF_CHUNKS = (BN + 127) / 128;
+  static constexpr int A_BYTES = kBM * kBK;
+  static constexpr int B_BYTES = BN * kBK;
+  static constexpr int SFB_BYTES = SF_CHUNKS * 512;
+  static constexpr int SFB_COLS = SF_CHUNKS * 4;
+  static constexpr int ACC_STAGES = (2 * BN + 4 + SFB_COLS <= 512) ? 2 : 1;
+  static constexpr int SFA_COL = ACC_STAGES * BN;
+  static constexpr int SFB_COL = SFA_COL + 4;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFB_BYTES;
+  static constexpr int SMEM_LIMIT = 232448;          // 227 KB opt-in per block
+  static constexpr int FIXED = 1024 + 512 + 256;      // alignment slack, A scales, barriers
+  static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr size_t SMEM = FIXED + static_cast<size_t>(STAGES) * STAGE_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is a multiple of 16 up to 256");
+  static_assert(SFB_COL + SFB_COLS <= 512, "TMEM columns");
+  static_assert(STAGES >= 2, "pipeline depth");
+  static_assert(B_BYTES % 1024 == 0, "swizzle atoms");
+};
+
+__device__ __forceinline__ void record_failure(uint32_t* status, volatile int* abort_flag, uint32_t code) {
+  atomicOr(status, code);
+  *abort_flag = 1;
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
+  return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    qkv_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
+                         const GemmShape g, const GemmArgs a) {
+  using C = K1Cfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + C::STAGES * C::A_BYTES;
+  uint8_t* sSFB = sB + C::STAGES * C::B_BYTES;
+  uint8_t* sSFA = sSFB + C::STAGES * C::SFB_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sSFA + 512);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&tfull[s]), 1);
+      mbar_init(smem_u32(&tempty[s]), 4);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp >= 2) {
+    // A-side block scales: UE8M0 127 (= 1.0) for every row and K block.
+    reinterpret_cast<uint32_t*>(sSFA)[threadIdx.x - 64] = 0x7F7F7F7Fu;
+    fence_proxy_async_smem();
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = g.m_tiles * g.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = (a.flags & kFlagTestStall) == 0;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int m_blk = tile / g.n_tiles;
+        const int n_blk = tile - m_blk * g.n_tiles;
+        for (int kb = 0; kb < g.k_stages; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
+            record_failure(a.status, abort_flag, kErrProducerEmptyWait);
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * kBK, m_blk * kBM, fb, pol_stream);
+          tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmW, kb * kBK, n_blk * BN, fb, pol_keep);
+          bulk_load(smem_u32(sSFB + stage * C::SFB_BYTES),
+                    a.sf_packed + (static_cast<size_t>(n_blk) * g.k_stages + kb) * C::SFB_BYTES,
+                    C::SFB_BYTES, fb);
+          ++issued;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Do not leave while our own copies may still be landing in shared memory:
+      // wait for the (at most STAGES) most recent loads.
+      const int pending = issued < C::STAGES ? issued : C::STAGES;
+      int s = stage;
+      uint32_t ph = phase;
+      for (int i = 0; i < pending; ++i) {
+        if (s == 0) {
+          s = C::STAGES - 1;
+          ph ^= 1u;
+        } else {
+          --s;
+        }
+        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, nullptr, kWaitLimitNs)) {
+          record_failure(a.status, abort_flag, kErrDrainWait);
+          break;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      const uint32_t idesc = idesc_mxf8_e4m3(kBM, BN);
+      const uint32_t sfa_t = tmem_base + C::SFA_COL;
+      const uint32_t sfb_t = tmem_base + C::SFB_COL;
+      tc_copy_32x128b_x4(sfa_t, smem_desc_plain(smem_u32(sSFA)));
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
+          record_failure(a.status, abort_flag, kErrMmaTmemEmptyWait);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < g.k_stages; ++kb) {
+          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
+            record_failure(a.status, abort_flag, kErrMmaFullWait);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sf_smem = smem_u32(sSFB + stage * C::SFB_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::SF_CHUNKS; ++c)
+            tc_copy_32x128b_x4(sfb_t + 4 * c, smem_desc_plain(sf_smem + 512 * c));
+          const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
+          const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k) {
+            // +32 bytes along K inside the swizzle atom = +2 in the 16-byte address field
+            mma_mxf8(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t,
+                     (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(smem_u32(&empty[stage]));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(smem_u32(&tfull[acc]));
+        if (++acc == C::ACC_STAGES) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      // Every tcgen05 operation issued above completes before TMEM is released.
+      tc_commit(smem_u32(drain));
+      if (!mbar_wait_bounded(smem_u32(drain), 0, nullptr, kWaitLimitNs))
+        record_failure(a.status, abort_flag, kErrDrainWait);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row_local = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m_blk = tile / g.n_tiles;
+      const int n_blk = tile - m_blk * g.n_tiles;
+      bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) record_failure(a.status, abort_flag, kErrEpilogueTmemFullWait);
+        break;
+      }
+      tc_fence_after();
+      const int row = m_blk * kBM + row_local;
+      const bool row_ok = row < g.T;
+      const float ascale = row_ok ? a.a_scale[row] : 0.0f;
+      const int col_base = n_blk * BN;
+      uint16_t* orow = a.O + static_cast<size_t>(row_ok ? row : 0) * g.I;
+      float ss_q = 0.0f, ss_k = 0.0f;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(t_lane + static_cast<uint32_t>(acc * BN + c0), r);
+        tmem_ld_wait();
+        const int col0 = col_base + c0;
+        if (col0 >= g.I) continue;  // ragged last N tile (uniform across the warp)
+        float cs[16];
+        if (a.w_col_scale != nullptr) {
+          const float4* p = reinterpret_cast<const float4*>(a.w_col_scale + col0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 v = __ldg(p + q);
+            cs[4 * q + 0] = v.x;
+            cs[4 * q + 1] = v.y;
+            cs[4 * q + 2] = v.z;
+            cs[4 * q + 3] = v.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) cs[j] = 1.0f;
+        }
+        float bias[16];
+        if (a.bias != nullptr) {
+          const uint4* p = reinterpret_cast<const uint4*>(a.bias + col0);
+          const uint4 b0 = __ldg(p), b1 = __ldg(p + 1);
+          const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            bias[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
+            bias[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) bias[j] = 0.0f;
+        }
+        uint32_t packed[8];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+          const float v0 = __uint_as_float(r[j]) * ascale * cs[j] + bias[j];
+          const float v1 = __uint_as_float(r[j + 1]) * ascale * cs[j + 1] + bias[j + 1];
+          const int c = col0 + j;
+          if (c < a.q_end) ss_q += v0 * v0; else if (c < a.k_end) ss_k += v0 * v0;
+          if (c + 1 < a.q_end) ss_q += v1 * v1; else if (c + 1 < a.k_end) ss_k += v1 * v1;
+          packed[j / 2] = pack_bf16x2(v0, v1);
+        }
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + col0);
+          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+      if (row_ok && a.sumsq != nullptr) {
+        if (col_base < a.q_end) atomicAdd(&a.sumsq[2 * static_cast<size_t>(row)], ss_q);
+        if (col_base + BN > a.q_end && col_base < a.k_end)
+          atomicAdd(&a.sumsq[2 * static_cast<size_t>(row) + 1], ss_k);
+      }
+      if (++acc == C::ACC_STAGES) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// Repack W's UE8M0 scales [I, H/32] into, per (N tile, K stage), SF_CHUNKS blocks of
+// 512 bytes: byte 16*r + 4*c + kb of block `chunk` is the scale of output column
+// n = tile*tile_n + 128*chunk + 32*c + r for K block 4*stage + kb. That is the
+// 32-row x 16-byte shared-memory image tcgen05.cp 32x128b.warpx4 turns into the
+// TMEM scale-factor layout of an M=128 block-scaled MMA. Columns past I (or past
+// the tile) get 127. Also clears the status word and the sum-of-squares buffer.
+__global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __restrict__ packed, int I,
+                                int k_blocks, int tile_n, int n_tiles, int k_stages, int sf_chunks,
+                                float* __restrict__ sumsq, size_t sumsq_count, uint32_t* status) {
+  const size_t words = static_cast<size_t>(n_tiles) * k_stages * sf_chunks * 128;
+  const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
+  const size_t first = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (size_t w = first; w < words; w += stride) {
+    const int within = static_cast<int>(w & 127);
+    const int r = within >> 2;
+    const int c = within & 3;
+    size_t rest = w >> 7;
+    const int chunk = static_cast<int>(rest % sf_chunks);
+    rest /= sf_chunks;
+    const int kst = static_cast<int>(rest % k_stages);
+    const int nt = static_cast<int>(rest / k_stages);
+    const int n_local = chunk * 128 + c * 32 + r;
+    const int n = nt * tile_n + n_local;
+    uint32_t v = 0x7F7F7F7Fu;
+    if (n_local < tile_n && n < I)
+      v = __ldg(reinterpret_cast<const uint32_t*>(w_sf + static_cast<size_t>(n) * k_blocks + kst * 4));
+    packed[w] = v;
+  }
+  for (size_t i = first; i < sumsq_count; i += stride) sumsq[i] = 0.0f;
+  if (first == 0 && status != nullptr) *status = 0u;
+}
+
+template <int BN>
+cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                          const GemmArgs& a, cudaStream_t s, int num_sms) {
+  using C = K1Cfg<BN>;
+  auto kern = qkv_gemm_mxf8_kernel<BN>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(C::SMEM));
+  if (e != cudaSuccess) return e;
+  const int tiles = g.m_tiles * g.n_tiles;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  kern<<<grid, kThreads, C::SMEM, s>>>(tmA, tmW, g, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool gemm_tile_supported(int tile_n) {
+  return tile_n == 128 || tile_n == 192 || tile_n == 240 || tile_n == 256;
+}
+
+int gemm_sf_chunks(int tile_n) { return (tile_n + 127) / 128; }
+
+size_t gemm_smem_bytes(int tile_n) {
+  switch (tile_n) {
+    case 128: return K1Cfg<128>::SMEM;
+    case 192: return K1Cfg<192>::SMEM;
+    case 240: return K1Cfg<240>::SMEM;
+    case 256: return K1Cfg<256>::SMEM;
+    default: return 0;
+  }
+}
+
+cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
+                        size_t sumsq_count, uint32_t* status, cudaStream_t s, int num_sms) {
+  const size_t words = static_cast<size_t>(g.n_tiles) * g.k_stages * g.sf_chunks * 128;
+  const size_t work = words > sumsq_count ? words : sumsq_count;
+  size_t blocks = (work + 255) / 256;
+  const size_t cap = static_cast<size_t>(num_sms) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks == 0) blocks = 1;
+  qkv_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+      w_sf, reinterpret_cast<uint32_t*>(sf_packed), g.I, g.H / 32, g.tile_n, g.n_tiles, g.k_stages,
+      g.sf_chunks, sumsq, sumsq_count, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                        const GemmArgs& a, cudaStream_t s, int num_sms) {
+  switch (g.tile_n) {
+    case 128: return launch_gemm_t<128>(g, tmA, tmW, a, s, num_sms);
+    case 192: return launch_gemm_t<192>(g, tmA, tmW, a, s, num_sms);
+    case 240: return launch_gemm_t<240>(g, tmA, tmW, a, s, num_sms);
+    case 256: return launch_gemm_t<256>(g, tmA, tmW, a, s, num_sms);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace qkvcte

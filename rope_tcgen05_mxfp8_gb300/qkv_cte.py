@@ -1,0 +1,222 @@
+"""Thin ctypes binding over libqkvcte.so (argument marshalling only).
+
+Each function has the name of the C entry point it calls (see include/qkv_cte.h).
+Tensors are torch CUDA tensors used as device memory; every step of the
+computation runs in the library's CUDA kernels. If the library has not been built
+the first call raises: there is no other implementation to fall back on.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqkvcte.so")
+
+QKV_CTE_OK = 0
+QKV_CTE_ERR_INVALID = -1
+QKV_CTE_ERR_UNSUPPORTED = -2
+QKV_CTE_ERR_CUDA = -3
+QKV_CTE_ERR_ARCH = -4
+QKV_CTE_ERR_DEVICE_TIMEOUT = -5
+QKV_CTE_MODE_FUSED = 0
+QKV_CTE_MODE_SEPARATE = 1
+QKV_CTE_LAYOUT_BSD = 0
+QKV_CTE_LAYOUT_NBSD = 1
+QKV_CTE_FLAG_TEST_STALL = 0x1
+QKV_CTE_FLAG_PROFILE = 0x2
+
+EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
+            "qkv_cte_last_error", "qkv_cte_version")
+
+
+class qkv_cte_desc(ctypes.Structure):
+    _fields_ = [
+        ("tokens", ctypes.c_int64),
+        ("hidden", ctypes.c_int32),
+        ("n_q_heads", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("d_head", ctypes.c_int32),
+        ("mode", ctypes.c_int32),
+        ("norm", ctypes.c_int32),
+        ("rope", ctypes.c_int32),
+        ("output_layout", ctypes.c_int32),
+        ("eps", ctypes.c_float),
+        ("flags", ctypes.c_uint32),
+        ("tile_n", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+class QkvCteError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"qkv_cte error {code}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libqkvcte.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    lib.qkv_cte_plan.argtypes = [ctypes.POINTER(P), ctypes.POINTER(qkv_cte_desc), ctypes.POINTER(ctypes.c_size_t)]
+    lib.qkv_cte_plan.restype = ctypes.c_int
+    lib.qkv_cte_run.argtypes = [P] * 15 + [ctypes.c_size_t, P]
+    lib.qkv_cte_run.restype = ctypes.c_int
+    lib.qkv_cte_status.argtypes = [P, P]
+    lib.qkv_cte_status.restype = ctypes.c_int
+    lib.qkv_cte_pass_times.argtypes = [P, ctypes.POINTER(ctypes.c_float)]
+    lib.qkv_cte_pass_times.restype = ctypes.c_int
+    lib.qkv_cte_destroy.argtypes = [P]
+    lib.qkv_cte_destroy.restype = None
+    lib.qkv_cte_last_error.argtypes = []
+    lib.qkv_cte_last_error.restype = ctypes.c_char_p
+    lib.qkv_cte_version.argtypes = []
+    lib.qkv_cte_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def qkv_cte_last_error() -> str:
+    return load().qkv_cte_last_error().decode()
+
+
+def qkv_cte_version() -> int:
+    return load().qkv_cte_version()
+
+
+def _check(rc: int) -> int:
+    if rc != QKV_CTE_OK:
+        raise QkvCteError(rc, qkv_cte_last_error())
+    return rc
+
+
+def make_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=1, rope=1, eps=1e-6,
+              mode=None, output_layout=QKV_CTE_LAYOUT_BSD, flags=0, tile_n=0) -> qkv_cte_desc:
+    if mode is None:
+        mode = QKV_CTE_MODE_FUSED if n_kv_heads > 0 else QKV_CTE_MODE_SEPARATE
+    return qkv_cte_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, mode, norm, rope, output_layout,
+                        eps, flags, tile_n, 0)
+
+
+def qkv_cte_plan(desc: qkv_cte_desc):
+    """Returns (plan handle, workspace bytes); raises QkvCteError on a rejected desc."""
+    plan = ctypes.c_void_p()
+    ws = ctypes.c_size_t()
+    _check(load().qkv_cte_plan(ctypes.byref(plan), ctypes.byref(desc), ctypes.byref(ws)))
+    return plan, ws.value
+
+
+def qkv_cte_destroy(plan) -> None:
+    load().qkv_cte_destroy(plan)
+
+
+_DTYPES = {
+    "A": (torch.uint8,), "W": (torch.uint8,), "w_sf": (torch.uint8,),
+    "a_scale": (torch.float32,), "w_col_scale": (torch.float32,),
+    "bias": (torch.bfloat16, torch.int16, torch.uint16),
+    "gamma_q": (torch.bfloat16, torch.int16, torch.uint16),
+    "gamma_k": (torch.bfloat16, torch.int16, torch.uint16),
+    "cos": (torch.float32,), "sin": (torch.float32,),
+    "O": (torch.bfloat16, torch.int16, torch.uint16),
+    "sumsq": (torch.float32,), "inv_rms": (torch.float32,), "workspace": (torch.uint8,),
+}
+
+
+def _ptr(name: str, t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor or None")
+    if t.dtype not in _DTYPES[name]:
+        raise TypeError(f"{name}: dtype {t.dtype} not in {_DTYPES[name]}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def qkv_cte_run(plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos, sin, O,
+                sumsq, inv_rms, workspace, stream=None) -> int:
+    """Launch the path on `stream` (torch.cuda.Stream, raw handle, or None = current stream)."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    args = [_ptr("A", A), _ptr("a_scale", a_scale), _ptr("W", W), _ptr("w_sf", w_sf),
+            _ptr("w_col_scale", w_col_scale), _ptr("bias", bias), _ptr("gamma_q", gamma_q),
+            _ptr("gamma_k", gamma_k), _ptr("cos", cos), _ptr("sin", sin), _ptr("O", O),
+            _ptr("sumsq", sumsq), _ptr("inv_rms", inv_rms), _ptr("workspace", workspace)]
+    return _check(load().qkv_cte_run(plan, *args, ctypes.c_size_t(ws_bytes), ctypes.c_void_p(handle)))
+
+
+def qkv_cte_status(workspace, stream=None) -> int:
+    """Synchronise the stream and raise QkvCteError if a bounded device wait ran out."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return _check(load().qkv_cte_status(_ptr("workspace", workspace), ctypes.c_void_p(handle)))
+
+
+def qkv_cte_pass_times(plan):
+    """(prep, GEMM, norm+RoPE) device milliseconds of the plan's latest run."""
+    ms = (ctypes.c_float * 3)()
+    _check(load().qkv_cte_pass_times(plan, ms))
+    return tuple(float(x) for x in ms)
+
+
+class QkvCte:
+    """A plan plus its workspace on one device: the usual way to call the library.
+
+    >>> op = QkvCte(tokens=T, hidden=H, n_q_heads=40, n_kv_heads=40, d_head=128)
+    >>> op(A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, out=O)
+    """
+
+    def __init__(self, tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=1, rope=1, eps=1e-6,
+                 tile_n=0, flags=0, device=None):
+        self.desc = make_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=norm, rope=rope,
+                              eps=eps, tile_n=tile_n, flags=flags)
+        self.plan, self.workspace_bytes = qkv_cte_plan(self.desc)
+        self.width = (n_q_heads + 2 * n_kv_heads) * d_head
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def __call__(self, A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, out=None,
+                 w_col_scale=None, sumsq=None, inv_rms=None, stream=None):
+        if out is None:
+            out = torch.empty(self.desc.tokens, self.width, dtype=torch.bfloat16, device=A.device)
+        qkv_cte_run(self.plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos, sin, out,
+                    sumsq, inv_rms, self.workspace, stream)
+        return out
+
+    def status(self, stream=None):
+        return qkv_cte_status(self.workspace, stream)
+
+    def pass_times(self):
+        return qkv_cte_pass_times(self.plan)
+
+    def close(self):
+        if self.plan is not None:
+            qkv_cte_destroy(self.plan)
+            self.plan = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

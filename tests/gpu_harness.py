@@ -1,0 +1,83 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI on seeded
+inputs and compare with the float64 oracle on the same inputs."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import torch
+
+import workloads as wl
+from oracle import qkv_cte_oracle as O
+from rope_tcgen05_mxfp8_gb300 import QkvCte
+
+# Tolerances: per bf16 output element |err| <= REL*|ref| + ABS; sums of squares and
+# inv_rms within SS_REL relative.
+REL = 1e-2
+ABS = 1e-2
+SS_REL = 1e-4
+
+
+def to_device(inp, dev):
+    return {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+
+
+def run_path(call, g, tile_n=0, flags=0, want_sumsq=True, want_inv=True, stream=None, out=None):
+    dev = g["A"].device
+    op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
+                rope=call.rope, eps=call.eps, tile_n=tile_n, flags=flags, device=dev)
+    sumsq = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev) if want_sumsq else None
+    inv = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev) if want_inv else None
+    if out is None:
+        out = torch.full((call.tokens, call.width), float("nan"), dtype=torch.bfloat16, device=dev)
+    op(g["A"], g["a_scale"], g["W"], g["w_sf"], g["bias"], g["gamma_q"] if call.norm else None,
+       g["gamma_k"] if call.norm else None, g["cos"], g["sin"], out=out, w_col_scale=g["w_col_scale"],
+       sumsq=sumsq, inv_rms=inv, stream=stream)
+    return op, out, sumsq, inv
+
+
+def _diag(name, got, ref, bad):
+    d = os.environ.get("QKV_DIAG_DIR")
+    if not d:
+        return ""
+    os.makedirs(d, exist_ok=True)
+    path = os.path.join(d, f"{name}.npz")
+    rows = np.unique(np.nonzero(bad)[0])[:16]
+    np.savez_compressed(path, got=got[rows], ref=ref[rows], rows=rows)
+    return f" (diagnostics in {path})"
+
+
+def check_outputs(call, inp, out, sumsq, inv, rows=None, name="case"):
+    """Compare the GPU outputs with the oracle on `rows` (all rows when None)."""
+    ref = O.qkv_cte_from_inputs(call, inp, rows=rows)
+    idx = torch.arange(call.tokens) if rows is None else torch.as_tensor(rows)
+    idx_dev = idx.to(out.device)
+    got = out.index_select(0, idx_dev).float().cpu().double().numpy()
+    r = ref["O"]
+    err = np.abs(got - r)
+    bad = ~(err <= REL * np.abs(r) + ABS)      # NaN in got counts as bad
+    if bad.any():
+        br, bc = np.nonzero(bad)
+        msg = (f"{name}: {int(bad.sum())}/{bad.size} outputs outside tolerance; first at row "
+               f"{int(idx[br[0]])} col {int(bc[0])}: got {got[br[0], bc[0]]!r} ref {r[br[0], bc[0]]!r}; "
+               f"bad rows {len(np.unique(br))}, bad cols {len(np.unique(bc))} "
+               f"(cols mod 128 {sorted(set((bc % 128).tolist()))[:8]}...)")
+        raise AssertionError(msg + _diag(name, got, r, bad))
+    segs = [0] + ([1] if call.n_kv_heads > 0 else [])
+    if sumsq is not None:
+        s = sumsq.index_select(0, idx_dev).cpu().double().numpy()
+        for c in segs:
+            rel = np.abs(s[:, c] - ref["sumsq"][:, c]) / np.maximum(np.abs(ref["sumsq"][:, c]), 1e-30)
+            assert np.all(rel <= SS_REL), f"{name}: sumsq[{c}] max rel err {np.nanmax(rel):.3e}"
+        if call.n_kv_heads == 0:
+            assert np.all(s[:, 1] == 0), f"{name}: sumsq K column should be 0 without a K segment"
+    if inv is not None and call.norm:
+        v = inv.index_select(0, idx_dev).cpu().double().numpy()
+        for c in segs:
+            rel = np.abs(v[:, c] - ref["inv_rms"][:, c]) / np.abs(ref["inv_rms"][:, c])
+            assert np.all(rel <= SS_REL), f"{name}: inv_rms[{c}] max rel err {np.nanmax(rel):.3e}"
+    return float(np.max(err)) if err.size else 0.0
+
+
+def sampled_rows(call, count=4096):
+    return wl.sample_rows(call, count).numpy()

@@ -1,0 +1,162 @@
+"""CPU checks of the C ABI: the library loads, exports every declared entry point,
+and its host-side plan validation returns the documented codes. No compute call
+is made here (there may be no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import rope_tcgen05_mxfp8_gb300 as pkg
+from rope_tcgen05_mxfp8_gb300 import build as b
+from rope_tcgen05_mxfp8_gb300 import qkv_cte as q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    b.build()
+
+
+def _declared_functions():
+    names = []
+    inc = os.path.join(ROOT, "include")
+    for fn in sorted(os.listdir(inc)):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(qkv_cte_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    declared = _declared_functions()
+    assert set(q.EXPORTED) <= set(declared)
+    lib = ctypes.CDLL(pkg.library_path())
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+
+
+def test_version():
+    assert pkg.qkv_cte_version() == 1
+
+
+def _plan_code(**kw):
+    base = dict(tokens=256, hidden=512, n_q_heads=4, n_kv_heads=4, d_head=128)
+    base.update(kw)
+    desc = q.make_desc(**{k: v for k, v in base.items() if k in
+                          ("tokens", "hidden", "n_q_heads", "n_kv_heads", "d_head", "norm", "rope", "eps",
+                           "mode", "output_layout", "flags", "tile_n")})
+    if "reserved" in kw:
+        desc.reserved = kw["reserved"]
+    try:
+        plan, ws = q.qkv_cte_plan(desc)
+    except q.QkvCteError as e:
+        return e.code
+    q.qkv_cte_destroy(plan)
+    return 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), 0),
+    (dict(tokens=0), 0),
+    (dict(tokens=1), 0),
+    (dict(tokens=-1), -1),
+    (dict(tokens=2 ** 31), -2),
+    (dict(hidden=0), -1),
+    (dict(hidden=100), -2),
+    (dict(hidden=192), -2),
+    (dict(d_head=0), -1),
+    (dict(d_head=24), -2),
+    (dict(n_q_heads=0), -1),
+    (dict(n_kv_heads=-1), -1),
+    (dict(n_kv_heads=0, mode=0), -1),
+    (dict(n_kv_heads=2, mode=1), -1),
+    (dict(mode=7), -1),
+    (dict(norm=2), -1),
+    (dict(rope=-1), -1),
+    (dict(eps=-1.0), -1),
+    (dict(eps=float("nan")), -1),
+    (dict(output_layout=1), -2),
+    (dict(output_layout=5), -1),
+    (dict(flags=0x80), -1),
+    (dict(tile_n=100), -2),
+    (dict(tile_n=240), 0),
+    (dict(reserved=3), -1),
+    (dict(n_kv_heads=0, mode=1, norm=1, rope=0), 0),
+])
+def test_plan_validation(kw, code):
+    assert _plan_code(**kw) == code
+
+
+def test_error_message_is_recorded():
+    with pytest.raises(q.QkvCteError) as ei:
+        q.qkv_cte_plan(q.make_desc(256, 100, 4, 4, 128))
+    assert "multiple of 128" in str(ei.value)
+    assert "multiple of 128" in q.qkv_cte_last_error()
+
+
+def test_workspace_size_formula():
+    for T, I_heads, tile in ((32760, (40, 40), 256), (1, (1, 1), 128), (4096, (40, 0), 240)):
+        nq, nkv = I_heads
+        desc = q.make_desc(T, 5120, nq, nkv, 128, rope=0 if nkv == 0 else 1, tile_n=tile)
+        plan, ws = q.qkv_cte_plan(desc)
+        q.qkv_cte_destroy(plan)
+        I = (nq + 2 * nkv) * 128
+        n_tiles = -(-I // tile)
+        sf = n_tiles * (5120 // 128) * (-(-tile // 128)) * 512
+        ss = -(-(T * 8) // 256) * 256
+        assert ws == 256 + ss + -(-sf // 256) * 256
+
+
+def test_run_rejects_null_plan_without_launch():
+    lib = pkg.load()
+    rc = lib.qkv_cte_run(None, *([None] * 14), ctypes.c_size_t(0), None)
+    assert rc == q.QKV_CTE_ERR_INVALID
+    assert "null plan" in q.qkv_cte_last_error()
+
+
+def test_destroy_null_is_noop():
+    pkg.load().qkv_cte_destroy(None)
+
+
+def test_run_argument_checks_precede_any_cuda_call():
+    """Missing required pointers are rejected on the host (no device touched)."""
+    lib = pkg.load()
+    plan, ws = q.qkv_cte_plan(q.make_desc(256, 512, 4, 4, 128))
+    try:
+        fake = ctypes.c_void_p(4096)
+        args = [fake] * 14
+        args[0] = None  # A missing
+        rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws), None)
+        assert rc == q.QKV_CTE_ERR_INVALID
+        args = [fake] * 14
+        args[7] = None  # gamma_k missing while norm and n_kv > 0
+        rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws), None)
+        assert rc == q.QKV_CTE_ERR_INVALID and "gamma_k" in q.qkv_cte_last_error()
+        args = [fake] * 14
+        args[8] = None  # cos missing while rope
+        rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws), None)
+        assert rc == q.QKV_CTE_ERR_INVALID and "cos" in q.qkv_cte_last_error()
+        args = [fake] * 14
+        args[0] = ctypes.c_void_p(4097)  # misaligned A
+        rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws), None)
+        assert rc == q.QKV_CTE_ERR_UNSUPPORTED
+        args = [fake] * 14
+        rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws - 1), None)
+        assert rc == q.QKV_CTE_ERR_INVALID and "workspace" in q.qkv_cte_last_error()
+    finally:
+        q.qkv_cte_destroy(plan)
+
+
+def test_zero_tokens_launches_nothing():
+    lib = pkg.load()
+    plan, ws = q.qkv_cte_plan(q.make_desc(0, 512, 4, 4, 128))
+    try:
+        fake = ctypes.c_void_p(4096)
+        rc = lib.qkv_cte_run(plan, *([fake] * 14), ctypes.c_size_t(ws), None)
+        assert rc == 0
+    finally:
+        q.qkv_cte_destroy(plan)

@@ -1,0 +1,129 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small shapes are compared element by element on every row (several 128-row tiles
+and N tiles, with ragged tails); the full Wan shapes are compared on 4096 seeded
+sampled rows (rows are independent, so each sampled row is exact), in the same
+launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from rope_tcgen05_mxfp8_gb300 import QKV_CTE_ERR_DEVICE_TIMEOUT, QKV_CTE_FLAG_TEST_STALL, QkvCteError
+
+from gpu_harness import check_outputs, run_path, sampled_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+def _case(call, tile_n=0, rows=None, name=None):
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, tile_n=tile_n)
+    op.status()
+    return check_outputs(call, inp, out, ss, inv, rows=rows, name=name or call.name)
+
+
+@pytest.mark.parametrize("tile_n", [0, 128, 192, 240, 256])
+def test_tiny_full(tile_n):
+    _case(wl.workload("tiny")[0], tile_n=tile_n, name=f"tiny_n{tile_n}")
+
+
+@pytest.mark.parametrize("T", [1, 127, 129, 300])
+@pytest.mark.parametrize("norm,rope", [(1, 1), (1, 0), (0, 1), (0, 0)])
+def test_ragged_rows_and_unaligned_segments(T, norm, rope):
+    # n_q = 3, n_kv = 1, d = 128: I = 640, Q|K boundary at 384 (inside a 256 tile),
+    # K|V boundary at 512, ragged last N tile; per-column weight scales on.
+    call = wl.custom_call(name=f"edge_T{T}", tokens=T, hidden=256, n_q_heads=3, n_kv_heads=1, d_head=128,
+                          norm=norm, rope=rope, seed=T, has_w_col_scale=True)
+    _case(call, name=f"edge_T{T}_n{norm}_r{rope}")
+
+
+@pytest.mark.parametrize("tile_n", [128, 240, 256])
+def test_d_head_64_many_heads(tile_n):
+    call = wl.custom_call(name="d64", tokens=200, hidden=384, n_q_heads=5, n_kv_heads=2, d_head=64,
+                          seed=21, has_w_col_scale=True)
+    _case(call, tile_n=tile_n, name=f"d64_n{tile_n}")
+
+
+@pytest.mark.parametrize("norm,rope", [(1, 0), (0, 0), (1, 1)])
+def test_separate_mode_small(norm, rope):
+    call = wl.custom_call(name="sep", tokens=333, hidden=512, n_q_heads=6, n_kv_heads=0, d_head=128,
+                          norm=norm, rope=rope, seed=31)
+    _case(call, name=f"sep_n{norm}_r{rope}")
+
+
+def test_large_hidden_small_tokens():
+    call = wl.custom_call(name="deepk", tokens=64, hidden=5120, n_q_heads=2, n_kv_heads=2, d_head=128, seed=41)
+    _case(call)
+
+
+def test_short_full():
+    _case(wl.workload("short")[0])
+
+
+def test_wan480p_sampled():
+    call = wl.workload("wan480p")[0]
+    _case(call, rows=sampled_rows(call))
+
+
+def test_wan720p_sampled():
+    call = wl.workload("wan720p")[0]
+    _case(call, rows=sampled_rows(call))
+
+
+def test_cross_attention_calls():
+    q, k, v = wl.workload("cross")
+    _case(q, rows=sampled_rows(q))
+    _case(k)
+    _case(v)
+
+
+def test_outputs_repeatable_on_side_stream():
+    call = wl.workload("tiny")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        op1, out1, ss1, _ = run_path(call, g, stream=s)
+        op2, out2, ss2, _ = run_path(call, g, stream=s)
+    s.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    torch.testing.assert_close(ss1, ss2, rtol=1e-6, atol=0)
+    check_outputs(call, inp, out2, ss2, None, name="side_stream")
+
+
+def test_norm_off_still_reports_sumsq():
+    call = wl.custom_call(name="ss_only", tokens=150, hidden=256, n_q_heads=2, n_kv_heads=1, d_head=128,
+                          norm=0, rope=0, seed=51)
+    _case(call)
+
+
+def test_zero_tokens():
+    call = wl.custom_call(name="empty", tokens=0, hidden=256, n_q_heads=2, n_kv_heads=1, d_head=128, seed=1)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g)
+    op.status()
+    assert out.numel() == 0
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The test hook stops the GEMM's load warp; every downstream wait must run out
+    (about two seconds each), the kernel must return, the status call must report
+    it, and the next ordinary call on the same context must be correct."""
+    call = wl.workload("tiny")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_TEST_STALL)
+    with pytest.raises(QkvCteError) as ei:
+        op.status()
+    assert ei.value.code == QKV_CTE_ERR_DEVICE_TIMEOUT
+    assert "mma-operands-ready" in str(ei.value)
+    op.status()  # the status word was cleared
+    op2, out2, ss2, inv2 = run_path(call, g)
+    op2.status()
+    check_outputs(call, inp, out2, ss2, inv2, name="after_timeout")
