@@ -294,10 +294,10 @@ def run_ours(args):
     hbm_gbs, bf16, bf16_sus, peak_src = _peaks()
     fp8_peak = bf16 * FP8_PER_BF16
     k1_achieved = flops / (gemm_ms * 1e-3) / 1e12
-    # norm + RoPE algorithmic bytes: read + write the Q and K columns (bf16), read the
-    # fp32 cos/sin rows and the fp32 [T, 2] sums of squares
+    # norm + RoPE bytes this design must move: read the fp32 Q/K hand-off, write the
+    # bf16 Q/K columns of O, read the fp32 cos/sin rows and the fp32 [T, 2] sums
     qk_cols = (call.n_q_heads + call.n_kv_heads) * call.d_head
-    k2_bytes = 2 * 2 * call.tokens * qk_cols + 2 * 4 * call.tokens * call.d_head + 8 * call.tokens
+    k2_bytes = (4 + 2) * call.tokens * qk_cols + 2 * 4 * call.tokens * call.d_head + 8 * call.tokens
     k2_gbs = k2_bytes / (norm_ms * 1e-3) / 1e9 if norm_ms > 0 else None
 
     e2e = None

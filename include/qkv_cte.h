@@ -28,10 +28,11 @@
  *   Every tensor pointer is a DEVICE pointer owned by the caller; the library never
  *   frees or keeps it past the call. The plan owns only host-side state. The workspace
  *   is caller-allocated device memory of the size qkv_cte_plan reports; it holds the
- *   per-call scratch (repacked weight scales, the sum-of-squares accumulator and a
- *   device status word) and must not be shared by calls that overlap on the GPU.
- *   qkv_cte_run is stream-ordered and asynchronous: it never synchronises. Q and K are
- *   normalised in place in O, so O must not alias any input.
+ *   per-call scratch (repacked weight scales, the sum-of-squares accumulator, a device
+ *   status word and, when a norm or RoPE pass runs, the un-normalised Q and K columns
+ *   in fp32: 4*T*(n_q + n_kv)*d_head bytes) and must not be shared by calls that
+ *   overlap on the GPU. qkv_cte_run is stream-ordered and asynchronous: it never
+ *   synchronises. O must not alias any input.
  *
  * Errors
  *   Every entry point returns 0 on success or a negative QKV_CTE_ERR_* code, never
@@ -112,6 +113,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
  *              segments ([qkv_cte] "Design" 1 step a; column 1 is 0 when n_kv == 0)
  * inv_rms    : fp32   [T, 2] or NULL: the rsqrt factors of step b (written iff norm)
  * workspace  : device scratch of at least the planned size; 256-byte aligned
+ * With tokens == 0 every tensor pointer may be NULL: no kernel is launched and only
+ * the workspace's status word is reset (when a workspace is given).
  * Returns 0 or -1/-2/-3/-4 (nothing launched on -1/-2/-4). */
 int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, const uint8_t* W,
                 const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias,
@@ -121,8 +124,10 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
 
 /* Synchronise `stream`, then read and clear the device status word in `workspace`.
  * Each run clears the word before its kernels start, so this reports the most recent
- * run that used `workspace`. Returns 0, -5 if one of its bounded device waits ran out
- * (the message names the wait), or -3 on a CUDA error. */
+ * run that used `workspace`; before the first run the workspace must hold zeros.
+ * Returns 0, -5 if one of its bounded device waits ran out (the message names the
+ * wait), -1 if the word holds bits no run writes (an uninitialised workspace), or -3
+ * on a CUDA error. */
 int qkv_cte_status(void* workspace, void* stream);
 
 /* Device time in milliseconds of each pass of the most recent run of `plan`, which

@@ -24,8 +24,10 @@ enum : uint32_t {
 //                            caller passes no sumsq buffer)
 //   [.., + sf_bytes)         W's UE8M0 scales repacked per (N tile, K stage) in the
 //                            order the MMA's scale-factor copy consumes them
+//   [.., + qk_bytes)         fp32 [T, I_q + I_k]: the un-normalised Q and K columns,
+//                            handed from K1 to K2 (only when a norm/RoPE pass runs)
 struct WorkspaceLayout {
-  size_t status_off, sumsq_off, sf_off, total;
+  size_t status_off, sumsq_off, sf_off, qk_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -44,6 +46,7 @@ struct GemmArgs {
   const uint16_t* bias;      // may be null
   const uint8_t* sf_packed;
   uint16_t* O;
+  float* qk;                 // fp32 [T, k_end] Q/K hand-off, or null: Q/K go to O as bf16
   float* sumsq;              // may be null: then no sum of squares is accumulated
   uint32_t* status;
   int q_end, k_end;          // Q = [0, q_end), K = [q_end, k_end), V = [k_end, I)
@@ -55,6 +58,7 @@ struct NormRopeArgs {
   int norm, rope;
   float eps;
   const float* sumsq;
+  const float* qk;           // fp32 [T, (n_q + n_kv) * d_head] un-normalised Q and K
   const uint16_t* gamma_q;
   const uint16_t* gamma_k;
   const float* cos_t;

@@ -1,5 +1,5 @@
-// Kernel K2: in-place across-heads RMSNorm apply + rotate-half RoPE over the Q and K
-// columns of O; V is never read.
+// Kernel K2: across-heads RMSNorm apply + rotate-half RoPE of the Q and K columns,
+// written into O; V is never read.
 //
 // Follows the `qkv_cte` kernel reference page, "Design" 1 (steps b and c: finish
 // inv_rms = 1/sqrt(sum(o^2) / (n_heads * d_head) + eps) per token and segment, re-read
@@ -8,10 +8,12 @@
 // position-only cos/sin broadcast over the heads).
 //
 // On one GPU every head is local, so the page's cross-rank AllReduce of the sums is
-// the identity: K1 already summed over every column tile of the row. This pass is
-// HBM-bound: each thread moves two 16-byte vectors of O (8 lanes of the low half of
-// a head and the 8 partner lanes d/2 away), with the per-position cos/sin and the
-// gamma vectors served from L1/L2.
+// the identity: K1 already summed over every column tile of the row. The page writes
+// the un-normalised Q/K into the output and re-reads it; here K1 hands them over in
+// fp32 (a workspace buffer) so the result is rounded to bf16 once, here. This pass
+// is HBM-bound: each thread reads 8 lanes of the low half of a head and the 8
+// partner lanes d/2 away (2 x 32 bytes of fp32) and writes 2 x 16 bytes of bf16 to
+// O, with the per-position cos/sin and the gamma vectors served from L1/L2.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -46,6 +48,14 @@ __device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
   f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
+// Read-once data: bypass L1 allocation.
+__device__ __forceinline__ void load8f_stream(const float* p, float (&f)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
 __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const NormRopeArgs p) {
   const int chunks = p.d_head / 16;  // 8-lane chunks in the low half of one head
   const int half = p.d_head / 2;
@@ -62,11 +72,13 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const NormRopeArgs p)
     const int h = seg ? hg - p.n_q : hg;
     const int n_heads = seg ? p.n_kv : p.n_q;
     const int off = h * p.d_head + c * 8;  // column inside the segment
-    uint16_t* row = p.O + static_cast<size_t>(t) * p.I + (seg ? p.n_q * p.d_head : 0);
+    const int seg_base = seg ? p.n_q * p.d_head : 0;
+    uint16_t* row = p.O + static_cast<size_t>(t) * p.I + seg_base;
+    const float* src = p.qk + static_cast<size_t>(t) * ((p.n_q + p.n_kv) * p.d_head) + seg_base + off;
 
     float lo[8], hi[8];
-    unpack8(*reinterpret_cast<const uint4*>(row + off), lo);
-    unpack8(*reinterpret_cast<const uint4*>(row + off + half), hi);
+    load8f_stream(src, lo);
+    load8f_stream(src + half, hi);
 
     float inv = 1.0f;
     if (p.norm) {

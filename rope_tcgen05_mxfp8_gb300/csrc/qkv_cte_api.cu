@@ -169,7 +169,9 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   w.status_off = 0;
   w.sumsq_off = 256;
   w.sf_off = w.sumsq_off + align_up((size_t)g.T * 2 * sizeof(float), 256);
-  w.total = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
+  w.qk_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
+  const bool second_pass = d.norm || d.rope;
+  w.total = w.qk_off + (second_pass ? align_up((size_t)g.T * p->k_end * sizeof(float), 256) : 0);
   *workspace_bytes = w.total;
   *out = p;
   return ok();
@@ -200,6 +202,14 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (plan == nullptr) return fail(QKV_CTE_ERR_INVALID, "null plan");
   const qkv_cte_desc& d = plan->d;
   const GemmShape& g = plan->g;
+  if (g.T == 0) {
+    // An empty problem reads and writes no tensor; it only resets the status word.
+    if (workspace != nullptr) {
+      cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
+    }
+    return ok();
+  }
   if (!A || !a_scale || !W || !w_sf || !O || !workspace)
     return fail(QKV_CTE_ERR_INVALID, "A, a_scale, W, w_sf, O and workspace are required");
   if (d.norm && !gamma_q) return fail(QKV_CTE_ERR_INVALID, "norm needs gamma_q");
@@ -221,7 +231,6 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (workspace_bytes < plan->ws.total)
     return fail(QKV_CTE_ERR_INVALID, "workspace of %zu bytes is smaller than the planned %zu",
                 workspace_bytes, plan->ws.total);
-  if (g.T == 0) return ok();
 
   DeviceInfo dev;
   int rc = device_info(&dev);
@@ -265,6 +274,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.bias = bias;
   ga.sf_packed = sf_packed;
   ga.O = O;
+  float* qk = (d.norm || d.rope) ? reinterpret_cast<float*>(ws + plan->ws.qk_off) : nullptr;
+  ga.qk = qk;
   ga.sumsq = need_ss ? ss : nullptr;
   ga.status = status;
   ga.q_end = plan->q_end;
@@ -284,6 +295,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.rope = d.rope;
   na.eps = d.eps;
   na.sumsq = ss;
+  na.qk = qk;
   na.gamma_q = gamma_q;
   na.gamma_k = gamma_k;
   na.cos_t = cos_table;
@@ -308,6 +320,12 @@ int qkv_cte_status(void* workspace, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   if (word == 0) return ok();
+  const uint32_t known = kErrProducerEmptyWait | kErrMmaFullWait | kErrMmaTmemEmptyWait |
+                         kErrEpilogueTmemFullWait | kErrDrainWait;
+  if (word & ~known)
+    return fail(QKV_CTE_ERR_INVALID,
+                "workspace status word holds 0x%x, which no run wrote: zero the workspace before its first use",
+                word);
   const uint32_t zero = 0;
   e = cudaMemcpyAsync(workspace, &zero, sizeof(zero), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);

@@ -17,10 +17,12 @@
 //     tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each, one UE8M0 scale per row of
 //     B per MMA, selected by the scale-factor byte id) into a TMEM fp32 accumulator;
 //   * warps 2-5: epilogue. tcgen05.ld the accumulator (one TMEM lane = one row per
-//     thread), apply the row scale / column scale / bias, store bf16, accumulate the
-//     Q and K sums of squares in fp32 and add them to sumsq[T, 2] with one atomic per
-//     row and segment. With two accumulator stages the epilogue of tile j overlaps
-//     the MMAs of tile j+1.
+//     thread), apply the row scale / column scale / bias, accumulate the Q and K sums
+//     of squares in fp32 and add them to sumsq[T, 2] with one atomic per row and
+//     segment. V columns are stored as final bf16. Q and K columns are stored in fp32
+//     to a workspace hand-off buffer when the norm/RoPE pass follows (so the only
+//     rounding to bf16 is the final one), else as bf16. With two accumulator stages
+//     the epilogue of tile j overlaps the MMAs of tile j+1.
 //   * A carries no MX scale of its own (its only scale is the fp32 row scale), so the
 //     A-side scale factors are the constant 2^0 (UE8M0 127), copied to TMEM once.
 // Every mbarrier wait is bounded; a wait that runs out records its role in the
@@ -299,17 +301,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 16; ++j) bias[j] = 0.0f;
         }
-        uint32_t packed[8];
+        float v[16];
 #pragma unroll
-        for (int j = 0; j < 16; j += 2) {
-          const float v0 = __uint_as_float(r[j]) * ascale * cs[j] + bias[j];
-          const float v1 = __uint_as_float(r[j + 1]) * ascale * cs[j + 1] + bias[j + 1];
+        for (int j = 0; j < 16; ++j) {
+          v[j] = __uint_as_float(r[j]) * ascale * cs[j] + bias[j];
           const int c = col0 + j;
-          if (c < a.q_end) ss_q += v0 * v0; else if (c < a.k_end) ss_k += v0 * v0;
-          if (c + 1 < a.q_end) ss_q += v1 * v1; else if (c + 1 < a.k_end) ss_k += v1 * v1;
-          packed[j / 2] = pack_bf16x2(v0, v1);
+          if (c < a.q_end) ss_q += v[j] * v[j]; else if (c < a.k_end) ss_k += v[j] * v[j];
         }
-        if (row_ok) {
+        if (!row_ok) continue;
+        if (a.qk != nullptr && col0 < a.k_end) {
+          // Q/K columns that the norm/RoPE pass will finish: hand over in fp32
+          float4* dst = reinterpret_cast<float4*>(a.qk + static_cast<size_t>(row) * a.k_end + col0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          uint32_t packed[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
           uint4* dst = reinterpret_cast<uint4*>(orow + col0);
           dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
           dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);

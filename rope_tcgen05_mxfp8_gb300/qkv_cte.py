@@ -194,7 +194,7 @@ class QkvCte:
         self.plan, self.workspace_bytes = qkv_cte_plan(self.desc)
         self.width = (n_q_heads + 2 * n_kv_heads) * d_head
         dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
-        self.workspace = torch.empty(max(self.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+        self.workspace = torch.zeros(max(self.workspace_bytes, 256), dtype=torch.uint8, device=dev)
 
     def __call__(self, A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, out=None,
                  w_col_scale=None, sumsq=None, inv_rms=None, stream=None):
