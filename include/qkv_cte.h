@@ -29,9 +29,10 @@
  *   frees or keeps it past the call. The plan owns only host-side state. The workspace
  *   is caller-allocated device memory of the size qkv_cte_plan reports; it holds the
  *   per-call scratch (repacked weight scales, the sum-of-squares accumulator, a device
- *   status word and, when a norm or RoPE pass runs, the un-normalised Q and K columns
- *   in fp32: 4*T*(n_q + n_kv)*d_head bytes) and must not be shared by calls that
- *   overlap on the GPU. qkv_cte_run is stream-ordered and asynchronous: it never
+ *   status word, per-panel completion counters, timing stamps and, when a norm or RoPE
+ *   pass runs, the un-normalised Q and K columns in fp32: 4*T*(n_q + n_kv)*d_head
+ *   bytes) and must not be shared by calls that overlap on the GPU. The norm/RoPE
+ *   kernel is launched as a programmatic dependent of the GEMM so the two overlap. qkv_cte_run is stream-ordered and asynchronous: it never
  *   synchronises. O must not alias any input.
  *
  * Errors
@@ -69,6 +70,9 @@ enum { QKV_CTE_LAYOUT_BSD = 0, QKV_CTE_LAYOUT_NBSD = 1 };
 /* Record CUDA events between the launches of each run so qkv_cte_pass_times() can
  * report per-pass device times. */
 #define QKV_CTE_FLAG_PROFILE 0x2u
+/* Launch the norm/RoPE pass after the GEMM has finished instead of overlapping the two
+ * (same results; used to time each pass on its own). */
+#define QKV_CTE_FLAG_SERIAL_PASSES 0x4u
 
 /* Problem description ([qkv_cte] "Interface" argument table, flattened to scalars). */
 typedef struct {
@@ -130,11 +134,16 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
  * on a CUDA error. */
 int qkv_cte_status(void* workspace, void* stream);
 
-/* Device time in milliseconds of each pass of the most recent run of `plan`, which
- * must have been created with QKV_CTE_FLAG_PROFILE: ms[0] = prep (scale repack and
- * clears), ms[1] = GEMM with its fused epilogue, ms[2] = norm + RoPE (0 when the call
- * has neither). Blocks until that run has finished. Returns 0, -1 (no flag, never run,
- * null pointer) or -3. */
+/* Device times in milliseconds of the most recent run of `plan`, which must have been
+ * created with QKV_CTE_FLAG_PROFILE. ms must hold 4 floats:
+ *   ms[0] prep (scale repack and clears), from CUDA events around its launch;
+ *   ms[1] GEMM with its fused epilogue, and ms[2] norm + RoPE (0 when the call has
+ *         neither): first-block start to last-block end, from %globaltimer stamps the
+ *         kernels write into the workspace (the two passes overlap, so no CUDA event
+ *         can separate them);
+ *   ms[3] the whole run, from CUDA events.
+ * Blocks until that run has finished; its workspace must still be valid. Returns 0, -1
+ * (no flag, never run, null pointer) or -3. */
 int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms);
 
 /* Release a plan. NULL is a no-op. */

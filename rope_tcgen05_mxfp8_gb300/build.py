@@ -24,7 +24,7 @@ SOURCES = ["qkv_cte_api.cu", "qkv_gemm_mxf8.cu", "qk_norm_rope.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-Wformat", "-Xcompiler", "-Werror=format",
                      "-I", INCLUDE, "-I", CSRC]
 
 

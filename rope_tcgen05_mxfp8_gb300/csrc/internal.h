@@ -16,29 +16,86 @@ enum : uint32_t {
   kErrMmaTmemEmptyWait = 1u << 2,
   kErrEpilogueTmemFullWait = 1u << 3,
   kErrDrainWait = 1u << 4,
+  kErrNormReadyWait = 1u << 5,
 };
 
 // Workspace layout (all offsets 256-byte aligned):
-//   [0, 256)                 status words
+//   [0, 256)                 status word (offset 0) and, at kStampOffset, four uint64
+//                            %globaltimer stamps: K1 first start, K1 last end, K2 first
+//                            start, K2 last end
 //   [256, 256 + ss_bytes)    fp32 [T, 2] sum-of-squares accumulator (used when the
 //                            caller passes no sumsq buffer)
 //   [.., + sf_bytes)         W's UE8M0 scales repacked per (N tile, K stage) in the
 //                            order the MMA's scale-factor copy consumes them
+//   [.., + ready_bytes)      uint32 [m_tiles]: per 128-row panel, how many epilogue
+//                            warp-tiles of K1's Q/K tiles have finished (4 per tile)
 //   [.., + qk_bytes)         fp32 [T, I_q + I_k]: the un-normalised Q and K columns,
 //                            handed from K1 to K2 (only when a norm/RoPE pass runs)
+constexpr size_t kStampOffset = 64;
+
 struct WorkspaceLayout {
-  size_t status_off, sumsq_off, sf_off, qk_off, total;
+  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+constexpr int kMaxBands = 16;
+
 // GEMM (kernel K1) configuration chosen at plan time.
+//
+// Tile order: the N tiles are cut into bands (contiguous runs of N tiles). The
+// persistent grid walks the bands one after the other and, inside a band, row panel
+// by row panel (m outer, n inner), so the CTAs running at any moment share one band's
+// slab of W, which stays resident in L2 while A streams through. Bands of tiles that
+// hold only V columns come first; the bands of tiles holding Q or K columns come last,
+// so the norm/RoPE pass (which waits for a panel's Q/K tiles only) overlaps them.
 struct GemmShape {
   int T, H, I;
   int tile_n;       // N tile (columns of O per tile)
   int m_tiles, n_tiles, k_stages;
   int sf_chunks;    // 128-column scale-factor chunks per N tile
+  int n_qk_tiles;   // N tiles holding at least one Q or K column: [0, n_qk_tiles)
+  int n_bands;
+  int band_n0[kMaxBands];          // first N tile of each band
+  int band_nc[kMaxBands];          // N tiles in each band
+  int band_tile0[kMaxBands + 1];   // linear index of each band's first tile
 };
+
+// (m, n) of linear tile `tile` in the banded order.
+__host__ __device__ inline void tile_coords(const GemmShape& g, int tile, int& m, int& n) {
+  int b = 0;
+  while (b + 1 < g.n_bands && tile >= g.band_tile0[b + 1]) ++b;
+  const int local = tile - g.band_tile0[b];
+  const int nc = g.band_nc[b];
+  m = local / nc;
+  n = g.band_n0[b] + (local - m * nc);
+}
+
+// Cut [0, n_tiles) into bands of at most `band_tiles` N tiles, V-only tiles first.
+inline void make_bands(GemmShape& g, int band_tiles) {
+  if (band_tiles < 1) band_tiles = 1;
+  const int runs[2][2] = {{g.n_qk_tiles, g.n_tiles - g.n_qk_tiles}, {0, g.n_qk_tiles}};
+  int need = 0;
+  for (const auto& r : runs) need += (r[1] + band_tiles - 1) / band_tiles;
+  while (need > kMaxBands) {
+    ++band_tiles;
+    need = 0;
+    for (const auto& r : runs) need += (r[1] + band_tiles - 1) / band_tiles;
+  }
+  g.n_bands = 0;
+  int tile0 = 0;
+  for (const auto& r : runs) {
+    for (int n0 = r[0]; n0 < r[0] + r[1]; n0 += band_tiles) {
+      const int nc = (r[0] + r[1] - n0) < band_tiles ? (r[0] + r[1] - n0) : band_tiles;
+      g.band_n0[g.n_bands] = n0;
+      g.band_nc[g.n_bands] = nc;
+      g.band_tile0[g.n_bands] = tile0;
+      tile0 += nc * g.m_tiles;
+      ++g.n_bands;
+    }
+  }
+  g.band_tile0[g.n_bands] = tile0;
+}
 
 struct GemmArgs {
   const float* a_scale;
@@ -48,6 +105,8 @@ struct GemmArgs {
   uint16_t* O;
   float* qk;                 // fp32 [T, k_end] Q/K hand-off, or null: Q/K go to O as bf16
   float* sumsq;              // may be null: then no sum of squares is accumulated
+  uint32_t* ready;           // per-panel completion counters (K2 overlaps K1 on them)
+  unsigned long long* stamps;  // [0] first CTA start (min), [1] last CTA end (max)
   uint32_t* status;
   int q_end, k_end;          // Q = [0, q_end), K = [q_end, k_end), V = [k_end, I)
   uint32_t flags;
@@ -65,6 +124,10 @@ struct NormRopeArgs {
   const float* sin_t;
   uint16_t* O;
   float* inv_rms;            // may be null
+  const uint32_t* ready;     // per 128-row panel: K1 epilogue warp-tiles finished
+  uint32_t ready_target;     // 4 * K1's Q/K tiles: the panel's Q and K are final
+  unsigned long long* stamps;  // [0] first block start (min), [1] last block end (max)
+  uint32_t* status;
 };
 
 // Supported N tiles (compile-time instantiations of K1).
@@ -74,9 +137,12 @@ size_t gemm_smem_bytes(int tile_n);
 
 // Launchers. Each returns cudaSuccess or the launch error.
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
-                        size_t sumsq_count, uint32_t* status, cudaStream_t s, int num_sms);
+                        size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
+                        cudaStream_t s, int num_sms);
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                         const GemmArgs& a, cudaStream_t s, int num_sms);
-cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms);
+// Launched right after K1 on the same stream as a programmatic dependent launch, so
+// its blocks start while K1 runs and take each row panel as soon as K1 marks it ready.
+cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap);
 
 }  // namespace qkvcte

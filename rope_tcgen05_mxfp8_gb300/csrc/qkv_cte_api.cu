@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -20,18 +21,20 @@ struct qkv_cte_plan_s {
   GemmShape g;
   WorkspaceLayout ws;
   int q_end, k_end;
-  // QKV_CTE_FLAG_PROFILE: events around the three launches of the latest run
-  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+  // QKV_CTE_FLAG_PROFILE: events before the prep kernel, after it, and after the last
+  // kernel of the latest run (no event between K1 and K2: it would serialise them)
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
   int ev_device = -1;
   bool ran = false;
   bool has_norm_pass = false;
+  const void* last_workspace = nullptr;
 };
 
 namespace {
 
 thread_local char g_last_error[512] = "";
 
-int fail(int code, const char* fmt, ...) {
+__attribute__((format(printf, 2, 3))) int fail(int code, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
   vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
@@ -103,10 +106,25 @@ int encode_operand(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return QKV_CTE_OK;
 }
 
+// N tiles per band: the band's W slab (tile_n * H bytes per N tile) is kept to about
+// 28 MB so that it stays resident in the 129 MB L2 beside the streaming traffic
+// (measured at the Wan 480p shape: 28 MB bands beat 56 MB, 110 MB and one band).
+// QKV_CTE_BAND_MB overrides the budget (for tuning sweeps).
+int band_tiles(const GemmShape& g) {
+  double mb = 28.0;
+  if (const char* e = getenv("QKV_CTE_BAND_MB")) {
+    const double v = atof(e);
+    if (v > 0) mb = v;
+  }
+  const double per_tile = (double)g.tile_n * (double)g.H;
+  int n = (int)(mb * 1048576.0 / per_tile);
+  return n < 1 ? 1 : n;
+}
+
 int choose_tile_n(const qkv_cte_desc& d, int I) {
   if (d.tile_n != 0) return d.tile_n;
   (void)I;
-  return 256;
+  return 240;  // two TMEM accumulator stages: the epilogue overlaps the next tile's MMAs
 }
 
 }  // namespace
@@ -143,7 +161,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   if (d.output_layout == QKV_CTE_LAYOUT_NBSD)
     return fail(QKV_CTE_ERR_UNSUPPORTED, "NBSd output layout is not built in this version");
   if (d.output_layout != QKV_CTE_LAYOUT_BSD) return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
-  if ((d.flags & ~(QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE)) != 0)
+  if ((d.flags & ~(QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES)) != 0)
     return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
   if (d.reserved != 0) return fail(QKV_CTE_ERR_INVALID, "reserved must be 0");
   const long long I = (long long)(d.n_q_heads + 2LL * d.n_kv_heads) * d.d_head;
@@ -165,11 +183,15 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   g.sf_chunks = gemm_sf_chunks(tile_n);
   p->q_end = d.n_q_heads * d.d_head;
   p->k_end = p->q_end + d.n_kv_heads * d.d_head;
+  g.n_qk_tiles = (p->k_end + tile_n - 1) / tile_n;
+  if (g.n_qk_tiles > g.n_tiles) g.n_qk_tiles = g.n_tiles;
+  make_bands(g, band_tiles(g));
   WorkspaceLayout& w = p->ws;
   w.status_off = 0;
   w.sumsq_off = 256;
   w.sf_off = w.sumsq_off + align_up((size_t)g.T * 2 * sizeof(float), 256);
-  w.qk_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
+  w.ready_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
+  w.qk_off = w.ready_off + align_up((size_t)g.m_tiles * sizeof(uint32_t), 256);
   const bool second_pass = d.norm || d.rope;
   w.total = w.qk_off + (second_pass ? align_up((size_t)g.T * p->k_end * sizeof(float), 256) : 0);
   *workspace_bytes = w.total;
@@ -188,10 +210,16 @@ int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms) {
   if (plan == nullptr || ms == nullptr) return fail(QKV_CTE_ERR_INVALID, "null argument");
   if (!(plan->d.flags & QKV_CTE_FLAG_PROFILE)) return fail(QKV_CTE_ERR_INVALID, "plan made without QKV_CTE_FLAG_PROFILE");
   if (!plan->ran) return fail(QKV_CTE_ERR_INVALID, "plan has not run");
-  cudaError_t e = cudaEventSynchronize(plan->ev[3]);
-  for (int i = 0; i < 3 && e == cudaSuccess; ++i) e = cudaEventElapsedTime(&ms[i], plan->ev[i], plan->ev[i + 1]);
+  cudaError_t e = cudaEventSynchronize(plan->ev[2]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[0], plan->ev[0], plan->ev[1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[3], plan->ev[0], plan->ev[2]);
+  unsigned long long st[4] = {0, 0, 0, 0};
+  if (e == cudaSuccess)
+    e = cudaMemcpy(st, static_cast<const uint8_t*>(plan->last_workspace) + kStampOffset, sizeof(st),
+                   cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "pass times: %s", cudaGetErrorString(e));
-  if (!plan->has_norm_pass) ms[2] = 0.0f;
+  ms[1] = st[1] > st[0] ? (float)((st[1] - st[0]) * 1e-6) : 0.0f;
+  ms[2] = (plan->has_norm_pass && st[3] > st[2]) ? (float)((st[3] - st[2]) * 1e-6) : 0.0f;
   return ok();
 }
 
@@ -255,7 +283,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
     cudaGetDevice(&cur);
     if (plan->ev[0] != nullptr && plan->ev_device != cur)
       return fail(QKV_CTE_ERR_INVALID, "a profiled plan must stay on one device");
-    for (int i = 0; i < 4 && plan->ev[i] == nullptr; ++i)
+    for (int i = 0; i < 3 && plan->ev[i] == nullptr; ++i)
       if ((e = cudaEventCreate(&plan->ev[i])) != cudaSuccess)
         return fail(QKV_CTE_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
     plan->ev_device = cur;
@@ -263,8 +291,10 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
       return fail(QKV_CTE_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
   }
 
-  e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0,
-                              status, s, dev.sms);
+  uint32_t* ready = reinterpret_cast<uint32_t*>(ws + plan->ws.ready_off);
+  unsigned long long* stamps = reinterpret_cast<unsigned long long*>(ws + kStampOffset);
+  e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0, ready, status,
+                  stamps, s, dev.sms);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
   if (prof) cudaEventRecord(plan->ev[1], s);
 
@@ -277,13 +307,14 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   float* qk = (d.norm || d.rope) ? reinterpret_cast<float*>(ws + plan->ws.qk_off) : nullptr;
   ga.qk = qk;
   ga.sumsq = need_ss ? ss : nullptr;
+  ga.ready = ready;
+  ga.stamps = stamps;
   ga.status = status;
   ga.q_end = plan->q_end;
   ga.k_end = plan->k_end;
   ga.flags = d.flags;
   e = launch_gemm(g, tmA, tmW, ga, s, dev.sms);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
-  if (prof) cudaEventRecord(plan->ev[2], s);
 
   NormRopeArgs na;
   na.T = g.T;
@@ -302,12 +333,17 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.sin_t = sin_table;
   na.O = O;
   na.inv_rms = inv_rms;
-  e = launch_norm_rope(na, s, dev.sms);
+  na.ready = ready;
+  na.ready_target = 4u * (uint32_t)g.n_qk_tiles;
+  na.status = status;
+  na.stamps = stamps + 2;
+  e = launch_norm_rope(na, s, dev.sms, (d.flags & QKV_CTE_FLAG_SERIAL_PASSES) == 0);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "norm/rope launch: %s", cudaGetErrorString(e));
   if (prof) {
-    cudaEventRecord(plan->ev[3], s);
+    cudaEventRecord(plan->ev[2], s);
     plan->ran = true;
     plan->has_norm_pass = d.norm || d.rope;
+    plan->last_workspace = workspace;
   }
   return ok();
 }
@@ -321,7 +357,7 @@ int qkv_cte_status(void* workspace, void* stream) {
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   if (word == 0) return ok();
   const uint32_t known = kErrProducerEmptyWait | kErrMmaFullWait | kErrMmaTmemEmptyWait |
-                         kErrEpilogueTmemFullWait | kErrDrainWait;
+                         kErrEpilogueTmemFullWait | kErrDrainWait | kErrNormReadyWait;
   if (word & ~known)
     return fail(QKV_CTE_ERR_INVALID,
                 "workspace status word holds 0x%x, which no run wrote: zero the workspace before its first use",
@@ -331,12 +367,13 @@ int qkv_cte_status(void* workspace, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
   return fail(QKV_CTE_ERR_DEVICE_TIMEOUT,
-              "device wait ran out (status 0x%x:%s%s%s%s%s)", word,
+              "device wait ran out (status 0x%x:%s%s%s%s%s%s)", word,
               (word & kErrProducerEmptyWait) ? " load-stage-free" : "",
               (word & kErrMmaFullWait) ? " mma-operands-ready" : "",
               (word & kErrMmaTmemEmptyWait) ? " mma-accumulator-free" : "",
               (word & kErrEpilogueTmemFullWait) ? " epilogue-accumulator-ready" : "",
-              (word & kErrDrainWait) ? " drain" : "");
+              (word & kErrDrainWait) ? " drain" : "",
+              (word & kErrNormReadyWait) ? " norm-panel-ready" : "");
 }
 
 }  // extern "C"

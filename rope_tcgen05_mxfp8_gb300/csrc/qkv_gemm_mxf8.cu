@@ -8,8 +8,9 @@
 // "Design" 1) folded into that same copy-out.
 //
 // GB300 design (not the page's Trainium schedule):
-//   * persistent grid, one CTA per SM, tiles of 128 rows x tile_n columns, walked
-//     row-panel-major so W (a few tens of MB) stays resident in L2 while A streams;
+//   * persistent grid, one CTA per SM, tiles of 128 rows x tile_n columns, walked in
+//     bands of N tiles (V-only tiles first), row-panel-major inside a band, so the
+//     band's slab of W stays resident in L2 while A streams;
 //   * warp 0: TMA producer. Per K stage it loads a 128x128-byte A tile and a
 //     tile_n x 128-byte W tile (128-byte swizzle) plus the stage's repacked UE8M0
 //     block scales, all counted on one mbarrier;
@@ -22,7 +23,10 @@
 //     segment. V columns are stored as final bf16. Q and K columns are stored in fp32
 //     to a workspace hand-off buffer when the norm/RoPE pass follows (so the only
 //     rounding to bf16 is the final one), else as bf16. With two accumulator stages
-//     the epilogue of tile j overlaps the MMAs of tile j+1.
+//     the epilogue of tile j overlaps the MMAs of tile j+1. After each tile every
+//     epilogue warp fences its stores and bumps its row panel's ready counter; the
+//     norm/RoPE pass, launched as a programmatic dependent of this grid, starts on a
+//     panel once all its tiles are in.
 //   * A carries no MX scale of its own (its only scale is the fp32 row scale), so the
 //     A-side scale factors are the constant 2^0 (UE8M0 127), copied to TMEM once.
 // Every mbarrier wait is bounded; a wait that runs out records its role in the
@@ -131,6 +135,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Every CTA of this persistent grid is resident: let the norm/RoPE pass launch now.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) atomicMin(&a.stamps[0], globaltimer_ns());
 
   const int num_tiles = g.m_tiles * g.n_tiles;
 
@@ -144,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int issued = 0;
       bool ok = (a.flags & kFlagTestStall) == 0;
       for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int m_blk = tile / g.n_tiles;
-        const int n_blk = tile - m_blk * g.n_tiles;
+        int m_blk, n_blk;
+        tile_coords(g, tile, m_blk, n_blk);
         for (int kb = 0; kb < g.k_stages; ++kb) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             record_failure(a.status, abort_flag, kErrProducerEmptyWait);
@@ -244,14 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    const uint64_t pol_out = policy_evict_first();
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row_local = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m_blk = tile / g.n_tiles;
-      const int n_blk = tile - m_blk * g.n_tiles;
+      int m_blk, n_blk;
+      tile_coords(g, tile, m_blk, n_blk);
       bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
@@ -318,9 +326,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t packed[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-          uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-          dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          // final values nothing here reads again: first out of L2
+          st_global_v4_hint(orow + col0, packed[0], packed[1], packed[2], packed[3], pol_out);
+          st_global_v4_hint(orow + col0 + 8, packed[4], packed[5], packed[6], packed[7], pol_out);
         }
       }
       tc_fence_before();
@@ -330,6 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (col_base < a.q_end) atomicAdd(&a.sumsq[2 * static_cast<size_t>(row)], ss_q);
         if (col_base + BN > a.q_end && col_base < a.k_end)
           atomicAdd(&a.sumsq[2 * static_cast<size_t>(row) + 1], ss_k);
+      }
+      // Publish this warp's 32 rows of a Q/K tile: its stores and sums, then the counter.
+      if (n_blk < g.n_qk_tiles) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.ready + m_blk, 1u);
       }
       if (++acc == C::ACC_STAGES) {
         acc = 0;
@@ -346,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+  if (threadIdx.x == 0) atomicMax(&a.stamps[1], globaltimer_ns());
 }
 
 // Repack W's UE8M0 scales [I, H/32] into, per (N tile, K stage), SF_CHUNKS blocks of
@@ -356,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the tile) get 127. Also clears the status word and the sum-of-squares buffer.
 __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __restrict__ packed, int I,
                                 int k_blocks, int tile_n, int n_tiles, int k_stages, int sf_chunks,
-                                float* __restrict__ sumsq, size_t sumsq_count, uint32_t* status) {
+                                float* __restrict__ sumsq, size_t sumsq_count, uint32_t* __restrict__ ready,
+                                int m_tiles, uint32_t* status, unsigned long long* stamps) {
   const size_t words = static_cast<size_t>(n_tiles) * k_stages * sf_chunks * 128;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   const size_t first = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -377,7 +393,12 @@ __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __re
     packed[w] = v;
   }
   for (size_t i = first; i < sumsq_count; i += stride) sumsq[i] = 0.0f;
-  if (first == 0 && status != nullptr) *status = 0u;
+  for (size_t i = first; i < static_cast<size_t>(m_tiles); i += stride) ready[i] = 0u;
+  if (first == 0) {
+    *status = 0u;
+    stamps[0] = stamps[2] = ~0ull;
+    stamps[1] = stamps[3] = 0ull;
+  }
 }
 
 template <int BN>
@@ -413,7 +434,8 @@ size_t gemm_smem_bytes(int tile_n) {
 }
 
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
-                        size_t sumsq_count, uint32_t* status, cudaStream_t s, int num_sms) {
+                        size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
+                        cudaStream_t s, int num_sms) {
   const size_t words = static_cast<size_t>(g.n_tiles) * g.k_stages * g.sf_chunks * 128;
   const size_t work = words > sumsq_count ? words : sumsq_count;
   size_t blocks = (work + 255) / 256;
@@ -422,7 +444,7 @@ cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_pac
   if (blocks == 0) blocks = 1;
   qkv_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
       w_sf, reinterpret_cast<uint32_t*>(sf_packed), g.I, g.H / 32, g.tile_n, g.n_tiles, g.k_stages,
-      g.sf_chunks, sumsq, sumsq_count, status);
+      g.sf_chunks, sumsq, sumsq_count, ready, g.m_tiles, status, stamps);
   return cudaGetLastError();
 }
 

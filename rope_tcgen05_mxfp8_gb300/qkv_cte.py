@@ -27,6 +27,7 @@ QKV_CTE_LAYOUT_BSD = 0
 QKV_CTE_LAYOUT_NBSD = 1
 QKV_CTE_FLAG_TEST_STALL = 0x1
 QKV_CTE_FLAG_PROFILE = 0x2
+QKV_CTE_FLAG_SERIAL_PASSES = 0x4
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
             "qkv_cte_last_error", "qkv_cte_version")
@@ -174,8 +175,8 @@ def qkv_cte_status(workspace, stream=None) -> int:
 
 
 def qkv_cte_pass_times(plan):
-    """(prep, GEMM, norm+RoPE) device milliseconds of the plan's latest run."""
-    ms = (ctypes.c_float * 3)()
+    """(prep, GEMM, norm+RoPE, whole run) device milliseconds of the plan's latest run."""
+    ms = (ctypes.c_float * 4)()
     _check(load().qkv_cte_pass_times(plan, ms))
     return tuple(float(x) for x in ms)
 

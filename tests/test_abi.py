@@ -109,7 +109,8 @@ def test_workspace_size_formula():
         sf = n_tiles * (5120 // 128) * (-(-tile // 128)) * 512
         ss = -(-(T * 8) // 256) * 256
         qk = -(-(T * (nq + nkv) * 128 * 4) // 256) * 256   # fp32 Q/K hand-off (norm on)
-        assert ws == 256 + ss + -(-sf // 256) * 256 + qk
+        ready = -(-(-(-T // 128) * 4) // 256) * 256        # per-panel counters
+        assert ws == 256 + ss + -(-sf // 256) * 256 + ready + qk
 
 
 def test_run_rejects_null_plan_without_launch():

@@ -127,3 +127,41 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     op2, out2, ss2, inv2 = run_path(call, g)
     op2.status()
     check_outputs(call, inp, out2, ss2, inv2, name="after_timeout")
+
+
+@pytest.mark.parametrize("name", ["tiny", "edge"])
+def test_serial_and_overlapped_passes_agree(name):
+    """The norm/RoPE pass launched after the GEMM (serial flag) and overlapped with it
+    (the default, gated on per-panel ready counters) give the same, correct result."""
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_SERIAL_PASSES
+
+    if name == "tiny":
+        call = wl.workload("tiny")[0]
+    else:
+        call = wl.custom_call(name="edge", tokens=1000, hidden=1024, n_q_heads=3, n_kv_heads=2, d_head=128,
+                              seed=77, has_w_col_scale=True)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op_a, out_a, ss_a, inv_a = run_path(call, g)
+    op_b, out_b, ss_b, inv_b = run_path(call, g, flags=QKV_CTE_FLAG_SERIAL_PASSES)
+    op_a.status()
+    op_b.status()
+    check_outputs(call, inp, out_a, ss_a, inv_a, name=f"{name}_overlapped")
+    check_outputs(call, inp, out_b, ss_b, inv_b, name=f"{name}_serial")
+    diff = (out_a.float() - out_b.float()).abs()
+    assert float(diff.max()) <= 2 ** -6 * float(out_a.float().abs().max())
+
+
+def test_pass_times_reported():
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_PROFILE
+
+    call = wl.workload("short")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_PROFILE)
+    prep, gemm, norm, run = op.pass_times()
+    op.status()
+    assert prep > 0 and gemm > 0 and norm > 0 and run > 0
+    assert run >= gemm
+    flops = call.flops / (gemm * 1e-3) / 1e12
+    assert 10 < flops < 6000, f"implausible GEMM rate {flops} TFLOP/s"

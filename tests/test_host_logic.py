@@ -1,0 +1,37 @@
+"""Host-side logic of the library, compiled with g++ and run on the CPU."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+CSRC = os.path.join(ROOT, "rope_tcgen05_mxfp8_gb300", "csrc")
+
+
+@pytest.fixture(scope="module")
+def bands_bin(tmp_path_factory):
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no g++")
+    out = str(tmp_path_factory.mktemp("host") / "bands_check")
+    cmd = [gxx, "-std=c++17", "-O1", "-I", CSRC, "-I", "/usr/local/cuda/include",
+           os.path.join(ROOT, "tests", "host", "bands_check.cpp"), "-o", out]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+@pytest.mark.parametrize("T,H,I,tile_n,k_end,band", [
+    (32760, 5120, 15360, 240, 10240, 45),   # Wan 480p: one V band, one Q/K band
+    (32760, 5120, 15360, 240, 10240, 10),
+    (75600, 5120, 15360, 256, 10240, 1),    # one N tile per band: capped at 16 bands
+    (256, 512, 1536, 240, 1024, 3),
+    (1, 256, 640, 128, 512, 2),
+    (4096, 5120, 5120, 240, 5120, 45),      # separate mode: every tile is Q
+    (129, 384, 576, 192, 448, 1000),
+])
+def test_banded_tile_order_covers_every_tile_once(bands_bin, T, H, I, tile_n, k_end, band):
+    r = subprocess.run([bands_bin, str(T), str(H), str(I), str(tile_n), str(k_end), str(band)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("ok")
