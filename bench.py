@@ -313,10 +313,12 @@ def run_ours(args):
     hbm_gbs, bf16, bf16_sus, peak_src = _peaks()
     fp8_peak = bf16 * FP8_PER_BF16
     k1_achieved = flops / (gemm_ms * 1e-3) / 1e12
-    # norm + RoPE bytes this design must move: read the fp32 Q/K hand-off, write the
-    # bf16 Q/K columns of O, read the fp32 cos/sin rows and the fp32 [T, 2] sums
+    # norm + RoPE bytes this design must move: read the Q/K hand-off (2 bytes per
+    # value plus one exponent byte per 16), write the bf16 Q/K columns of O, read the
+    # fp32 cos/sin rows and the fp32 [T, 2] sums
     qk_cols = (call.n_q_heads + call.n_kv_heads) * call.d_head
-    k2_bytes = (4 + 2) * call.tokens * qk_cols + 2 * 4 * call.tokens * call.d_head + 8 * call.tokens
+    k2_bytes = (2 + 2) * call.tokens * qk_cols + call.tokens * qk_cols // 16 \
+        + 2 * 4 * call.tokens * call.d_head + 8 * call.tokens
     k2_gbs = k2_bytes / (norm_ms * 1e-3) / 1e9 if norm_ms > 0 else None
 
     e2e = None

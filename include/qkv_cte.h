@@ -30,8 +30,8 @@
  *   is caller-allocated device memory of the size qkv_cte_plan reports; it holds the
  *   per-call scratch (repacked weight scales, the sum-of-squares accumulator, a device
  *   status word, per-panel completion counters, timing stamps and, when a norm or RoPE
- *   pass runs, the un-normalised Q and K columns in fp32: 4*T*(n_q + n_kv)*d_head
- *   bytes) and must not be shared by calls that overlap on the GPU. The norm/RoPE
+ *   pass runs, the un-normalised Q and K columns in block floating point: about
+ *   2.06*ceil(T/128)*128*(n_q + n_kv)*d_head bytes) and must not be shared by calls that overlap on the GPU. The norm/RoPE
  *   kernel is launched as a programmatic dependent of the GEMM so the two overlap. qkv_cte_run is stream-ordered and asynchronous: it never
  *   synchronises. O must not alias any input.
  *
@@ -111,8 +111,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
  * gamma_q    : bf16   [n_q*d_head] segment-wide Q gamma; required iff norm; 16-byte aligned
  * gamma_k    : bf16   [n_kv*d_head] K gamma; required iff norm and n_kv > 0, else NULL
  * cos_table, sin_table: fp32 [T, d_head] rotate-half tables; required iff rope, else NULL;
- *              16-byte aligned
- * O          : bf16   [T, I] (BSD) output; 16-byte aligned; must not alias any input
+ *              32-byte aligned
+ * O          : bf16   [T, I] (BSD) output; 32-byte aligned; must not alias any input
  * sumsq      : fp32   [T, 2] or NULL: per-token sum of o^2 over the un-normalised Q and K
  *              segments ([qkv_cte] "Design" 1 step a; column 1 is 0 when n_kv == 0)
  * inv_rms    : fp32   [T, 2] or NULL: the rsqrt factors of step b (written iff norm)

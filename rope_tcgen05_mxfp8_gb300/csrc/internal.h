@@ -21,20 +21,26 @@ enum : uint32_t {
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)                 status word (offset 0) and, at kStampOffset, four uint64
-//                            %globaltimer stamps: K1 first start, K1 last end, K2 first
-//                            start, K2 last end
+//                            %globaltimer stamps:
+//                            K1 first start, K1 last end, K2 first start, K2 last end
 //   [256, 256 + ss_bytes)    fp32 [T, 2] sum-of-squares accumulator (used when the
 //                            caller passes no sumsq buffer)
 //   [.., + sf_bytes)         W's UE8M0 scales repacked per (N tile, K stage) in the
 //                            order the MMA's scale-factor copy consumes them
 //   [.., + ready_bytes)      uint32 [m_tiles]: per 128-row panel, how many epilogue
 //                            warp-tiles of K1's Q/K tiles have finished (4 per tile)
-//   [.., + qk_bytes)         fp32 [T, I_q + I_k]: the un-normalised Q and K columns,
-//                            handed from K1 to K2 (only when a norm/RoPE pass runs)
+//   [.., + qk_bytes)         the un-normalised Q and K columns handed from K1 to K2
+//                            (only when a norm/RoPE pass runs) in block floating
+//                            point: per row and 16-column chunk, one power-of-two
+//                            exponent byte E and 16 fp16 values f with
+//                            value = f * 2^(E-127), |f| < 2. Tile-major: for row t and
+//                            chunk k < k_end/16, idx = (t/128 * k_end/16 + k) * 128
+//                            + t%128; the 16 fp16 sit at qk_val[idx*16 ..] (32 bytes)
+//                            and the exponent at qk_exp[idx]
 constexpr size_t kStampOffset = 64;
 
 struct WorkspaceLayout {
-  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, total;
+  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, qk_exp_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -46,9 +52,9 @@ constexpr int kMaxBands = 16;
 // Tile order: the N tiles are cut into bands (contiguous runs of N tiles). The
 // persistent grid walks the bands one after the other and, inside a band, row panel
 // by row panel (m outer, n inner), so the CTAs running at any moment share one band's
-// slab of W, which stays resident in L2 while A streams through. Bands of tiles that
-// hold only V columns come first; the bands of tiles holding Q or K columns come last,
-// so the norm/RoPE pass (which waits for a panel's Q/K tiles only) overlaps them.
+// slab of W, which stays resident in L2 while A streams through. The bands of tiles
+// holding Q or K columns come first and the V-only bands last: the norm/RoPE pass
+// waits only for a panel's Q/K tiles, so it overlaps the V bands.
 struct GemmShape {
   int T, H, I;
   int tile_n;       // N tile (columns of O per tile)
@@ -71,10 +77,10 @@ __host__ __device__ inline void tile_coords(const GemmShape& g, int tile, int& m
   n = g.band_n0[b] + (local - m * nc);
 }
 
-// Cut [0, n_tiles) into bands of at most `band_tiles` N tiles, V-only tiles first.
+// Cut [0, n_tiles) into bands of at most `band_tiles` N tiles, Q/K tiles first.
 inline void make_bands(GemmShape& g, int band_tiles) {
   if (band_tiles < 1) band_tiles = 1;
-  const int runs[2][2] = {{g.n_qk_tiles, g.n_tiles - g.n_qk_tiles}, {0, g.n_qk_tiles}};
+  const int runs[2][2] = {{0, g.n_qk_tiles}, {g.n_qk_tiles, g.n_tiles - g.n_qk_tiles}};
   int need = 0;
   for (const auto& r : runs) need += (r[1] + band_tiles - 1) / band_tiles;
   while (need > kMaxBands) {
@@ -103,7 +109,8 @@ struct GemmArgs {
   const uint16_t* bias;      // may be null
   const uint8_t* sf_packed;
   uint16_t* O;
-  float* qk;                 // fp32 [T, k_end] Q/K hand-off, or null: Q/K go to O as bf16
+  uint16_t* qk_val;          // Q/K hand-off fp16 values, or null: Q/K go to O as bf16
+  uint8_t* qk_exp;           // Q/K hand-off exponent bytes
   float* sumsq;              // may be null: then no sum of squares is accumulated
   uint32_t* ready;           // per-panel completion counters (K2 overlaps K1 on them)
   unsigned long long* stamps;  // [0] first CTA start (min), [1] last CTA end (max)
@@ -117,7 +124,8 @@ struct NormRopeArgs {
   int norm, rope;
   float eps;
   const float* sumsq;
-  const float* qk;           // fp32 [T, (n_q + n_kv) * d_head] un-normalised Q and K
+  const uint16_t* qk_val;    // block floating point hand-off of the un-normalised Q/K
+  const uint8_t* qk_exp;
   const uint16_t* gamma_q;
   const uint16_t* gamma_k;
   const float* cos_t;

@@ -10,14 +10,17 @@
 // On one GPU every head is local, so the page's cross-rank AllReduce of the sums is
 // the identity: K1 already summed over every column tile of the row. The pass is
 // launched as a programmatic dependent of K1: its blocks run beside K1's persistent
-// CTAs and take each 16-row unit once K1's counter says the unit's 128-row panel is
+// CTAs and take each 32-row unit once K1's counter says the unit's 128-row panel is
 // complete (a bounded acquire wait), so it mostly hides under the GEMM. The page writes
 // the un-normalised Q/K into the output and re-reads it; here K1 hands them over in
-// fp32 (a workspace buffer) so the result is rounded to bf16 once, here. This pass
-// is HBM-bound: each thread reads 8 lanes of the low half of a head and the 8
-// partner lanes d/2 away (2 x 32 bytes of fp32) and writes 2 x 16 bytes of bf16 to
-// O, with the per-position cos/sin and the gamma vectors served from L1/L2.
+// block floating point (fp16 with a power-of-two exponent per row and 16 columns, in
+// a tile-major workspace buffer), so the result is rounded to bf16 once, here. This
+// pass is HBM-bound. Lanes map to rows: a warp reads the hand-off with 1 KB
+// coalesced loads, keeps its row's cos/sin chunk and inv_rms in registers across all
+// heads, reads gamma as warp-wide broadcasts, and writes one full 32-byte sector of
+// O per row and half-head.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 
@@ -34,32 +37,10 @@ __device__ __forceinline__ void unpack8(const uint4 v, float (&f)[8]) {
   }
 }
 
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-  uint32_t w[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    __nv_bfloat162 b = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
-    w[j] = *reinterpret_cast<uint32_t*>(&b);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
 
-__device__ __forceinline__ void load8f(const float* p, float (&f)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
 
-// Data another kernel wrote while this one runs: read through L2 (not L1).
-__device__ __forceinline__ void load8f_l2(const float* p, float (&f)[8]) {
-  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldcg(reinterpret_cast<const float4*>(p) + 1);
-  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
-}
 
-constexpr int kUnitRows = 16;                       // rows per work unit (divides 128)
+constexpr int kThreads = 128;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -68,105 +49,165 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
-// Wait (bounded) until K1 has finished every tile of the row panel.
-__device__ bool wait_panel_ready(const uint32_t* flag, uint32_t target) {
-  if (ld_acquire(flag) >= target) return true;
-  uint64_t t0;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-  while (true) {
-    __nanosleep(500);
-    if (ld_acquire(flag) >= target) return true;
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    if (t - t0 > kWaitLimitNs) return false;
-  }
-}
-
 __device__ __forceinline__ unsigned long long now_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
 
-__global__ void __launch_bounds__(256) qk_norm_rope_kernel(const NormRopeArgs p) {
-  __shared__ int s_ok;
+// Wait (bounded) until K1 has finished every Q/K tile of the row panel.
+__device__ bool wait_panel_ready(const uint32_t* flag, uint32_t target) {
+  if (ld_acquire(flag) >= target) return true;
+  const unsigned long long t0 = now_ns();
+  while (true) {
+    __nanosleep(500);
+    if (ld_acquire(flag) >= target) return true;
+    if (now_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ void st_global_v8_b32(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
+// One hand-off chunk of a row: 16 fp16 (32 bytes) and the exponent byte, read
+// through L2 (written by the GEMM while this kernel runs), decoded to fp32.
+__device__ __forceinline__ void load_handoff16(const uint16_t* val, const uint8_t* ex, float* f) {
+  uint32_t w[8];
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "l"(val)
+               : "memory");
+  uint16_t e;
+  asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(e) : "l"(ex) : "memory");
+  const float up = __uint_as_float(static_cast<uint32_t>(e) << 23);  // 2^(e - 127)
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+    f[2 * j] = p.x * up;
+    f[2 * j + 1] = p.y * up;
+  }
+}
+
+__device__ __forceinline__ void ld_v8_nc(const float* p, float* v) {
+  asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+
+__device__ __forceinline__ void load_gamma16(const uint16_t* g, float* f) {
+  const uint4 a = __ldg(reinterpret_cast<const uint4*>(g));
+  const uint4 b = __ldg(reinterpret_cast<const uint4*>(g) + 1);
+  unpack8(a, *reinterpret_cast<float(*)[8]>(f));
+  unpack8(b, *reinterpret_cast<float(*)[8]>(f + 8));
+}
+
+// One warp task = 32 consecutive rows (one per lane) x one 16-column chunk c of the
+// low half of every head, with its partner chunk d/2 away: the rotation pairs lane
+// j with lane j + d/2 inside each head.
+__global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeArgs p) {
   if (threadIdx.x == 0) atomicMin(&p.stamps[0], now_ns());
-  const int chunks = p.d_head / 16;  // 8-lane chunks in the low half of one head
-  const int half = p.d_head / 2;
-  const int qk_width = (p.n_q + p.n_kv) * p.d_head;
-  const int per_row = (p.n_q + p.n_kv) * chunks;
-  const int n_units = (p.T + kUnitRows - 1) / kUnitRows;
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-    const int row0 = u * kUnitRows;
-    const int rows = min(kUnitRows, p.T - row0);
-    if (threadIdx.x == 0) {
-      const bool ok = wait_panel_ready(p.ready + row0 / 128, p.ready_target);
-      if (!ok) atomicOr(p.status, kErrNormReadyWait);
-      s_ok = ok ? 1 : 0;
+  const int lane = threadIdx.x & 31;
+  const int d = p.d_head;
+  const int half = d / 2;
+  const int chunks = d / 32;  // 16-column chunks in the low half of a head
+  const int heads = p.n_q + p.n_kv;
+  const int qk_chunks = heads * d / 16;
+  const long long units = (p.T + 31) / 32;
+  const long long tasks = units * chunks;
+  const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
+  for (long long task = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); task < tasks;
+       task += warps) {
+    const int u = static_cast<int>(task / chunks);
+    const int c = static_cast<int>(task - static_cast<long long>(u) * chunks);
+    const int row0 = u * 32;
+    const int t = row0 + lane;
+    const bool row_ok = t < p.T;
+    const int panel = row0 >> 7;
+    int ok = 1;
+    if (lane == 0) ok = wait_panel_ready(p.ready + panel, p.ready_target) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) {
+      if (lane == 0) atomicOr(p.status, kErrNormReadyWait);
+      break;
     }
-    __syncthreads();
-    if (!s_ok) break;  // uniform across the block
-    const int items = rows * per_row;
-#pragma unroll 2
-    for (int it = threadIdx.x; it < items; it += blockDim.x) {
-      const int tr = it / per_row;
-      const int rem = it - tr * per_row;
-      const int t = row0 + tr;
-      const int hg = rem / chunks;
-      const int c = rem - hg * chunks;
+    (void)ld_acquire(p.ready + panel);  // each lane acquires the panel's publication
+    const int tr = row_ok ? t : p.T - 1;
+
+    float inv_q = 1.0f, inv_k = 1.0f;
+    if (p.norm) {
+      inv_q = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr)] / static_cast<float>(p.n_q * d) + p.eps);
+      if (p.n_kv > 0)
+        inv_k = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr) + 1] / static_cast<float>(p.n_kv * d) + p.eps);
+    }
+    float cl[16], ch[16], sl[16], sh[16];
+    if (p.rope) {
+      const float* cr = p.cos_t + static_cast<size_t>(tr) * d + c * 16;
+      const float* sr = p.sin_t + static_cast<size_t>(tr) * d + c * 16;
+      ld_v8_nc(cr, cl);
+      ld_v8_nc(cr + 8, cl + 8);
+      ld_v8_nc(cr + half, ch);
+      ld_v8_nc(cr + half + 8, ch + 8);
+      ld_v8_nc(sr, sl);
+      ld_v8_nc(sr + 8, sl + 8);
+      ld_v8_nc(sr + half, sh);
+      ld_v8_nc(sr + half + 8, sh + 8);
+    }
+    const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (row0 & 127) + lane;
+    uint16_t* orow = p.O + static_cast<size_t>(tr) * p.I;
+    for (int hg = 0; hg < heads; ++hg) {
       const int seg = hg >= p.n_q ? 1 : 0;
       const int h = seg ? hg - p.n_q : hg;
-      const int n_heads = seg ? p.n_kv : p.n_q;
-      const int off = h * p.d_head + c * 8;  // column inside the segment
-      const int seg_base = seg ? p.n_q * p.d_head : 0;
-      uint16_t* row = p.O + static_cast<size_t>(t) * p.I + seg_base;
-      const float* src = p.qk + static_cast<size_t>(t) * qk_width + seg_base + off;
-
-      float lo[8], hi[8];
-      load8f_l2(src, lo);
-      load8f_l2(src + half, hi);
-
+      const int off = h * d + c * 16;                 // column inside the segment
+      const int col = (seg ? p.n_q * d : 0) + off;    // column of O (low half)
+      float lo[16], hi[16];
+      const size_t i_lo = idx0 + static_cast<size_t>(col >> 4) * 128;
+      const size_t i_hi = idx0 + static_cast<size_t>((col + half) >> 4) * 128;
+      load_handoff16(p.qk_val + i_lo * 16, p.qk_exp + i_lo, lo);
+      load_handoff16(p.qk_val + i_hi * 16, p.qk_exp + i_hi, hi);
       if (p.norm) {
-        const float ss = p.sumsq[2 * static_cast<size_t>(t) + seg];
-        const float inv = 1.0f / sqrtf(ss / static_cast<float>(n_heads * p.d_head) + p.eps);
         const uint16_t* gamma = seg ? p.gamma_k : p.gamma_q;
-        float glo[8], ghi[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off)), glo);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off + half)), ghi);
+        const float inv = seg ? inv_k : inv_q;
+        float glo[16], ghi[16];
+        load_gamma16(gamma + off, glo);
+        load_gamma16(gamma + off + half, ghi);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 16; ++j) {
           lo[j] = lo[j] * inv * glo[j];
           hi[j] = hi[j] * inv * ghi[j];
         }
-        if (p.inv_rms != nullptr && h == 0 && c == 0) {
-          p.inv_rms[2 * static_cast<size_t>(t) + seg] = inv;
-          if (p.n_kv == 0) p.inv_rms[2 * static_cast<size_t>(t) + 1] = 0.0f;
-        }
       }
       if (p.rope) {
-        const float* cr = p.cos_t + static_cast<size_t>(t) * p.d_head + c * 8;
-        const float* sr = p.sin_t + static_cast<size_t>(t) * p.d_head + c * 8;
-        float cl[8], ch[8], sl[8], sh[8];
-        load8f(cr, cl);
-        load8f(cr + half, ch);
-        load8f(sr, sl);
-        load8f(sr + half, sh);
-        float olo[8], ohi[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          olo[j] = lo[j] * cl[j] - hi[j] * sl[j];
-          ohi[j] = hi[j] * ch[j] + lo[j] * sh[j];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          lo[j] = olo[j];
-          hi[j] = ohi[j];
+        for (int j = 0; j < 16; ++j) {
+          const float a = lo[j] * cl[j] - hi[j] * sl[j];
+          const float b = hi[j] * ch[j] + lo[j] * sh[j];
+          lo[j] = a;
+          hi[j] = b;
         }
       }
-      *reinterpret_cast<uint4*>(row + off) = pack8(lo);
-      *reinterpret_cast<uint4*>(row + off + half) = pack8(hi);
+      if (row_ok) {
+        uint32_t w[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162 v = __floats2bfloat162_rn(lo[2 * j], lo[2 * j + 1]);
+          w[j] = *reinterpret_cast<uint32_t*>(&v);
+        }
+        st_global_v8_b32(orow + col, w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          __nv_bfloat162 v = __floats2bfloat162_rn(hi[2 * j], hi[2 * j + 1]);
+          w[j] = *reinterpret_cast<uint32_t*>(&v);
+        }
+        st_global_v8_b32(orow + col + half, w);
+      }
     }
-    __syncthreads();  // s_ok is rewritten for the next unit
+    if (c == 0 && row_ok && p.norm && p.inv_rms != nullptr) {
+      p.inv_rms[2 * static_cast<size_t>(t)] = inv_q;
+      p.inv_rms[2 * static_cast<size_t>(t) + 1] = p.n_kv > 0 ? inv_k : 0.0f;
+    }
   }
   if (threadIdx.x == 0) atomicMax(&p.stamps[1], now_ns());
 }
@@ -175,12 +216,13 @@ __global__ void __launch_bounds__(256) qk_norm_rope_kernel(const NormRopeArgs p)
 
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap) {
   if (!a.norm && !a.rope) return cudaSuccess;
-  const int n_units = (a.T + kUnitRows - 1) / kUnitRows;
-  if (n_units == 0) return cudaSuccess;
-  const int blocks = n_units < 2 * num_sms ? n_units : 2 * num_sms;
+  const long long tasks = static_cast<long long>((a.T + 31) / 32) * (a.d_head / 32);
+  if (tasks == 0) return cudaSuccess;
+  long long blocks = (tasks + kThreads / 32 - 1) / (kThreads / 32);
+  if (blocks > 2LL * num_sms) blocks = 2LL * num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

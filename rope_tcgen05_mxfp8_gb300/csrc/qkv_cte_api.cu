@@ -193,7 +193,9 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   w.ready_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
   w.qk_off = w.ready_off + align_up((size_t)g.m_tiles * sizeof(uint32_t), 256);
   const bool second_pass = d.norm || d.rope;
-  w.total = w.qk_off + (second_pass ? align_up((size_t)g.T * p->k_end * sizeof(float), 256) : 0);
+  const size_t hand_rows = second_pass ? (size_t)g.m_tiles * 128 : 0;
+  w.qk_exp_off = w.qk_off + align_up(hand_rows * p->k_end * sizeof(uint16_t), 256);
+  w.total = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
   *workspace_bytes = w.total;
   *out = p;
   return ok();
@@ -247,14 +249,15 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (gamma_q && !d.norm) return fail(QKV_CTE_ERR_INVALID, "gamma_q given but norm is off");
   if (d.rope && (!cos_table || !sin_table)) return fail(QKV_CTE_ERR_INVALID, "rope needs cos and sin tables");
   if (!d.rope && (cos_table || sin_table)) return fail(QKV_CTE_ERR_INVALID, "cos/sin given but rope is off");
-  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(O, 16))
-    return fail(QKV_CTE_ERR_UNSUPPORTED, "A, W and O must be 16-byte aligned");
+  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(O, 32))
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "A and W must be 16-byte aligned and O 32-byte aligned");
   if (!aligned(a_scale, 4) || !aligned(w_sf, 4) || (sumsq && !aligned(sumsq, 4)) || (inv_rms && !aligned(inv_rms, 4)))
     return fail(QKV_CTE_ERR_UNSUPPORTED, "a_scale, w_sf, sumsq and inv_rms must be 4-byte aligned");
   if ((w_col_scale && !aligned(w_col_scale, 16)) || (bias && !aligned(bias, 16)) ||
-      (gamma_q && !aligned(gamma_q, 16)) || (gamma_k && !aligned(gamma_k, 16)) ||
-      (cos_table && !aligned(cos_table, 16)) || (sin_table && !aligned(sin_table, 16)))
-    return fail(QKV_CTE_ERR_UNSUPPORTED, "w_col_scale, bias, gamma and cos/sin must be 16-byte aligned");
+      (gamma_q && !aligned(gamma_q, 16)) || (gamma_k && !aligned(gamma_k, 16)))
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "w_col_scale, bias and gamma must be 16-byte aligned");
+  if ((cos_table && !aligned(cos_table, 32)) || (sin_table && !aligned(sin_table, 32)))
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "cos and sin tables must be 32-byte aligned");
   if (!aligned(workspace, 256)) return fail(QKV_CTE_ERR_UNSUPPORTED, "workspace must be 256-byte aligned");
   if (workspace_bytes < plan->ws.total)
     return fail(QKV_CTE_ERR_INVALID, "workspace of %zu bytes is smaller than the planned %zu",
@@ -304,8 +307,10 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.bias = bias;
   ga.sf_packed = sf_packed;
   ga.O = O;
-  float* qk = (d.norm || d.rope) ? reinterpret_cast<float*>(ws + plan->ws.qk_off) : nullptr;
-  ga.qk = qk;
+  uint16_t* qk_val = (d.norm || d.rope) ? reinterpret_cast<uint16_t*>(ws + plan->ws.qk_off) : nullptr;
+  uint8_t* qk_exp = (d.norm || d.rope) ? ws + plan->ws.qk_exp_off : nullptr;
+  ga.qk_val = qk_val;
+  ga.qk_exp = qk_exp;
   ga.sumsq = need_ss ? ss : nullptr;
   ga.ready = ready;
   ga.stamps = stamps;
@@ -326,7 +331,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.rope = d.rope;
   na.eps = d.eps;
   na.sumsq = ss;
-  na.qk = qk;
+  na.qk_val = qk_val;
+  na.qk_exp = qk_exp;
   na.gamma_q = gamma_q;
   na.gamma_k = gamma_k;
   na.cos_t = cos_table;

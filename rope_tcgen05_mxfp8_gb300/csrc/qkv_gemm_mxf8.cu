@@ -20,9 +20,11 @@
 //   * warps 2-5: epilogue. tcgen05.ld the accumulator (one TMEM lane = one row per
 //     thread), apply the row scale / column scale / bias, accumulate the Q and K sums
 //     of squares in fp32 and add them to sumsq[T, 2] with one atomic per row and
-//     segment. V columns are stored as final bf16. Q and K columns are stored in fp32
-//     to a workspace hand-off buffer when the norm/RoPE pass follows (so the only
-//     rounding to bf16 is the final one), else as bf16. With two accumulator stages
+//     segment. V columns are stored as final bf16. Q and K columns go to a
+//     tile-major workspace hand-off when the norm/RoPE pass follows, in block
+//     floating point (fp16 with a power-of-two exponent per row and 16 columns: 11
+//     significant bits, any range), so the bf16 rounding happens once, at the end,
+//     and the stores coalesce whatever row a thread owns; else as bf16. With two accumulator stages
 //     the epilogue of tile j overlaps the MMAs of tile j+1. After each tile every
 //     epilogue warp fences its stores and bumps its row panel's ready counter; the
 //     norm/RoPE pass, launched as a programmatic dependent of this grid, starts on a
@@ -33,6 +35,7 @@
 // status word and the CTA unwinds, waiting for its own copies and MMAs before it
 // releases TMEM.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -77,6 +80,11 @@ __device__ __forceinline__ void record_failure(uint32_t* status, volatile int* a
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -251,10 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    // Each warp owns 32 rows (its TMEM lane quarter) of every tile, one row per
+    // thread. Per 16 columns: o = acc * (a_scale * w_col_scale) + bias, the Q/K sum
+    // of squares (a 16-column chunk never straddles a segment boundary: both are
+    // multiples of 16), then one 32-byte store. Q/K chunks go to the hand-off in
+    // block floating point (16 fp16 scaled by the chunk's power-of-two exponent,
+    // tile-major, so the warp's store writes 1 KB of consecutive memory); V goes to
+    // O row-major as final bf16 (one full 32-byte sector per row).
     const uint64_t pol_out = policy_evict_first();
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
     const int row_local = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int qk_chunks = a.k_end >> 4;
+    const size_t qk_panel_idx0 = static_cast<size_t>(row_local);
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -272,63 +289,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float ascale = row_ok ? a.a_scale[row] : 0.0f;
       const int col_base = n_blk * BN;
       uint16_t* orow = a.O + static_cast<size_t>(row_ok ? row : 0) * g.I;
+      const size_t qk_row_idx = static_cast<size_t>(m_blk) * qk_chunks * 128 + qk_panel_idx0;
       float ss_q = 0.0f, ss_k = 0.0f;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(t_lane + static_cast<uint32_t>(acc * BN + c0), r);
+#pragma unroll
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        uint32_t r[32];
+        const uint32_t taddr = t_lane + static_cast<uint32_t>(acc * BN + c0);
+        if (c0 + 32 <= BN)
+          tmem_ld_32x32b_x32(taddr, r);
+        else
+          tmem_ld_32x32b_x16(taddr, r);
         tmem_ld_wait();
-        const int col0 = col_base + c0;
-        if (col0 >= g.I) continue;  // ragged last N tile (uniform across the warp)
-        float cs[16];
-        if (a.w_col_scale != nullptr) {
-          const float4* p = reinterpret_cast<const float4*>(a.w_col_scale + col0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 v = __ldg(p + q);
-            cs[4 * q + 0] = v.x;
-            cs[4 * q + 1] = v.y;
-            cs[4 * q + 2] = v.z;
-            cs[4 * q + 3] = v.w;
+        for (int h = 0; h < 2; ++h) {
+          if (c0 + 16 * h >= BN) break;
+          const int col0 = col_base + c0 + 16 * h;
+          if (col0 >= g.I) break;  // ragged last N tile (uniform across the warp)
+          float sc[16];
+          if (a.w_col_scale != nullptr) {
+            const float4* p = reinterpret_cast<const float4*>(a.w_col_scale + col0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 v4 = __ldg(p + q);
+              sc[4 * q + 0] = ascale * v4.x;
+              sc[4 * q + 1] = ascale * v4.y;
+              sc[4 * q + 2] = ascale * v4.z;
+              sc[4 * q + 3] = ascale * v4.w;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sc[j] = ascale;
           }
-        } else {
+          float bias[16];
+          if (a.bias != nullptr) {
+            const uint4* p = reinterpret_cast<const uint4*>(a.bias + col0);
+            const uint4 b0 = __ldg(p), b1 = __ldg(p + 1);
+            const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-          for (int j = 0; j < 16; ++j) cs[j] = 1.0f;
-        }
-        float bias[16];
-        if (a.bias != nullptr) {
-          const uint4* p = reinterpret_cast<const uint4*>(a.bias + col0);
-          const uint4 b0 = __ldg(p), b1 = __ldg(p + 1);
-          const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            for (int j = 0; j < 8; ++j) {
+              bias[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
+              bias[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+            }
+          } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            bias[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
-            bias[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
+            for (int j = 0; j < 16; ++j) bias[j] = 0.0f;
           }
-        } else {
+          float v[16];
+          float sq = 0.0f;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) bias[j] = 0.0f;
-        }
-        float v[16];
+          for (int j = 0; j < 16; ++j) {
+            v[j] = fmaf(__uint_as_float(r[16 * h + j]), sc[j], bias[j]);
+            sq = fmaf(v[j], v[j], sq);
+          }
+          if (col0 < a.q_end) ss_q += sq; else if (col0 < a.k_end) ss_k += sq;
+          if (a.qk_val != nullptr && col0 < a.k_end) {
+            // Q/K columns that the norm/RoPE pass will finish: the chunk's exponent
+            // E = floor(log2 max|v|) (clamped; 0 for zero or non-finite maxima) and
+            // v * 2^-E in fp16, so every value keeps 11 significant bits relative
+            // to the chunk maximum whatever its range.
+            float m = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          v[j] = __uint_as_float(r[j]) * ascale * cs[j] + bias[j];
-          const int c = col0 + j;
-          if (c < a.q_end) ss_q += v[j] * v[j]; else if (c < a.k_end) ss_k += v[j] * v[j];
-        }
-        if (!row_ok) continue;
-        if (a.qk != nullptr && col0 < a.k_end) {
-          // Q/K columns that the norm/RoPE pass will finish: hand over in fp32
-          float4* dst = reinterpret_cast<float4*>(a.qk + static_cast<size_t>(row) * a.k_end + col0);
+            for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+            const int field = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu);
+            int e = (field == 0 || field == 255) ? 0 : field - 127;
+            e = e < -126 ? -126 : (e > 126 ? 126 : e);
+            const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+            uint32_t hv[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-          uint32_t packed[8];
+            for (int j = 0; j < 8; ++j) hv[j] = pack_f16x2(v[2 * j] * down, v[2 * j + 1] * down);
+            const size_t idx = qk_row_idx + static_cast<size_t>(col0 >> 4) * 128;
+            st_global_v8_b32(a.qk_val + idx * 16, hv);
+            a.qk_exp[idx] = static_cast<uint8_t>(e + 127);
+          } else if (row_ok) {
+            uint32_t packed[8];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-          // final values nothing here reads again: first out of L2
-          st_global_v4_hint(orow + col0, packed[0], packed[1], packed[2], packed[3], pol_out);
-          st_global_v4_hint(orow + col0 + 8, packed[4], packed[5], packed[6], packed[7], pol_out);
+            for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+            // final values nothing here reads again: first out of L2
+            st_global_v8_b32_hint(orow + col0, packed, pol_out);
+          }
         }
       }
       tc_fence_before();
@@ -368,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // n = tile*tile_n + 128*chunk + 32*c + r for K block 4*stage + kb. That is the
 // 32-row x 16-byte shared-memory image tcgen05.cp 32x128b.warpx4 turns into the
 // TMEM scale-factor layout of an M=128 block-scaled MMA. Columns past I (or past
-// the tile) get 127. Also clears the status word and the sum-of-squares buffer.
+// the tile) get 127. Also clears the status word, the panel counters, the timing
+// stamps and the sum-of-squares buffer.
 __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __restrict__ packed, int I,
                                 int k_blocks, int tile_n, int n_tiles, int k_stages, int sf_chunks,
                                 float* __restrict__ sumsq, size_t sumsq_count, uint32_t* __restrict__ ready,
@@ -395,7 +434,7 @@ __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __re
   for (size_t i = first; i < sumsq_count; i += stride) sumsq[i] = 0.0f;
   for (size_t i = first; i < static_cast<size_t>(m_tiles); i += stride) ready[i] = 0u;
   if (first == 0) {
-    *status = 0u;
+    status[0] = 0u;
     stamps[0] = stamps[2] = ~0ull;
     stamps[1] = stamps[3] = 0ull;
   }

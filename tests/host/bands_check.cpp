@@ -24,15 +24,15 @@ int main(int argc, char** argv) {
   if (g.band_tile0[g.n_bands] != total) { printf("bad total %d vs %d\n", g.band_tile0[g.n_bands], total); return 1; }
   if (g.n_bands > qkvcte::kMaxBands) { printf("too many bands\n"); return 1; }
   std::vector<int> seen(total, 0);
-  bool in_qk = false;
+  bool in_v = false;
   for (int t = 0; t < total; ++t) {
     int m, n;
     qkvcte::tile_coords(g, t, m, n);
     if (m < 0 || m >= g.m_tiles || n < 0 || n >= g.n_tiles) { printf("out of range at %d\n", t); return 1; }
     seen[m * g.n_tiles + n]++;
     const bool qk = n < g.n_qk_tiles;
-    if (in_qk && !qk) { printf("V tile after a Q/K tile at %d\n", t); return 1; }
-    in_qk = in_qk || qk;
+    if (in_v && qk) { printf("Q/K tile after a V tile at %d\n", t); return 1; }
+    in_v = in_v || !qk;
   }
   for (int i = 0; i < total; ++i)
     if (seen[i] != 1) { printf("tile %d visited %d times\n", i, seen[i]); return 1; }

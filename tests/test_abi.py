@@ -108,7 +108,9 @@ def test_workspace_size_formula():
         n_tiles = -(-I // tile)
         sf = n_tiles * (5120 // 128) * (-(-tile // 128)) * 512
         ss = -(-(T * 8) // 256) * 256
-        qk = -(-(T * (nq + nkv) * 128 * 4) // 256) * 256   # fp32 Q/K hand-off (norm on)
+        rows = -(-T // 128) * 128
+        kq = (nq + nkv) * 128
+        qk = -(-(rows * kq * 2) // 256) * 256 + -(-(rows * kq // 16) // 256) * 256  # hand-off
         ready = -(-(-(-T // 128) * 4) // 256) * 256        # per-panel counters
         assert ws == 256 + ss + -(-sf // 256) * 256 + ready + qk
 

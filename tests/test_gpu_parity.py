@@ -83,6 +83,7 @@ def test_cross_attention_calls():
 
 
 def test_outputs_repeatable_on_side_stream():
+    """Two runs on a non-default stream: same results to rounding, both correct."""
     call = wl.workload("tiny")[0]
     inp = wl.make_inputs(call)
     g = to_device(inp, DEV)
@@ -91,9 +92,14 @@ def test_outputs_repeatable_on_side_stream():
         op1, out1, ss1, _ = run_path(call, g, stream=s)
         op2, out2, ss2, _ = run_path(call, g, stream=s)
     s.synchronize()
-    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    # The per-row sums of squares are fp32 atomics whose order varies between runs,
+    # so inv_rms may differ in its last bit and flip an occasional bf16 rounding:
+    # repeat runs agree to one bf16 ulp, and each matches the oracle.
+    a, b = out1.float(), out2.float()
+    assert torch.all((a - b).abs() <= 2 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-30)
     torch.testing.assert_close(ss1, ss2, rtol=1e-6, atol=0)
-    check_outputs(call, inp, out2, ss2, None, name="side_stream")
+    check_outputs(call, inp, out1, ss1, None, name="side_stream_1")
+    check_outputs(call, inp, out2, ss2, None, name="side_stream_2")
 
 
 def test_norm_off_still_reports_sumsq():
