@@ -146,6 +146,36 @@ int qkv_cte_status(void* workspace, void* stream);
  * (no flag, never run, null pointer) or -3. */
 int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms);
 
+/* Size of the scratch array behind qkv_cte_run_noalloc: 16 MiB on every GPU that
+ * loads the library, held until the process exits. */
+#define QKV_CTE_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* qkv_cte_run without a workspace, for callers that cannot allocate device memory
+ * when they run the projection (a server that forbids allocation after start-up, a
+ * plug-in whose host framework owns all device memory, a latency-critical path where
+ * an allocation could synchronise the device). The page this library follows has no
+ * counterpart: it is an addition of this library.
+ *
+ * Arguments, layouts and return codes are those of qkv_cte_run without `workspace`
+ * and `workspace_bytes`: the scratch is a fixed array of QKV_CTE_NOALLOC_SCRATCH_BYTES
+ * inside the library. The call allocates nothing (no cudaMalloc, no allocating
+ * library routine). A problem whose planned workspace exceeds the array is rejected
+ * with QKV_CTE_ERR_UNSUPPORTED before any launch. With the fused Wan layout (H=5120,
+ * 40+40 heads of 128) up to 640 tokens fit; so do the separate cross-attention K and
+ * V calls on 512 context tokens.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the one array and each call clears the parts that must start at
+ * zero, so calls that overlap on the GPU (different streams, or other host threads)
+ * race and corrupt each other's results: serialise them. Bounded-wait timeouts are
+ * recorded in the array's status word, which this entry point does not report; use
+ * qkv_cte_run with a workspace to read them with qkv_cte_status. */
+int qkv_cte_run_noalloc(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, const uint8_t* W,
+                        const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias,
+                        const uint16_t* gamma_q, const uint16_t* gamma_k, const float* cos_table,
+                        const float* sin_table, uint16_t* O, float* sumsq, float* inv_rms, void* stream);
+
 /* Release a plan. NULL is a no-op. */
 void qkv_cte_destroy(qkv_cte_plan_t plan);
 

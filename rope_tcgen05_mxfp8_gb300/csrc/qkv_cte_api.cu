@@ -383,3 +383,66 @@ int qkv_cte_status(void* workspace, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point
+//
+// Some callers cannot allocate device memory at the moment they want to run this
+// projection: a serving process that allocates everything at start-up and forbids
+// cudaMalloc afterwards (it can stall or fragment a pool other work relies on), a
+// plug-in inside a framework whose allocator owns all device memory, or code on a
+// latency-critical path where an allocation may synchronise the device. For them
+// this entry point runs the same kernels with their scratch in a fixed array that
+// is part of the library image instead of a caller-provided workspace.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+// The scratch: QKV_CTE_NOALLOC_SCRATCH_BYTES on every GPU that loads the library,
+// held until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[QKV_CTE_NOALLOC_SCRATCH_BYTES];
+
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mu;
+
+// Device address of the scratch on the current device, looked up once per device.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(QKV_CTE_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(QKV_CTE_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return QKV_CTE_OK;
+}
+
+}  // namespace
+
+extern "C" int qkv_cte_run_noalloc(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, const uint8_t* W,
+                                   const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias,
+                                   const uint16_t* gamma_q, const uint16_t* gamma_k, const float* cos_table,
+                                   const float* sin_table, uint16_t* O, float* sumsq, float* inv_rms,
+                                   void* stream) {
+  if (plan == nullptr) return fail(QKV_CTE_ERR_INVALID, "null plan");
+  if (plan->ws.total > (size_t)QKV_CTE_NOALLOC_SCRATCH_BYTES)
+    return fail(QKV_CTE_ERR_UNSUPPORTED,
+                "this problem needs %zu bytes of scratch; qkv_cte_run_noalloc holds %zu "
+                "(use qkv_cte_run with a workspace)",
+                plan->ws.total, (size_t)QKV_CTE_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if (plan->g.T > 0) {
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != QKV_CTE_OK) return rc;
+  }
+  // qkv_cte_run clears everything that must start at zero (status word, sums of
+  // squares, panel counters) in its first kernel, on the same stream.
+  return qkv_cte_run(plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos_table, sin_table, O,
+                     sumsq, inv_rms, scratch, (size_t)QKV_CTE_NOALLOC_SCRATCH_BYTES, stream);
+}

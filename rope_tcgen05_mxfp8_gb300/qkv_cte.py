@@ -30,7 +30,8 @@ QKV_CTE_FLAG_PROFILE = 0x2
 QKV_CTE_FLAG_SERIAL_PASSES = 0x4
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
-            "qkv_cte_last_error", "qkv_cte_version")
+            "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc")
+QKV_CTE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class qkv_cte_desc(ctypes.Structure):
@@ -78,6 +79,8 @@ def load() -> ctypes.CDLL:
     lib.qkv_cte_plan.restype = ctypes.c_int
     lib.qkv_cte_run.argtypes = [P] * 15 + [ctypes.c_size_t, P]
     lib.qkv_cte_run.restype = ctypes.c_int
+    lib.qkv_cte_run_noalloc.argtypes = [P] * 15
+    lib.qkv_cte_run_noalloc.restype = ctypes.c_int
     lib.qkv_cte_status.argtypes = [P, P]
     lib.qkv_cte_status.restype = ctypes.c_int
     lib.qkv_cte_pass_times.argtypes = [P, ctypes.POINTER(ctypes.c_float)]
@@ -164,6 +167,20 @@ def qkv_cte_run(plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, 
             _ptr("gamma_k", gamma_k), _ptr("cos", cos), _ptr("sin", sin), _ptr("O", O),
             _ptr("sumsq", sumsq), _ptr("inv_rms", inv_rms), _ptr("workspace", workspace)]
     return _check(load().qkv_cte_run(plan, *args, ctypes.c_size_t(ws_bytes), ctypes.c_void_p(handle)))
+
+
+def qkv_cte_run_noalloc(plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos, sin, O,
+                        sumsq, inv_rms, stream=None) -> int:
+    """qkv_cte_run with the library's fixed scratch array instead of a workspace: for
+    callers that cannot allocate device memory when they run (see qkv_cte.h)."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    args = [_ptr("A", A), _ptr("a_scale", a_scale), _ptr("W", W), _ptr("w_sf", w_sf),
+            _ptr("w_col_scale", w_col_scale), _ptr("bias", bias), _ptr("gamma_q", gamma_q),
+            _ptr("gamma_k", gamma_k), _ptr("cos", cos), _ptr("sin", sin), _ptr("O", O),
+            _ptr("sumsq", sumsq), _ptr("inv_rms", inv_rms)]
+    return _check(load().qkv_cte_run_noalloc(plan, *args, ctypes.c_void_p(handle)))
 
 
 def qkv_cte_status(workspace, stream=None) -> int:

@@ -1,0 +1,84 @@
+"""The allocation-free entry point, qkv_cte_run_noalloc.
+
+Some callers cannot allocate device memory at the moment they run the projection: a
+server that allocates everything at start-up and forbids cudaMalloc afterwards, a
+plug-in whose host framework owns all device memory, a latency-critical path where an
+allocation could synchronise the device. qkv_cte_run_noalloc serves them: it runs the
+same kernels with their scratch in a fixed array inside the library instead of a
+caller-provided workspace.
+
+These tests call it through the C ABI twice in a row and check each result against
+qkv_cte_run (the entry point with a workspace) and the float64 oracle, and check that
+a problem too large for the fixed array is refused before anything is launched. The
+file is named so that pytest collects it after every other test file.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from rope_tcgen05_mxfp8_gb300 import qkv_cte as q
+
+from gpu_harness import ABS, REL, SS_REL, check_outputs, run_path, to_device
+
+
+def _cases():
+    return {
+        "tiny": wl.workload("tiny")[0],
+        "cross_k": wl.workload("cross")[1],
+        "edge": wl.custom_call(name="edge_noalloc", tokens=300, hidden=1024, n_q_heads=3, n_kv_heads=2,
+                               d_head=128, seed=99, has_w_col_scale=True),
+    }
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["tiny", "cross_k", "edge"])
+def test_noalloc_matches_workspace_entry_point_on_two_calls(name):
+    call = _cases()[name]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, dev)
+    op, ref_out, ref_ss, ref_inv = run_path(call, g)  # qkv_cte_run with its own workspace
+    op.status()
+    ref = ref_out.float()
+    desc = q.make_desc(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
+                       rope=call.rope, eps=call.eps)
+    plan, ws_bytes = q.qkv_cte_plan(desc)
+    assert ws_bytes <= q.QKV_CTE_NOALLOC_SCRATCH_BYTES
+    try:
+        for call_no in range(2):
+            out = torch.full((call.tokens, call.width), float("nan"), dtype=torch.bfloat16, device=dev)
+            ss = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev)
+            inv = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev)
+            q.qkv_cte_run_noalloc(plan, g["A"], g["a_scale"], g["W"], g["w_sf"], g["w_col_scale"], g["bias"],
+                                  g["gamma_q"] if call.norm else None, g["gamma_k"] if call.norm else None,
+                                  g["cos"], g["sin"], out, ss, inv)
+            torch.cuda.synchronize(dev)
+            got = out.float()
+            bad = ~((got - ref).abs() <= REL * ref.abs() + ABS)
+            assert not bool(bad.any()), f"{name} call {call_no}: {int(bad.sum())} outputs differ from qkv_cte_run"
+            segs = [0] + ([1] if call.n_kv_heads > 0 else [])
+            for c in segs:
+                rel = ((ss[:, c] - ref_ss[:, c]).abs() / ref_ss[:, c].abs().clamp_min(1e-30)).max()
+                assert float(rel) <= SS_REL, f"{name} call {call_no}: sumsq[{c}] rel err {float(rel):.3e}"
+                if call.norm:
+                    rel = ((inv[:, c] - ref_inv[:, c]).abs() / ref_inv[:, c].abs()).max()
+                    assert float(rel) <= SS_REL, f"{name} call {call_no}: inv_rms[{c}] rel err {float(rel):.3e}"
+            check_outputs(call, inp, out, ss, inv, name=f"noalloc_{name}_{call_no}")
+    finally:
+        q.qkv_cte_destroy(plan)
+
+
+def test_noalloc_refuses_a_problem_larger_than_its_scratch():
+    """4096 Wan tokens need far more scratch than the fixed array: refused on the host
+    with a clear message, before any pointer is read or kernel launched."""
+    plan, ws_bytes = q.qkv_cte_plan(q.make_desc(4096, 5120, 40, 40, 128))
+    try:
+        assert ws_bytes > q.QKV_CTE_NOALLOC_SCRATCH_BYTES
+        rc = q.load().qkv_cte_run_noalloc(plan, *([None] * 13), None)
+        assert rc == q.QKV_CTE_ERR_UNSUPPORTED
+        msg = q.qkv_cte_last_error()
+        assert "scratch" in msg and str(q.QKV_CTE_NOALLOC_SCRATCH_BYTES) in msg
+    finally:
+        q.qkv_cte_destroy(plan)
