@@ -243,7 +243,7 @@ def run_ours(args):
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
                 rope=call.rope, eps=call.eps, tile_n=args.tile_n, flags=QKV_CTE_FLAG_PROFILE, device=dev)
-    tile_n = op.desc.tile_n if op.desc.tile_n else 256
+    tile_n = op.info.tile_n
     out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=dev)
     sumsq = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

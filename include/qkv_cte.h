@@ -93,12 +93,24 @@ typedef struct {
 
 typedef struct qkv_cte_plan_s* qkv_cte_plan_t;
 
+/* What a plan chose (host only). */
+typedef struct {
+    int32_t tile_n;          /* GEMM N tile (columns of O per tile) */
+    int32_t m_tiles;         /* 128-row panels */
+    int32_t n_tiles;         /* N tiles */
+    int32_t n_bands;         /* bands of N tiles in the GEMM's tile order */
+    int64_t workspace_bytes; /* as returned by qkv_cte_plan */
+} qkv_cte_plan_info;
+
 /* Validate `desc` (host only, no CUDA call) and create a plan.
  * out            : receives the plan (set to NULL on error).
  * workspace_bytes: receives the device workspace size qkv_cte_run needs.
  * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values) or
  * -2 (H % 128, d_head % 16, T > INT32_MAX, NBSd layout, unknown tile_n). */
 int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes);
+
+/* Fill `info` for `plan`. Returns 0 or -1 (null pointer). */
+int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info);
 
 /* Run the whole path on `stream` (a cudaStream_t; NULL = legacy default stream).
  *

@@ -16,9 +16,9 @@
 // block floating point (fp16 with a power-of-two exponent per row and 16 columns, in
 // a tile-major workspace buffer), so the result is rounded to bf16 once, here. This
 // pass is HBM-bound. Lanes map to rows: a warp reads the hand-off with 1 KB
-// coalesced loads, keeps its row's cos/sin chunk and inv_rms in registers across all
-// heads, reads gamma as warp-wide broadcasts, and writes one full 32-byte sector of
-// O per row and half-head.
+// coalesced loads (four heads' worth in flight at once), keeps its row's cos/sin
+// chunk and inv_rms in registers across all heads, reads gamma as warp-wide
+// broadcasts, and writes one full 32-byte sector of O per row and half-head.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -66,47 +66,62 @@ __device__ bool wait_panel_ready(const uint32_t* flag, uint32_t target) {
   }
 }
 
+
+// One hand-off chunk of a row, raw: 16 fp16 (32 bytes) and the chunk's exponent
+// byte, read through L2 (the GEMM writes them while this kernel runs).
+struct RawChunk {
+  uint32_t w[8];
+  uint16_t e;
+};
+
+__device__ __forceinline__ void load_raw(const uint16_t* val, const uint8_t* ex, RawChunk& r) {
+  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
+                 "=r"(r.w[6]), "=r"(r.w[7])
+               : "l"(val)
+               : "memory");
+  asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(r.e) : "l"(ex) : "memory");
+}
+
+__device__ __forceinline__ void decode16(const RawChunk& r, float* f) {
+  const float up = __uint_as_float(static_cast<uint32_t>(r.e) << 23);  // 2^(e - 127)
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&r.w[j]));
+    f[2 * j] = p.x * up;
+    f[2 * j + 1] = p.y * up;
+  }
+}
+
+__device__ __forceinline__ void load8_nc(const float* p, float* v) {
+  asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+
 __device__ __forceinline__ void st_global_v8_b32(void* p, const uint32_t* w) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
                "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
                : "memory");
 }
 
-// One hand-off chunk of a row: 16 fp16 (32 bytes) and the exponent byte, read
-// through L2 (written by the GEMM while this kernel runs), decoded to fp32.
-__device__ __forceinline__ void load_handoff16(const uint16_t* val, const uint8_t* ex, float* f) {
+__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float* f) {
   uint32_t w[8];
-  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
-               : "l"(val)
-               : "memory");
-  uint16_t e;
-  asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(e) : "l"(ex) : "memory");
-  const float up = __uint_as_float(static_cast<uint32_t>(e) << 23);  // 2^(e - 127)
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
-    f[2 * j] = p.x * up;
-    f[2 * j + 1] = p.y * up;
+    __nv_bfloat162 v = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+    w[j] = *reinterpret_cast<uint32_t*>(&v);
   }
+  st_global_v8_b32(dst, w);
 }
 
-__device__ __forceinline__ void ld_v8_nc(const float* p, float* v) {
-  asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
-               : "l"(p));
-}
-
-__device__ __forceinline__ void load_gamma16(const uint16_t* g, float* f) {
-  const uint4 a = __ldg(reinterpret_cast<const uint4*>(g));
-  const uint4 b = __ldg(reinterpret_cast<const uint4*>(g) + 1);
-  unpack8(a, *reinterpret_cast<float(*)[8]>(f));
-  unpack8(b, *reinterpret_cast<float(*)[8]>(f + 8));
-}
+constexpr int kHeadBatch = 4;   // heads whose hand-off loads are in flight together
+constexpr int kHeadGroup = 20;  // heads per warp task (a multiple of kHeadBatch)
 
 // One warp task = 32 consecutive rows (one per lane) x one 16-column chunk c of the
-// low half of every head, with its partner chunk d/2 away: the rotation pairs lane
-// j with lane j + d/2 inside each head.
+// low half of up to kHeadGroup heads, with its partner chunk d/2 away (the rotation
+// pairs lane j with lane j + d/2 inside each head). Small tasks keep the warps
+// evenly loaded to the end.
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeArgs p) {
   if (threadIdx.x == 0) atomicMin(&p.stamps[0], now_ns());
   const int lane = threadIdx.x & 31;
@@ -115,13 +130,18 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
   const int chunks = d / 32;  // 16-column chunks in the low half of a head
   const int heads = p.n_q + p.n_kv;
   const int qk_chunks = heads * d / 16;
+  const int groups = (heads + kHeadGroup - 1) / kHeadGroup;
   const long long units = (p.T + 31) / 32;
-  const long long tasks = units * chunks;
+  const long long tasks = units * chunks * groups;
   const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
   for (long long task = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); task < tasks;
        task += warps) {
-    const int u = static_cast<int>(task / chunks);
-    const int c = static_cast<int>(task - static_cast<long long>(u) * chunks);
+    const int u = static_cast<int>(task / (chunks * groups));
+    const int rem = static_cast<int>(task - static_cast<long long>(u) * chunks * groups);
+    const int c = rem / groups;
+    const int grp = rem - c * groups;
+    const int h_begin = grp * kHeadGroup;
+    const int h_end = min(heads, h_begin + kHeadGroup);
     const int row0 = u * 32;
     const int t = row0 + lane;
     const bool row_ok = t < p.T;
@@ -146,65 +166,70 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
     if (p.rope) {
       const float* cr = p.cos_t + static_cast<size_t>(tr) * d + c * 16;
       const float* sr = p.sin_t + static_cast<size_t>(tr) * d + c * 16;
-      ld_v8_nc(cr, cl);
-      ld_v8_nc(cr + 8, cl + 8);
-      ld_v8_nc(cr + half, ch);
-      ld_v8_nc(cr + half + 8, ch + 8);
-      ld_v8_nc(sr, sl);
-      ld_v8_nc(sr + 8, sl + 8);
-      ld_v8_nc(sr + half, sh);
-      ld_v8_nc(sr + half + 8, sh + 8);
+      load8_nc(cr, cl);
+      load8_nc(cr + 8, cl + 8);
+      load8_nc(cr + half, ch);
+      load8_nc(cr + half + 8, ch + 8);
+      load8_nc(sr, sl);
+      load8_nc(sr + 8, sl + 8);
+      load8_nc(sr + half, sh);
+      load8_nc(sr + half + 8, sh + 8);
     }
     const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (row0 & 127) + lane;
     uint16_t* orow = p.O + static_cast<size_t>(tr) * p.I;
-    for (int hg = 0; hg < heads; ++hg) {
-      const int seg = hg >= p.n_q ? 1 : 0;
-      const int h = seg ? hg - p.n_q : hg;
-      const int off = h * d + c * 16;                 // column inside the segment
-      const int col = (seg ? p.n_q * d : 0) + off;    // column of O (low half)
-      float lo[16], hi[16];
-      const size_t i_lo = idx0 + static_cast<size_t>(col >> 4) * 128;
-      const size_t i_hi = idx0 + static_cast<size_t>((col + half) >> 4) * 128;
-      load_handoff16(p.qk_val + i_lo * 16, p.qk_exp + i_lo, lo);
-      load_handoff16(p.qk_val + i_hi * 16, p.qk_exp + i_hi, hi);
-      if (p.norm) {
-        const uint16_t* gamma = seg ? p.gamma_k : p.gamma_q;
-        const float inv = seg ? inv_k : inv_q;
-        float glo[16], ghi[16];
-        load_gamma16(gamma + off, glo);
-        load_gamma16(gamma + off + half, ghi);
+    for (int hg0 = h_begin; hg0 < h_end; hg0 += kHeadBatch) {
+      RawChunk raw_lo[kHeadBatch], raw_hi[kHeadBatch];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          lo[j] = lo[j] * inv * glo[j];
-          hi[j] = hi[j] * inv * ghi[j];
-        }
+      for (int k = 0; k < kHeadBatch; ++k) {
+        const int hg = hg0 + k;
+        if (hg >= h_end) break;
+        const int seg = hg >= p.n_q ? 1 : 0;
+        const int col = (seg ? p.n_q * d : 0) + (seg ? hg - p.n_q : hg) * d + c * 16;
+        const size_t i_lo = idx0 + static_cast<size_t>(col >> 4) * 128;
+        const size_t i_hi = idx0 + static_cast<size_t>((col + half) >> 4) * 128;
+        load_raw(p.qk_val + i_lo * 16, p.qk_exp + i_lo, raw_lo[k]);
+        load_raw(p.qk_val + i_hi * 16, p.qk_exp + i_hi, raw_hi[k]);
       }
-      if (p.rope) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float a = lo[j] * cl[j] - hi[j] * sl[j];
-          const float b = hi[j] * ch[j] + lo[j] * sh[j];
-          lo[j] = a;
-          hi[j] = b;
-        }
-      }
-      if (row_ok) {
-        uint32_t w[8];
+      for (int k = 0; k < kHeadBatch; ++k) {
+        const int hg = hg0 + k;
+        if (hg >= h_end) break;
+        const int seg = hg >= p.n_q ? 1 : 0;
+        const int off = (seg ? hg - p.n_q : hg) * d + c * 16;  // column inside the segment
+        const int col = (seg ? p.n_q * d : 0) + off;            // column of O (low half)
+        float lo[16], hi[16];
+        decode16(raw_lo[k], lo);
+        decode16(raw_hi[k], hi);
+        if (p.norm) {
+          const uint16_t* gamma = seg ? p.gamma_k : p.gamma_q;
+          const float inv = seg ? inv_k : inv_q;
+          float g[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          __nv_bfloat162 v = __floats2bfloat162_rn(lo[2 * j], lo[2 * j + 1]);
-          w[j] = *reinterpret_cast<uint32_t*>(&v);
-        }
-        st_global_v8_b32(orow + col, w);
+          for (int q = 0; q < 2; ++q) {
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off) + q), g);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          __nv_bfloat162 v = __floats2bfloat162_rn(hi[2 * j], hi[2 * j + 1]);
-          w[j] = *reinterpret_cast<uint32_t*>(&v);
+            for (int j = 0; j < 8; ++j) lo[8 * q + j] *= inv * g[j];
+            unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off + half) + q), g);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) hi[8 * q + j] *= inv * g[j];
+          }
         }
-        st_global_v8_b32(orow + col + half, w);
+        if (p.rope) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float a = lo[j] * cl[j] - hi[j] * sl[j];
+            const float b = hi[j] * ch[j] + lo[j] * sh[j];
+            lo[j] = a;
+            hi[j] = b;
+          }
+        }
+        if (row_ok) {
+          store16_bf16(orow + col, lo);
+          store16_bf16(orow + col + half, hi);
+        }
       }
     }
-    if (c == 0 && row_ok && p.norm && p.inv_rms != nullptr) {
+    if (c == 0 && grp == 0 && row_ok && p.norm && p.inv_rms != nullptr) {
       p.inv_rms[2 * static_cast<size_t>(t)] = inv_q;
       p.inv_rms[2 * static_cast<size_t>(t) + 1] = p.n_kv > 0 ? inv_k : 0.0f;
     }
@@ -216,10 +241,22 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
 
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap) {
   if (!a.norm && !a.rope) return cudaSuccess;
-  const long long tasks = static_cast<long long>((a.T + 31) / 32) * (a.d_head / 32);
+  const long long tasks = static_cast<long long>((a.T + 31) / 32) * (a.d_head / 32) *
+                          ((a.n_q + a.n_kv + kHeadGroup - 1) / kHeadGroup);
   if (tasks == 0) return cudaSuccess;
+  // Overlapped with the GEMM, the grid is kept to what fits beside each GEMM CTA
+  // (registers are the limit) so every block finds its units as their panels
+  // complete. That sizing only affects speed: the GEMM never waits for this kernel.
+  // Alone, the pass takes every SM it can hold.
+  int per_sm = 1;
+  if (!overlap) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qk_norm_rope_kernel, kThreads, 0) == cudaSuccess &&
+        occ > per_sm)
+      per_sm = occ;
+  }
   long long blocks = (tasks + kThreads / 32 - 1) / (kThreads / 32);
-  if (blocks > 2LL * num_sms) blocks = 2LL * num_sms;
+  if (blocks > static_cast<long long>(per_sm) * num_sms) blocks = static_cast<long long>(per_sm) * num_sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks));
   cfg.blockDim = dim3(kThreads);

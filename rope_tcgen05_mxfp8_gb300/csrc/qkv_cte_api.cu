@@ -201,6 +201,16 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   return ok();
 }
 
+int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return fail(QKV_CTE_ERR_INVALID, "null argument");
+  info->tile_n = plan->g.tile_n;
+  info->m_tiles = plan->g.m_tiles;
+  info->n_tiles = plan->g.n_tiles;
+  info->n_bands = plan->g.n_bands;
+  info->workspace_bytes = (int64_t)plan->ws.total;
+  return ok();
+}
+
 void qkv_cte_destroy(qkv_cte_plan_t plan) {
   if (plan == nullptr) return;
   for (cudaEvent_t e : plan->ev)

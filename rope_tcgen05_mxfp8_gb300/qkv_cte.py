@@ -30,7 +30,7 @@ QKV_CTE_FLAG_PROFILE = 0x2
 QKV_CTE_FLAG_SERIAL_PASSES = 0x4
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
-            "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc")
+            "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info")
 QKV_CTE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -49,6 +49,16 @@ class qkv_cte_desc(ctypes.Structure):
         ("flags", ctypes.c_uint32),
         ("tile_n", ctypes.c_int32),
         ("reserved", ctypes.c_int32),
+    ]
+
+
+class qkv_cte_plan_info(ctypes.Structure):
+    _fields_ = [
+        ("tile_n", ctypes.c_int32),
+        ("m_tiles", ctypes.c_int32),
+        ("n_tiles", ctypes.c_int32),
+        ("n_bands", ctypes.c_int32),
+        ("workspace_bytes", ctypes.c_int64),
     ]
 
 
@@ -79,6 +89,8 @@ def load() -> ctypes.CDLL:
     lib.qkv_cte_plan.restype = ctypes.c_int
     lib.qkv_cte_run.argtypes = [P] * 15 + [ctypes.c_size_t, P]
     lib.qkv_cte_run.restype = ctypes.c_int
+    lib.qkv_cte_get_plan_info.argtypes = [P, ctypes.POINTER(qkv_cte_plan_info)]
+    lib.qkv_cte_get_plan_info.restype = ctypes.c_int
     lib.qkv_cte_run_noalloc.argtypes = [P] * 15
     lib.qkv_cte_run_noalloc.restype = ctypes.c_int
     lib.qkv_cte_status.argtypes = [P, P]
@@ -123,6 +135,12 @@ def qkv_cte_plan(desc: qkv_cte_desc):
     ws = ctypes.c_size_t()
     _check(load().qkv_cte_plan(ctypes.byref(plan), ctypes.byref(desc), ctypes.byref(ws)))
     return plan, ws.value
+
+
+def qkv_cte_get_plan_info(plan) -> qkv_cte_plan_info:
+    info = qkv_cte_plan_info()
+    _check(load().qkv_cte_get_plan_info(plan, ctypes.byref(info)))
+    return info
 
 
 def qkv_cte_destroy(plan) -> None:
@@ -210,6 +228,7 @@ class QkvCte:
         self.desc = make_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=norm, rope=rope,
                               eps=eps, tile_n=tile_n, flags=flags)
         self.plan, self.workspace_bytes = qkv_cte_plan(self.desc)
+        self.info = qkv_cte_get_plan_info(self.plan)
         self.width = (n_q_heads + 2 * n_kv_heads) * d_head
         dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.workspace = torch.zeros(max(self.workspace_bytes, 256), dtype=torch.uint8, device=dev)

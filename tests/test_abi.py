@@ -91,6 +91,21 @@ def test_plan_validation(kw, code):
     assert _plan_code(**kw) == code
 
 
+def test_plan_info_reports_the_choices():
+    plan, ws = q.qkv_cte_plan(q.make_desc(32760, 5120, 40, 40, 128))
+    try:
+        info = q.qkv_cte_get_plan_info(plan)
+        assert info.tile_n == 240 and info.m_tiles == 256 and info.n_tiles == 64
+        assert info.workspace_bytes == ws and 1 <= info.n_bands <= 16
+    finally:
+        q.qkv_cte_destroy(plan)
+    plan, ws = q.qkv_cte_plan(q.make_desc(512, 512, 4, 4, 128, tile_n=128))
+    try:
+        assert q.qkv_cte_get_plan_info(plan).tile_n == 128
+    finally:
+        q.qkv_cte_destroy(plan)
+
+
 def test_error_message_is_recorded():
     with pytest.raises(q.QkvCteError) as ei:
         q.qkv_cte_plan(q.make_desc(256, 100, 4, 4, 128))
