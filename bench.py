@@ -135,16 +135,21 @@ class ClockSampler:
 
 
 def _k1_traffic(workload, tile_n):
-    """DRAM bytes per K1 launch from the committed ncu summary, if it was taken on the
-    current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "k1_traffic.json")
+    """DRAM bytes per GEMM launch from the committed ncu summary
+    (profiles/qkv_gemm_mxf8_wan480p.md), if it was taken on the current kernel
+    source and this workload/tile; else None."""
+    path = os.path.join(ROOT, "profiles", "qkv_gemm_mxf8_%s.md" % workload)
     if not os.path.exists(path):
         return None
     try:
+        rec = {}
         with open(path) as f:
-            rec = json.load(f)
+            for line in f:
+                if ":" in line and not line.startswith(("|", " ", "#", "-")):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
         h = hashlib.sha256()
-        for fn in rec["sources"]:
+        for fn in rec["sources"].split():
             with open(os.path.join(ROOT, fn), "rb") as f:
                 h.update(f.read())
         if h.hexdigest() != rec["source_sha256"]:
