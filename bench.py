@@ -48,6 +48,8 @@ def _args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="wan480p")
     p.add_argument("--tile-n", type=int, default=0)
+    p.add_argument("--gemm", choices=["auto", "pair", "single"], default="auto",
+                   help="GEMM form: 256-row tiles on SM pairs, 128-row tiles on one SM, or the library's choice")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
@@ -224,7 +226,8 @@ def run_ours(args):
     import torch
 
     import workloads as wl
-    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_SERIAL_PASSES, QkvCte
+    from rope_tcgen05_mxfp8_gb300 import (QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA,
+                                          QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_SERIAL_PASSES, QkvCte)
     from rope_tcgen05_mxfp8_gb300 import build as b
 
     world, rank, local = _dist()
@@ -246,8 +249,9 @@ def run_ours(args):
     call = wl.workload(args.workload)[0]
     inp = wl.make_inputs(call)
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    gemm_flag = {"auto": 0, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA}[args.gemm]
     op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
-                rope=call.rope, eps=call.eps, tile_n=args.tile_n, flags=QKV_CTE_FLAG_PROFILE, device=dev)
+                rope=call.rope, eps=call.eps, tile_n=args.tile_n, flags=QKV_CTE_FLAG_PROFILE | gemm_flag, device=dev)
     tile_n = op.info.tile_n
     out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=dev)
     sumsq = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
@@ -302,7 +306,7 @@ def run_ours(args):
     # serialised, to time the norm/RoPE pass on its own for its bandwidth roofline.
     serial = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
                     rope=call.rope, eps=call.eps, tile_n=args.tile_n,
-                    flags=QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES, device=dev)
+                    flags=QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES | gemm_flag, device=dev)
     ser = []
     for i in range(max(3, min(args.steps, 10))):
         if not args.no_flush:
@@ -373,7 +377,7 @@ def run_ours(args):
                "sample": (f"{len(rows)} seeded rows of the {call.tokens}-token workload in one oracle call "
                           f"({dt:.2f} s; float64 numpy, BLAS threads via {how})")}
 
-    traffic = _k1_traffic(args.workload, tile_n)
+    traffic = _k1_traffic(args.workload, tile_n) if not op.info.cta_pair else None
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -390,7 +394,9 @@ def run_ours(args):
                              "GEMM; 'serial' is a side run with the passes serialised"},
         "norm_rope": {"GB/s": k2_gbs, "bytes": k2_bytes, "measured_on": "serial side run",
                       "frac_of_hbm": (k2_gbs / hbm_gbs) if k2_gbs else None, "peak_GB/s": hbm_gbs},
-        "roofline": {"bound": "tensor", "kernel": f"qkv_gemm_mxf8_kernel<{tile_n}>", "achieved": k1_achieved,
+        "roofline": {"bound": "tensor",
+                     "kernel": ("qkv_gemm_mxf8_pair_kernel<%d>" if op.info.cta_pair else "qkv_gemm_mxf8_kernel<%d>")
+                     % tile_n, "achieved": k1_achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": k1_achieved / fp8_peak,
                      "traffic": traffic,
                      "peak_source": (f"{peak_src} bf16 burst {bf16:.1f} TFLOP/s x nominal fp8/bf16 ratio "

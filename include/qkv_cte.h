@@ -73,6 +73,11 @@ enum { QKV_CTE_LAYOUT_BSD = 0, QKV_CTE_LAYOUT_NBSD = 1 };
 /* Launch the norm/RoPE pass after the GEMM has finished instead of overlapping the two
  * (same results; used to time each pass on its own). */
 #define QKV_CTE_FLAG_SERIAL_PASSES 0x4u
+/* GEMM form: tiles of 256 rows on a pair of SMs (M = 256 MMAs; each SM stages half
+ * of the weight tile), or tiles of 128 rows on one SM. Neither flag: the library
+ * chooses. Both: -1. */
+#define QKV_CTE_FLAG_GEMM_CTA_PAIR 0x8u
+#define QKV_CTE_FLAG_GEMM_SINGLE_CTA 0x10u
 
 /* Problem description ([qkv_cte] "Interface" argument table, flattened to scalars). */
 typedef struct {
@@ -96,9 +101,11 @@ typedef struct qkv_cte_plan_s* qkv_cte_plan_t;
 /* What a plan chose (host only). */
 typedef struct {
     int32_t tile_n;          /* GEMM N tile (columns of O per tile) */
-    int32_t m_tiles;         /* 128-row panels */
+    int32_t m_tiles;         /* GEMM row tiles (128 rows, or 256 with a CTA pair) */
     int32_t n_tiles;         /* N tiles */
     int32_t n_bands;         /* bands of N tiles in the GEMM's tile order */
+    int32_t cta_pair;        /* 1: 256-row tiles on SM pairs; 0: 128-row tiles */
+    int32_t reserved;
     int64_t workspace_bytes; /* as returned by qkv_cte_plan */
 } qkv_cte_plan_info;
 

@@ -27,7 +27,7 @@ enum : uint32_t {
 //                            caller passes no sumsq buffer)
 //   [.., + sf_bytes)         W's UE8M0 scales repacked per (N tile, K stage) in the
 //                            order the MMA's scale-factor copy consumes them
-//   [.., + ready_bytes)      uint32 [m_tiles]: per 128-row panel, how many epilogue
+//   [.., + ready_bytes)      uint32 [blocks128]: per 128-row block, how many epilogue
 //                            warp-tiles of K1's Q/K tiles have finished (4 per tile)
 //   [.., + qk_bytes)         the un-normalised Q and K columns handed from K1 to K2
 //                            (only when a norm/RoPE pass runs) in block floating
@@ -58,6 +58,8 @@ constexpr int kMaxBands = 16;
 struct GemmShape {
   int T, H, I;
   int tile_n;       // N tile (columns of O per tile)
+  int cta_pair;     // 1: tiles of 256 rows computed by a CTA pair (M = 256 MMA)
+  int blocks128;    // ceil(T / 128): 128-row blocks (counters, hand-off rows)
   int m_tiles, n_tiles, k_stages;
   int sf_chunks;    // 128-column scale-factor chunks per N tile
   int n_qk_tiles;   // N tiles holding at least one Q or K column: [0, n_qk_tiles)
@@ -147,8 +149,10 @@ size_t gemm_smem_bytes(int tile_n);
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
                         size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
                         cudaStream_t s, int num_sms);
+// tmSF: the repacked scales as a uint32 [n_tiles * k_stages, sf_chunks * 128] map with
+// one-row boxes (used by the CTA-pair kernel).
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                        const GemmArgs& a, cudaStream_t s, int num_sms);
+                        const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms);
 // Launched right after K1 on the same stream as a programmatic dependent launch, so
 // its blocks start while K1 runs and take each row panel as soon as K1 marks it ready.
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap);

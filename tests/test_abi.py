@@ -95,7 +95,7 @@ def test_plan_info_reports_the_choices():
     plan, ws = q.qkv_cte_plan(q.make_desc(32760, 5120, 40, 40, 128))
     try:
         info = q.qkv_cte_get_plan_info(plan)
-        assert info.tile_n == 240 and info.m_tiles == 256 and info.n_tiles == 64
+        assert info.tile_n == 240 and info.m_tiles == 128 and info.n_tiles == 64 and info.cta_pair == 1
         assert info.workspace_bytes == ws and 1 <= info.n_bands <= 16
     finally:
         q.qkv_cte_destroy(plan)
@@ -104,6 +104,17 @@ def test_plan_info_reports_the_choices():
         assert q.qkv_cte_get_plan_info(plan).tile_n == 128
     finally:
         q.qkv_cte_destroy(plan)
+    for T, flags, pair, m_tiles in ((100, 0, 0, 1), (300, 0, 1, 2), (300, q.QKV_CTE_FLAG_GEMM_SINGLE_CTA, 0, 3),
+                                    (100, q.QKV_CTE_FLAG_GEMM_CTA_PAIR, 1, 1)):
+        plan, ws = q.qkv_cte_plan(q.make_desc(T, 512, 4, 4, 128, flags=flags))
+        try:
+            info = q.qkv_cte_get_plan_info(plan)
+            assert (info.cta_pair, info.m_tiles) == (pair, m_tiles), (T, flags)
+        finally:
+            q.qkv_cte_destroy(plan)
+    with pytest.raises(q.QkvCteError):
+        q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, 128,
+                                   flags=q.QKV_CTE_FLAG_GEMM_CTA_PAIR | q.QKV_CTE_FLAG_GEMM_SINGLE_CTA))
 
 
 def test_error_message_is_recorded():

@@ -171,3 +171,88 @@ def test_pass_times_reported():
     assert run >= gemm
     flops = call.flops / (gemm * 1e-3) / 1e12
     assert 10 < flops < 6000, f"implausible GEMM rate {flops} TFLOP/s"
+
+
+# --- the CTA-pair GEMM (256-row tiles, M = 256 MMAs on two SMs) ------------------
+
+def _pair_case(call, tile_n=0, rows=None, name=None):
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_CTA_PAIR
+
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, tile_n=tile_n, flags=QKV_CTE_FLAG_GEMM_CTA_PAIR)
+    assert op.info.cta_pair == 1
+    op.status()
+    return check_outputs(call, inp, out, ss, inv, rows=rows, name=name or f"pair_{call.name}")
+
+
+@pytest.mark.parametrize("tile_n", [240, 128, 256])
+def test_cta_pair_tiny_full(tile_n):
+    _pair_case(wl.workload("tiny")[0], tile_n=tile_n, name=f"pair_tiny_n{tile_n}")
+
+
+@pytest.mark.parametrize("T", [1, 129, 257, 300, 640])
+def test_cta_pair_ragged_rows(T):
+    # T mod 256 in (0, 128] leaves the second CTA's half of the last tile empty.
+    call = wl.custom_call(name=f"pair_T{T}", tokens=T, hidden=256, n_q_heads=3, n_kv_heads=1, d_head=128,
+                          seed=T + 7, has_w_col_scale=True)
+    _pair_case(call)
+
+
+def test_cta_pair_d64_and_separate():
+    _pair_case(wl.custom_call(name="pair_d64", tokens=200, hidden=384, n_q_heads=5, n_kv_heads=2, d_head=64,
+                              seed=23, has_w_col_scale=True))
+    _pair_case(wl.custom_call(name="pair_sep", tokens=333, hidden=512, n_q_heads=6, n_kv_heads=0, d_head=128,
+                              norm=1, rope=0, seed=33))
+
+
+def test_cta_pair_short_full():
+    _pair_case(wl.workload("short")[0])
+
+
+def test_cta_pair_wan480p_sampled():
+    call = wl.workload("wan480p")[0]
+    _pair_case(call, rows=sampled_rows(call))
+
+
+def test_cta_pair_bounded_wait_reports_timeout():
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_CTA_PAIR
+
+    call = wl.workload("tiny")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_GEMM_CTA_PAIR)
+    with pytest.raises(QkvCteError) as ei:
+        op.status()
+    assert ei.value.code == QKV_CTE_ERR_DEVICE_TIMEOUT
+    _pair_case(call, name="pair_after_timeout")
+
+
+# --- the single-CTA GEMM (128-row tiles), forced ---------------------------------
+
+def _single_case(call, tile_n=0, rows=None, name=None):
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_SINGLE_CTA
+
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, tile_n=tile_n, flags=QKV_CTE_FLAG_GEMM_SINGLE_CTA)
+    assert op.info.cta_pair == 0
+    op.status()
+    return check_outputs(call, inp, out, ss, inv, rows=rows, name=name or f"single_{call.name}")
+
+
+@pytest.mark.parametrize("tile_n", [240, 128, 192, 256])
+def test_single_cta_tiny_full(tile_n):
+    _single_case(wl.workload("tiny")[0], tile_n=tile_n, name=f"single_tiny_n{tile_n}")
+
+
+@pytest.mark.parametrize("T", [129, 300])
+def test_single_cta_ragged_rows(T):
+    call = wl.custom_call(name=f"single_T{T}", tokens=T, hidden=256, n_q_heads=3, n_kv_heads=1, d_head=128,
+                          seed=T + 11, has_w_col_scale=True)
+    _single_case(call)
+
+
+def test_single_cta_wan480p_sampled():
+    call = wl.workload("wan480p")[0]
+    _single_case(call, rows=sampled_rows(call))
