@@ -74,11 +74,11 @@ struct RawChunk {
   uint16_t e;
 };
 
-__device__ __forceinline__ void load_raw(const uint16_t* val, const uint8_t* ex, RawChunk& r) {
-  asm volatile("ld.global.cg.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+__device__ __forceinline__ void load_raw(const uint16_t* val, const uint8_t* ex, RawChunk& r, uint64_t policy) {
+  asm volatile("ld.global.cg.L2::cache_hint.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
                : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]),
                  "=r"(r.w[6]), "=r"(r.w[7])
-               : "l"(val)
+               : "l"(val), "l"(policy)
                : "memory");
   asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(r.e) : "l"(ex) : "memory");
 }
@@ -99,20 +99,26 @@ __device__ __forceinline__ void load8_nc(const float* p, float* v) {
                : "l"(p));
 }
 
-__device__ __forceinline__ void st_global_v8_b32(void* p, const uint32_t* w) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
-               "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+__device__ __forceinline__ void st_global_v8_b32(void* p, const uint32_t* w, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]), "l"(policy)
                : "memory");
 }
 
-__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float* f) {
+__device__ __forceinline__ void store16_bf16(uint16_t* dst, const float* f, uint64_t policy) {
   uint32_t w[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     __nv_bfloat162 v = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
     w[j] = *reinterpret_cast<uint32_t*>(&v);
   }
-  st_global_v8_b32(dst, w);
+  st_global_v8_b32(dst, w, policy);
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 constexpr int kHeadBatch = 4;   // heads whose hand-off loads are in flight together
@@ -134,6 +140,9 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
   const long long units = (p.T + 31) / 32;
   const long long tasks = units * chunks * groups;
   const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
+  // Read-once hand-off and write-once output: first out of L2, so the GEMM's
+  // L2-resident weight band running beside this pass keeps its place.
+  const uint64_t once = evict_first_policy();
   for (long long task = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); task < tasks;
        task += warps) {
     const int u = static_cast<int>(task / (chunks * groups));
@@ -187,8 +196,8 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
         const int col = (seg ? p.n_q * d : 0) + (seg ? hg - p.n_q : hg) * d + c * 16;
         const size_t i_lo = idx0 + static_cast<size_t>(col >> 4) * 128;
         const size_t i_hi = idx0 + static_cast<size_t>((col + half) >> 4) * 128;
-        load_raw(p.qk_val + i_lo * 16, p.qk_exp + i_lo, raw_lo[k]);
-        load_raw(p.qk_val + i_hi * 16, p.qk_exp + i_hi, raw_hi[k]);
+        load_raw(p.qk_val + i_lo * 16, p.qk_exp + i_lo, raw_lo[k], once);
+        load_raw(p.qk_val + i_hi * 16, p.qk_exp + i_hi, raw_hi[k], once);
       }
 #pragma unroll
       for (int k = 0; k < kHeadBatch; ++k) {
@@ -224,8 +233,8 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
           }
         }
         if (row_ok) {
-          store16_bf16(orow + col, lo);
-          store16_bf16(orow + col + half, hi);
+          store16_bf16(orow + col, lo, once);
+          store16_bf16(orow + col + half, hi, once);
         }
       }
     }
