@@ -170,6 +170,22 @@ def _dist():
     return world, rank, local
 
 
+def replica_throughput(local_ms_total, units_per_rank, world, device=None):
+    """Whole-job throughput of `world` replicas that each processed `units_per_rank`
+    units in `local_ms_total` milliseconds: all ranks' units over the slowest rank's
+    time. With world > 1 the time is max-reduced over the default process group.
+    Returns (units per second, the max time in ms)."""
+    total_ms = float(local_ms_total)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return world * units_per_rank / (total_ms * 1e-3), total_ms
+
+
 def run_reference(args):
     """The oracle, as it stands, on the host cores: a bounded row sample per step."""
     import numpy as np
@@ -286,16 +302,10 @@ def run_ours(args):
     clocks = sampler.stop()
     op.status(stream)
     step_ms = [s.elapsed_time(e) for s, e in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
     flops = call.flops
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    per_s, total_ms = replica_throughput(sum(step_ms), flops * args.steps, world, device=dev)
+    ms_per_step = total_ms / args.steps
+    value = per_s / 1e12
 
     prep_ms = statistics.mean(p[0] for p in passes)
     gemm_ms = statistics.mean(p[1] for p in passes)
@@ -349,14 +359,9 @@ def run_ours(args):
             if i >= args.warmup:
                 e2e_ev.append((e0, e1))
         torch.cuda.synchronize(dev)
-        e2e_ms = sum(a.elapsed_time(b2) for a, b2 in e2e_ev)
-        if world > 1:
-            import torch.distributed as dist
-
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * flops * args.steps / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e_per_s, e2e_ms = replica_throughput(sum(a.elapsed_time(b2) for a, b2 in e2e_ev), flops * args.steps,
+                                               world, device=dev)
+        e2e = {"value": e2e_per_s / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(A_h.numel() * A_h.element_size() + s_h.numel() * s_h.element_size()),
                "d2h_bytes_per_step": int(O_h.numel() * O_h.element_size()),
                "ms_per_step": e2e_ms / args.steps,
