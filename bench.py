@@ -136,11 +136,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
-def _k1_traffic(workload, tile_n):
-    """DRAM bytes per GEMM launch from the committed ncu summary
-    (profiles/qkv_gemm_mxf8_wan480p.md), if it was taken on the current kernel
-    source and this workload/tile; else None."""
-    path = os.path.join(ROOT, "profiles", "qkv_gemm_mxf8_%s.md" % workload)
+def _k1_traffic(workload, tile_n, pair):
+    """DRAM bytes per GEMM launch from the committed ncu summary of that GEMM form
+    (profiles/qkv_gemm_mxf8[_pair]_<workload>.md), if it was taken on the current
+    kernel source and this workload/tile; else None."""
+    name = "qkv_gemm_mxf8_pair" if pair else "qkv_gemm_mxf8"
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (name, workload))
     if not os.path.exists(path):
         return None
     try:
@@ -382,7 +383,7 @@ def run_ours(args):
                "sample": (f"{len(rows)} seeded rows of the {call.tokens}-token workload in one oracle call "
                           f"({dt:.2f} s; float64 numpy, BLAS threads via {how})")}
 
-    traffic = _k1_traffic(args.workload, tile_n) if not op.info.cta_pair else None
+    traffic = _k1_traffic(args.workload, tile_n, bool(op.info.cta_pair))
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
