@@ -50,6 +50,8 @@ def _args():
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--gemm", choices=["auto", "pair", "single"], default="auto",
                    help="GEMM form: 256-row tiles on SM pairs, 128-row tiles on one SM, or the library's choice")
+    p.add_argument("--layout", choices=["bsd", "nbsd"], default="bsd",
+                   help="output layout: BSD [T, I] or NBSd [heads, T, d_head]")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
@@ -225,7 +227,7 @@ def run_reference(args):
     return 0
 
 
-def _config(call, tile_n, flushed=True):
+def _config(call, tile_n, flushed=True, layout="bsd"):
     return {
         "workload": (f"{call.name}: Wan2.2-style fused QKV self-attention projection, T={call.tokens} "
                      f"H={call.hidden} n_q={call.n_q_heads} n_kv={call.n_kv_heads} d_head={call.d_head} "
@@ -233,6 +235,7 @@ def _config(call, tile_n, flushed=True):
         "tokens": call.tokens, "hidden": call.hidden, "width": call.width,
         "n_q_heads": call.n_q_heads, "n_kv_heads": call.n_kv_heads, "d_head": call.d_head,
         "tile_n": tile_n,
+        "output_layout": "NBSd [heads, T, d_head]" if layout == "nbsd" else "BSD [T, I]",
         "l2": "flushed between timed steps (256 MB write, outside the step events)" if flushed
         else "not flushed",
     }
@@ -244,7 +247,8 @@ def run_ours(args):
 
     import workloads as wl
     from rope_tcgen05_mxfp8_gb300 import (QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA,
-                                          QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_SERIAL_PASSES, QkvCte)
+                                          QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_SERIAL_PASSES, QKV_CTE_LAYOUT_BSD,
+                                          QKV_CTE_LAYOUT_NBSD, QkvCte)
     from rope_tcgen05_mxfp8_gb300 import build as b
 
     world, rank, local = _dist()
@@ -267,8 +271,10 @@ def run_ours(args):
     inp = wl.make_inputs(call)
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     gemm_flag = {"auto": 0, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA}[args.gemm]
+    layout = QKV_CTE_LAYOUT_NBSD if args.layout == "nbsd" else QKV_CTE_LAYOUT_BSD
     op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
-                rope=call.rope, eps=call.eps, tile_n=args.tile_n, flags=QKV_CTE_FLAG_PROFILE | gemm_flag, device=dev)
+                rope=call.rope, eps=call.eps, tile_n=args.tile_n, flags=QKV_CTE_FLAG_PROFILE | gemm_flag, device=dev,
+                output_layout=layout)
     tile_n = op.info.tile_n
     out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=dev)
     sumsq = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
@@ -317,7 +323,8 @@ def run_ours(args):
     # serialised, to time the norm/RoPE pass on its own for its bandwidth roofline.
     serial = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
                     rope=call.rope, eps=call.eps, tile_n=args.tile_n,
-                    flags=QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES | gemm_flag, device=dev)
+                    flags=QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES | gemm_flag, device=dev,
+                    output_layout=layout)
     ser = []
     for i in range(max(3, min(args.steps, 10))):
         if not args.no_flush:
@@ -388,7 +395,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; Wan2.2 480p shapes and distributions)",
-        "config": _config(call, tile_n, flushed=not args.no_flush),
+        "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout),
         "pct_nominal_dense_fp8_peak": 100.0 * value / (world * NOMINAL_FP8_TFLOPS),
         "pct_measured_fp8_peak": 100.0 * value / (world * fp8_peak),
         "passes_ms": {"prep": prep_ms, "gemm_epilogue": gemm_ms, "norm_rope_span": norm_span_ms,

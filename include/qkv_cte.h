@@ -6,7 +6,9 @@
  * projection", vllm-omni-neuron docs, kernels/qkv-cte), cited below as [qkv_cte]
  * with the page's section headings:
  *
- *   O[T, I] = dequant(A_fp8[T, H] @ W_fp8[H, I]) (+ bias),  I = (n_q + 2 n_kv) * d_head
+ *   O[T, I] = dequant(A_fp8[T, H] @ W_fp8[H, I]) (+ bias),  I = (n_q + 2 n_kv) * d_head,
+ *             stored as BSD [T, I] or NBSd [I/d_head, T, d_head] ([qkv_cte] "Upstream
+ *             behavior" output layouts; "Interface" output_layout)
  *             ([qkv_cte] "Upstream behavior", first bullet; "Interface" argument table)
  *   Q, K   : across-heads RMSNorm - one RMS per token over the whole Q (or K) segment,
  *            inv_rms = 1/sqrt(sum(o^2) / (n_heads * d_head) + eps), times a segment-wide
@@ -89,7 +91,8 @@ typedef struct {
     int32_t mode;          /* QKV_CTE_MODE_FUSED (n_kv >= 1) or QKV_CTE_MODE_SEPARATE (n_kv == 0) */
     int32_t norm;          /* 1: across-heads RMSNorm on Q (and K); 0: none */
     int32_t rope;          /* 1: rotate-half RoPE on Q (and K); needs cos/sin */
-    int32_t output_layout; /* QKV_CTE_LAYOUT_BSD ([T, I]); NBSd is not built yet (-2) */
+    int32_t output_layout; /* QKV_CTE_LAYOUT_BSD: O[T, I]; QKV_CTE_LAYOUT_NBSD: O[I/d_head, T, d_head]
+                              (heads in column order: Q heads, then K, then V) */
     float eps;             /* norm epsilon, >= 0 */
     uint32_t flags;        /* 0 or QKV_CTE_FLAG_* bits */
     int32_t tile_n;        /* GEMM N tile: 0 = automatic, else 128, 192, 240 or 256 */
@@ -113,7 +116,7 @@ typedef struct {
  * out            : receives the plan (set to NULL on error).
  * workspace_bytes: receives the device workspace size qkv_cte_run needs.
  * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values) or
- * -2 (H % 128, d_head % 16, T > INT32_MAX, NBSd layout, unknown tile_n). */
+ * -2 (H % 128, d_head % 16, T > INT32_MAX, unknown tile_n). */
 int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes);
 
 /* Fill `info` for `plan`. Returns 0 or -1 (null pointer). */
@@ -131,7 +134,8 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info);
  * gamma_k    : bf16   [n_kv*d_head] K gamma; required iff norm and n_kv > 0, else NULL
  * cos_table, sin_table: fp32 [T, d_head] rotate-half tables; required iff rope, else NULL;
  *              32-byte aligned
- * O          : bf16   [T, I] (BSD) output; 32-byte aligned; must not alias any input
+ * O          : bf16 output, [T, I] (BSD) or [I/d_head, T, d_head] (NBSd: element (h, t, j)
+ *              is column h*d_head + j of token t); 32-byte aligned; must not alias any input
  * sumsq      : fp32   [T, 2] or NULL: per-token sum of o^2 over the un-normalised Q and K
  *              segments ([qkv_cte] "Design" 1 step a; column 1 is 0 when n_kv == 0)
  * inv_rms    : fp32   [T, 2] or NULL: the rsqrt factors of step b (written iff norm)

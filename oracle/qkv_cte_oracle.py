@@ -247,6 +247,17 @@ def qkv_cte(A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, *, n_q_heads:
     return dict(O=out, sumsq=ss, inv_rms=inv, projected=o)
 
 
+def to_nbsd(O: np.ndarray, d_head: int) -> np.ndarray:
+    """BSD [T, I] -> NBSd [n_heads, T, d_head] with n_heads = I / d_head: element (h, t, j)
+    is O[t, h*d_head + j], heads in column order (Q heads, then K, then V).
+
+    [qkv_cte] "Upstream behavior" (BSD and NBSd output layouts) and "Interface" table
+    (output_layout: NBSd [num_heads, B, S, d_head]; B*S is the token axis here).
+    """
+    T, I = O.shape
+    return O.reshape(T, I // d_head, d_head).transpose(1, 0, 2)
+
+
 def qkv_cte_from_inputs(call, inp, rows=None):
     """Convenience wrapper over :func:`qkv_cte` for a ``workloads.Call`` and its inputs."""
     from workloads import as_numpy_bits

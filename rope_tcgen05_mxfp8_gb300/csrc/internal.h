@@ -118,8 +118,20 @@ struct GemmArgs {
   unsigned long long* stamps;  // [0] first CTA start (min), [1] last CTA end (max)
   uint32_t* status;
   int q_end, k_end;          // Q = [0, q_end), K = [q_end, k_end), V = [k_end, I)
+  int d_head;
+  int nbsd;                  // O layout: 0 = BSD [T, I]; 1 = NBSd [I/d_head, T, d_head]
   uint32_t flags;
 };
+
+// Element (row t, column c) of O in either layout (c and the 16 columns after it
+// lie in one head: d_head and every chunk start are multiples of 16).
+__host__ __device__ inline size_t out_index(int nbsd, int T, int I, int d_head, int t, int c) {
+  if (nbsd) {
+    const int h = c / d_head;
+    return (static_cast<size_t>(h) * T + t) * d_head + (c - h * d_head);
+  }
+  return static_cast<size_t>(t) * I + c;
+}
 
 struct NormRopeArgs {
   int T, I, n_q, n_kv, d_head;
@@ -134,6 +146,7 @@ struct NormRopeArgs {
   const float* sin_t;
   uint16_t* O;
   float* inv_rms;            // may be null
+  int nbsd;                  // O layout (see GemmArgs)
   const uint32_t* ready;     // per 128-row panel: K1 epilogue warp-tiles finished
   uint32_t ready_target;     // 4 * K1's Q/K tiles: the panel's Q and K are final
   unsigned long long* stamps;  // [0] first block start (min), [1] last block end (max)

@@ -185,7 +185,6 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
       load8_nc(sr + half + 8, sh + 8);
     }
     const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (row0 & 127) + lane;
-    uint16_t* orow = p.O + static_cast<size_t>(tr) * p.I;
     for (int hg0 = h_begin; hg0 < h_end; hg0 += kHeadBatch) {
       RawChunk raw_lo[kHeadBatch], raw_hi[kHeadBatch];
 #pragma unroll
@@ -233,8 +232,8 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
           }
         }
         if (row_ok) {
-          store16_bf16(orow + col, lo, once);
-          store16_bf16(orow + col + half, hi, once);
+          store16_bf16(p.O + out_index(p.nbsd, p.T, p.I, d, t, col), lo, once);
+          store16_bf16(p.O + out_index(p.nbsd, p.T, p.I, d, t, col + half), hi, once);
         }
       }
     }

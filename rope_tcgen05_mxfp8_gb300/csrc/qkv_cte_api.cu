@@ -174,9 +174,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   if (d.norm != 0 && d.norm != 1) return fail(QKV_CTE_ERR_INVALID, "norm must be 0 or 1");
   if (d.rope != 0 && d.rope != 1) return fail(QKV_CTE_ERR_INVALID, "rope must be 0 or 1");
   if (!(d.eps >= 0.0f) || d.eps > 1e30f) return fail(QKV_CTE_ERR_INVALID, "eps must be finite and >= 0");
-  if (d.output_layout == QKV_CTE_LAYOUT_NBSD)
-    return fail(QKV_CTE_ERR_UNSUPPORTED, "NBSd output layout is not built in this version");
-  if (d.output_layout != QKV_CTE_LAYOUT_BSD) return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
+  if (d.output_layout != QKV_CTE_LAYOUT_BSD && d.output_layout != QKV_CTE_LAYOUT_NBSD)
+    return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
   const uint32_t known_flags = QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES |
                                QKV_CTE_FLAG_GEMM_CTA_PAIR | QKV_CTE_FLAG_GEMM_SINGLE_CTA;
   if ((d.flags & ~known_flags) != 0) return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
@@ -360,6 +359,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.q_end = plan->q_end;
   ga.k_end = plan->k_end;
   ga.flags = d.flags;
+  ga.d_head = d.d_head;
+  ga.nbsd = d.output_layout == QKV_CTE_LAYOUT_NBSD ? 1 : 0;
   CUtensorMap tmSF;
   if ((rc = encode_scales(&tmSF, sf_packed, g)) != QKV_CTE_OK) return rc;
   e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms);
@@ -383,6 +384,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.sin_t = sin_table;
   na.O = O;
   na.inv_rms = inv_rms;
+  na.nbsd = d.output_layout == QKV_CTE_LAYOUT_NBSD ? 1 : 0;
   na.ready = ready;
   na.ready_target = 4u * (uint32_t)g.n_qk_tiles;
   na.status = status;

@@ -101,7 +101,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // are multiples of 16), then one 32-byte store. Q/K chunks go to the hand-off in
 // block floating point (16 fp16 scaled by the chunk's power-of-two exponent,
 // tile-major, so the warp's store writes 1 KB of consecutive memory); V goes to O
-// row-major as final bf16 (one full 32-byte sector per row).
+// as final bf16 (one full 32-byte sector per row), BSD or NBSd.
 // ---------------------------------------------------------------------------
 template <int BN>
 __device__ __forceinline__ void epilogue_drain(const GemmShape& g, const GemmArgs& a, uint32_t t_acc, int block128,
@@ -110,7 +110,6 @@ __device__ __forceinline__ void epilogue_drain(const GemmShape& g, const GemmArg
   const int row = block128 * 128 + row_in_block;
   const bool row_ok = row < g.T;
   const float ascale = row_ok ? a.a_scale[row] : 0.0f;
-  uint16_t* orow = a.O + static_cast<size_t>(row_ok ? row : 0) * g.I;
   const int qk_chunks = a.k_end >> 4;
   const size_t qk_row_idx = static_cast<size_t>(block128) * qk_chunks * 128 + row_in_block;
   ss_q = 0.0f;
@@ -189,7 +188,7 @@ __device__ __forceinline__ void epilogue_drain(const GemmShape& g, const GemmArg
 #pragma unroll
         for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
         // final values nothing here reads again: first out of L2
-        st_global_v8_b32_hint(orow + col0, packed, pol_out);
+        st_global_v8_b32_hint(a.O + out_index(a.nbsd, g.T, g.I, a.d_head, row, col0), packed, pol_out);
       }
     }
   }

@@ -228,9 +228,9 @@ class QkvCte:
     """
 
     def __init__(self, tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=1, rope=1, eps=1e-6,
-                 tile_n=0, flags=0, device=None):
+                 tile_n=0, flags=0, device=None, output_layout=QKV_CTE_LAYOUT_BSD):
         self.desc = make_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=norm, rope=rope,
-                              eps=eps, tile_n=tile_n, flags=flags)
+                              eps=eps, tile_n=tile_n, flags=flags, output_layout=output_layout)
         self.plan, self.workspace_bytes = qkv_cte_plan(self.desc)
         self.info = qkv_cte_get_plan_info(self.plan)
         self.width = (n_q_heads + 2 * n_kv_heads) * d_head
@@ -240,7 +240,11 @@ class QkvCte:
     def __call__(self, A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, out=None,
                  w_col_scale=None, sumsq=None, inv_rms=None, stream=None):
         if out is None:
-            out = torch.empty(self.desc.tokens, self.width, dtype=torch.bfloat16, device=A.device)
+            if self.desc.output_layout == QKV_CTE_LAYOUT_NBSD:
+                d = self.desc.d_head
+                out = torch.empty(self.width // d, self.desc.tokens, d, dtype=torch.bfloat16, device=A.device)
+            else:
+                out = torch.empty(self.desc.tokens, self.width, dtype=torch.bfloat16, device=A.device)
         qkv_cte_run(self.plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos, sin, out,
                     sumsq, inv_rms, self.workspace, stream)
         return out

@@ -79,7 +79,7 @@ def _plan_code(**kw):
     (dict(rope=-1), -1),
     (dict(eps=-1.0), -1),
     (dict(eps=float("nan")), -1),
-    (dict(output_layout=1), -2),
+    (dict(output_layout=1), 0),
     (dict(output_layout=5), -1),
     (dict(flags=0x80), -1),
     (dict(tile_n=100), -2),

@@ -256,3 +256,65 @@ def test_single_cta_ragged_rows(T):
 def test_single_cta_wan480p_sampled():
     call = wl.workload("wan480p")[0]
     _single_case(call, rows=sampled_rows(call))
+
+
+# --- NBSd output layout [heads, T, d_head] ----------------------------------------
+
+def _nbsd_case(call, flags=0, tile_n=0, rows=None, name=None):
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, tile_n=tile_n, flags=flags, nbsd=True)
+    op.status()
+    # run_path hands back the NBSd buffer viewed as BSD; every element was written
+    # (the buffer starts as NaN, which the tolerance check rejects)
+    return check_outputs(call, inp, out, ss, inv, rows=rows, name=name or f"nbsd_{call.name}")
+
+
+@pytest.mark.parametrize("form", ["auto", "single", "pair"])
+def test_nbsd_tiny_full(form):
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA
+
+    flags = {"auto": 0, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR}[form]
+    _nbsd_case(wl.workload("tiny")[0], flags=flags, name=f"nbsd_tiny_{form}")
+
+
+@pytest.mark.parametrize("T", [1, 129, 300])
+def test_nbsd_ragged_rows_d64(T):
+    call = wl.custom_call(name=f"nbsd_T{T}", tokens=T, hidden=384, n_q_heads=5, n_kv_heads=2, d_head=64,
+                          seed=T + 101, has_w_col_scale=True)
+    _nbsd_case(call)
+
+
+def test_nbsd_serial_passes_and_separate_mode():
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_SERIAL_PASSES
+
+    call = wl.custom_call(name="nbsd_edge", tokens=1000, hidden=1024, n_q_heads=3, n_kv_heads=2, d_head=128,
+                          seed=78, has_w_col_scale=True)
+    _nbsd_case(call, flags=QKV_CTE_FLAG_SERIAL_PASSES, name="nbsd_edge_serial")
+    _nbsd_case(call, name="nbsd_edge_overlapped")
+    sep = wl.custom_call(name="nbsd_sep", tokens=333, hidden=512, n_q_heads=6, n_kv_heads=0, d_head=128,
+                         norm=1, rope=1, seed=34)
+    _nbsd_case(sep)
+
+
+def test_nbsd_cross_attention_calls():
+    q, k, v = wl.workload("cross")
+    _nbsd_case(q, rows=sampled_rows(q))
+    _nbsd_case(k)
+    _nbsd_case(v)
+
+
+def test_nbsd_wan480p_sampled_matches_bsd():
+    """At the full size: NBSd on sampled rows against the oracle, and the whole NBSd
+    result against the BSD run permuted (same kernels, same arithmetic, different
+    addresses: equal to one bf16 ulp, the sums of squares being fp32 atomics)."""
+    call = wl.workload("wan480p")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op_n, out_n, ss_n, inv_n = run_path(call, g, nbsd=True)
+    op_n.status()
+    check_outputs(call, inp, out_n, ss_n, inv_n, rows=sampled_rows(call), name="nbsd_wan480p")
+    op_b, out_b, _, _ = run_path(call, g)
+    op_b.status()
+    a, b = out_n.float(), out_b.float()
+    assert torch.all((a - b).abs() <= 2 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-30)

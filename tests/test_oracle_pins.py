@@ -325,7 +325,19 @@ def pin_rows_subset():
         _close(sub[k], full[k][rows], rel=0, what=k)
 
 
-PINS = [pin_e4m3_exhaustive, pin_e4m3_spec_values, pin_ue8m0_exhaustive, pin_bf16_exhaustive,
+def pin_nbsd_layout():
+    rng = np.random.default_rng(12)
+    T, heads, d = 5, 3, 4
+    o = rng.normal(size=(T, heads * d))
+    n = O.to_nbsd(o, d)
+    assert n.shape == (heads, T, d)
+    for h in range(heads):
+        for t in range(T):
+            for j in range(d):
+                assert n[h, t, j] == o[t, h * d + j]
+
+
+PINS = [pin_nbsd_layout, pin_e4m3_exhaustive, pin_e4m3_spec_values, pin_ue8m0_exhaustive, pin_bf16_exhaustive,
         pin_full_bruteforce, pin_separate_bruteforce, pin_hand_example, pin_norm_vs_torch_rms_norm,
         pin_rope_complex_closed_form, pin_unit_rms_invariant, pin_pair_norm_invariant,
         pin_v_is_plain_projection, pin_separate_equals_fused_slice, pin_rows_subset]
@@ -343,7 +355,7 @@ def test_pin(pin):
 _orig = {name: getattr(O, name) for name in
          ("decode_e4m3", "decode_ue8m0", "decode_bf16", "dequant_activations", "dequant_weights",
           "project", "segments", "segment_sumsq", "inv_rms", "rotate_half", "apply_norm_rope",
-          "qkv_cte")}
+          "qkv_cte", "to_nbsd")}
 
 
 def _e4m3_bias8(codes):
@@ -474,6 +486,11 @@ def _v_normalised(*args, **kw):
     return res
 
 
+def _nbsd_heads_swapped(O_, d):
+    T, I = O_.shape
+    return O_.reshape(T, d, I // d).transpose(2, 0, 1)
+
+
 def _k_uses_gamma_q(*args, **kw):
     args = list(args)
     if args[6] is not None:
@@ -505,6 +522,7 @@ MUTANTS = {
     "gamma_ignored": ("apply_norm_rope", _gamma_ignored),
     "v_normalised": ("qkv_cte", _v_normalised),
     "k_uses_gamma_q": ("qkv_cte", _k_uses_gamma_q),
+    "nbsd_heads_swapped": ("to_nbsd", _nbsd_heads_swapped),
 }
 
 
