@@ -89,5 +89,29 @@ def check_outputs(call, inp, out, sumsq, inv, rows=None, name="case"):
     return float(np.max(err)) if err.size else 0.0
 
 
+def assert_same_to_rounding(call, a, b, name="runs"):
+    """Two runs of the same inputs through the same kernels (BSD views [T, I]).
+
+    V columns must be bit-identical: nothing in their arithmetic depends on order.
+    Q/K depend on inv_rms, whose fp32 sum of squares is built from atomics in a
+    run-dependent order, so it may differ in its last bits. The fp32 values before
+    rounding then differ by a few 2^-24 of |lo|+|hi| of the rotated pair, and the
+    rotation keeps the pair's norm, so that is at most 2 * the row's largest |O|.
+    Bound: one bf16 ulp of the larger value (a flipped rounding) + 2^-18 of the
+    row's largest magnitude (the pre-rounding drift, with margin), where the
+    rotation cancels."""
+    assert a.shape == b.shape == (call.tokens, call.width)
+    assert bool(torch.isfinite(a).all()) and bool(torch.isfinite(b).all()), f"{name}: non-finite output"
+    k_end = (call.n_q_heads + call.n_kv_heads) * call.d_head
+    assert torch.equal(a[:, k_end:], b[:, k_end:]), f"{name}: V columns differ"
+    fa, fb = a[:, :k_end].float(), b[:, :k_end].float()
+    mag = torch.maximum(fa.abs(), fb.abs())
+    rowmax = mag.amax(dim=1, keepdim=True)
+    tol = 2 ** -7 * mag + 2 ** -18 * rowmax
+    bad = (fa - fb).abs() > tol
+    nbad = int(bad.sum())
+    assert nbad == 0, f"{name}: {nbad} Q/K outputs differ by more than rounding"
+
+
 def sampled_rows(call, count=4096):
     return wl.sample_rows(call, count).numpy()

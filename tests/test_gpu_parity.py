@@ -12,7 +12,7 @@ import torch
 import workloads as wl
 from rope_tcgen05_mxfp8_gb300 import QKV_CTE_ERR_DEVICE_TIMEOUT, QKV_CTE_FLAG_TEST_STALL, QkvCteError
 
-from gpu_harness import check_outputs, run_path, sampled_rows, to_device
+from gpu_harness import assert_same_to_rounding, check_outputs, run_path, sampled_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -92,11 +92,9 @@ def test_outputs_repeatable_on_side_stream():
         op1, out1, ss1, _ = run_path(call, g, stream=s)
         op2, out2, ss2, _ = run_path(call, g, stream=s)
     s.synchronize()
-    # The per-row sums of squares are fp32 atomics whose order varies between runs,
-    # so inv_rms may differ in its last bit and flip an occasional bf16 rounding:
-    # repeat runs agree to one bf16 ulp, and each matches the oracle.
-    a, b = out1.float(), out2.float()
-    assert torch.all((a - b).abs() <= 2 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-30)
+    # The per-row sums of squares are fp32 atomics whose order varies between runs:
+    # repeat runs agree to rounding, and each matches the oracle.
+    assert_same_to_rounding(call, out1, out2, name="side_stream")
     torch.testing.assert_close(ss1, ss2, rtol=1e-6, atol=0)
     check_outputs(call, inp, out1, ss1, None, name="side_stream_1")
     check_outputs(call, inp, out2, ss2, None, name="side_stream_2")
@@ -307,7 +305,8 @@ def test_nbsd_cross_attention_calls():
 def test_nbsd_wan480p_sampled_matches_bsd():
     """At the full size: NBSd on sampled rows against the oracle, and the whole NBSd
     result against the BSD run permuted (same kernels, same arithmetic, different
-    addresses: equal to one bf16 ulp, the sums of squares being fp32 atomics)."""
+    addresses: V bit-identical, Q/K equal to rounding, the sums of squares being
+    fp32 atomics)."""
     call = wl.workload("wan480p")[0]
     inp = wl.make_inputs(call)
     g = to_device(inp, DEV)
@@ -316,5 +315,4 @@ def test_nbsd_wan480p_sampled_matches_bsd():
     check_outputs(call, inp, out_n, ss_n, inv_n, rows=sampled_rows(call), name="nbsd_wan480p")
     op_b, out_b, _, _ = run_path(call, g)
     op_b.status()
-    a, b = out_n.float(), out_b.float()
-    assert torch.all((a - b).abs() <= 2 ** -7 * torch.maximum(a.abs(), b.abs()) + 1e-30)
+    assert_same_to_rounding(call, out_n, out_b, name="nbsd_vs_bsd_wan480p")
