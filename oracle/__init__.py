@@ -5,5 +5,6 @@ Test infrastructure only: the product path never imports this package.
 from .qkv_cte_oracle import (  # noqa: F401
     decode_bf16, decode_e4m3, decode_ue8m0, dequant_activations, dequant_weights, project,
     segments, segment_sumsq, inv_rms, rotate_half, apply_norm_rope, qkv_cte,
-    qkv_cte_from_inputs, to_nbsd, SEG_Q, SEG_K, SEG_V,
+    qkv_cte_from_inputs, to_nbsd, encode_e4m3, row_quantise, pack_rows, unpack_rows,
+    SEG_Q, SEG_K, SEG_V,
 )

@@ -27,6 +27,10 @@ with the page's own section headings:
   4. V is never normalised ([qkv_cte] "Design" 1, step c); with n_kv_heads = 0 the
      whole projection is one segment, normalised as Q ([qkv_cte] "Design",
      "5) Individual QKV projections for cross-attention").
+  5. The producer step before the projection: bf16 activations quantised per row
+     to FP8 codes plus one fp32 dequant scale, optionally packed as [T, H + 4]
+     rows (codes, then the scale's four bytes) ([qkv_cte] "Upstream behavior",
+     packed H + 4 layout; "Interface" table, packed_hidden row).
 
 Readings of points the page leaves open (each also listed in the design notes):
 
@@ -43,6 +47,9 @@ Readings of points the page leaves open (each also listed in the design notes):
     y = x * inv_rms * gamma, then the rotate-half combination ("Design" 1 step c
     with "Design" 2).
   * norm off leaves gamma unused (gamma belongs to the norm); RoPE off leaves y.
+  * Row quantisation: s = amax / 448 (1 for an all-zero row), code = e4m3(x / s)
+    rounded to nearest-even with saturation, both divisions in fp32; the packed
+    scale tail is little-endian.
 
 Pins: every function here is checked in tests/test_oracle_pins.py against
 something other than itself - an exhaustive comparison with torch's float8 codecs,
@@ -256,6 +263,80 @@ def to_nbsd(O: np.ndarray, d_head: int) -> np.ndarray:
     """
     T, I = O.shape
     return O.reshape(T, I // d_head, d_head).transpose(1, 0, 2)
+
+
+# ---------------------------------------------------------------------------
+# the producer step: bf16 -> ROW_MX rows, and the packed H + 4 row layout
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def encode_e4m3(v) -> np.ndarray:
+    """Real values -> FP8 E4M3 ("fn") codes: the nearest point of the e4m3 grid,
+    ties to the even code (mantissa LSB 0), magnitudes above 448 clamped to 448
+    (a saturating conversion: finite in, finite out), the sign kept (a negative value
+    that rounds to zero gives -0, code 0x80). NaN gives 0x7F.
+
+    The grid is whatever ``decode_e4m3`` says the 127 non-negative finite codes are;
+    codes are ascending in magnitude, so neighbours on the grid are neighbouring codes.
+    """
+    v = np.asarray(v, dtype=np.float64)
+    mags = decode_e4m3(np.arange(0x7F, dtype=np.uint8))      # codes 0x00..0x7E, ascending
+    a = np.minimum(np.abs(v), E4M3_MAX)
+    a = np.where(np.isnan(a), 0.0, a)
+    hi = np.minimum(np.searchsorted(mags, a, side="left"), 0x7E)  # mags[hi - 1] < a <= mags[hi]
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - mags[lo]
+    d_hi = mags[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(take_hi, hi, lo).astype(np.uint8)
+    code = code | (np.signbit(v).astype(np.uint8) << 7)
+    return np.where(np.isnan(v), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def row_quantise(x_bits: np.ndarray):
+    """bf16 activations [T, H] (bit patterns) -> ROW_MX rows: (codes uint8 [T, H],
+    dequant scale float32 [T]).
+
+    Per row: amax = max |x| (exact); s = amax / 448 (1 for an all-zero row); each
+    code is x / s rounded to e4m3 by ``encode_e4m3``, so code * s reproduces x to
+    FP8 precision and the row's largest element maps to 448. [qkv_cte] "Interface"
+    table, packed_hidden row (per-row FP8 codes plus an fp32 dequant scale; the
+    projection does not quantise bf16 itself, its producer does) and "Upstream
+    behavior" (the ROW_MX quantization mode).
+
+    The page fixes no precision for this step. A code is an integer that a floating
+    point quotient decides, so the two divisions are taken in IEEE fp32 (numpy
+    float32, correctly rounded, subnormals kept), the precision of the scale the
+    page stores; the CUDA producer divides the same way.
+    """
+    x = decode_bf16(x_bits).astype(np.float32)             # exact: bf16 is a truncated fp32
+    amax = np.abs(x).max(axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+        q = (x / s[:, None]).astype(np.float32)
+    return encode_e4m3(q.astype(np.float64)), s
+
+
+def pack_rows(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """ROW_MX rows -> the packed layout [T, H + 4]: each row's H codes, then the four
+    bytes of its fp32 dequant scale, little-endian. [qkv_cte] "Upstream behavior"
+    (the packed H + 4 activation layout) and "Interface" table, packed_hidden."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    T, H = codes.shape
+    tail = np.asarray(scale, dtype="<f4").reshape(T, 1).view(np.uint8)
+    return np.concatenate([codes, tail], axis=1)
+
+
+def unpack_rows(packed: np.ndarray):
+    """Packed [T, H + 4] -> (codes uint8 [T, H], scale float32 [T]); the inverse of
+    ``pack_rows``."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    H = packed.shape[1] - 4
+    codes = np.ascontiguousarray(packed[:, :H])
+    scale = np.ascontiguousarray(packed[:, H:]).view("<f4").reshape(-1).astype(np.float32)
+    return codes, scale
 
 
 def qkv_cte_from_inputs(call, inp, rows=None):

@@ -337,7 +337,140 @@ def pin_nbsd_layout():
                 assert n[h, t, j] == o[t, h * d + j]
 
 
-PINS = [pin_nbsd_layout, pin_e4m3_exhaustive, pin_e4m3_spec_values, pin_ue8m0_exhaustive, pin_bf16_exhaustive,
+# --- the producer step: e4m3 encoder, row quantiser, packed rows ------------------
+
+def _e4m3_grid():
+    return _torch_e4m3(np.arange(0x7F, dtype=np.uint8))      # ascending magnitudes 0 .. 448
+
+
+def pin_encode_e4m3_vs_torch():
+    """The encoder against torch's float32 -> float8_e4m3fn cast (round to nearest,
+    ties to even) on every grid point, every midpoint (the ties), one fp32 ulp either
+    side of each midpoint, and random values over the whole range, both signs.
+    torch does not saturate, so this covers |v| <= 448; saturation has its own pin."""
+    g = _e4m3_grid()
+    mid = (g[1:] + g[:-1]) / 2
+    m32 = mid.astype(np.float32)
+    assert np.all(m32.astype(np.float64) == mid)              # the ties are exact in fp32
+    up = np.nextafter(m32, np.float32(np.inf))
+    dn = np.nextafter(m32, np.float32(0))
+    rng = np.random.default_rng(60)
+    rnd = np.exp2(rng.uniform(-14, np.log2(448.0), size=20000)).astype(np.float32)
+    v = np.concatenate([g.astype(np.float32), m32, up[up <= 448], dn, rnd, np.float32([0.0])])
+    v = np.concatenate([v, -v])
+    got = O.encode_e4m3(v.astype(np.float64))
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, ref), f"{int((got != ref).sum())} codes differ from torch's cast"
+    assert O.encode_e4m3(np.float64(-0.0)) == 0x80 and O.encode_e4m3(np.float64(0.0)) == 0x00
+
+
+def pin_encode_e4m3_saturation():
+    """Saturating conversion: every finite magnitude above 448 (including those past
+    the would-be next binade, and infinity) gives the largest finite code, 0x7E /
+    0xFE (S.1111.110 = 448 by the OFP8 table); NaN stays NaN (0x7F)."""
+    v = np.array([448.0, 455.9, 464.0, 470.0, 480.0, 1e4, 3.0e38, np.inf])
+    assert np.all(O.encode_e4m3(v) == 0x7E)
+    assert np.all(O.encode_e4m3(-v) == 0xFE)
+    assert O.encode_e4m3(np.float64(np.nan)) == 0x7F
+    assert _torch_e4m3(np.uint8([0x7E]))[0] == 448.0
+
+
+def _quant_rows():
+    """bf16 rows covering the method's cases: Gaussian, heavy outliers, values in the
+    bf16 subnormal range, an all-zero row, a one-hot row, a row of negative zeros and
+    tiny negatives, and one row per exponent band."""
+    rng = np.random.default_rng(61)
+    H = 64
+    rows = [rng.normal(0, 1, H), rng.normal(0, 1, H) * np.where(rng.random(H) < 0.05, 300.0, 1.0),
+            rng.normal(0, 1, H) * 1e-39, np.zeros(H), np.eye(1, H, 17)[0] * -3.5,
+            np.concatenate([[-0.0] * (H // 2), -np.abs(rng.normal(0, 1e-6, H // 2))]),
+            rng.normal(0, 1, H) * 1e30, rng.normal(0, 1, H) * 2.0 ** -100]
+    x = torch.tensor(np.stack(rows), dtype=torch.float32).to(torch.bfloat16)
+    return x.view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_row_quantise_invariants():
+    bits = _quant_rows()
+    x = _torch_bf16(bits)
+    codes, s = O.row_quantise(bits)
+    assert codes.dtype == np.uint8 and codes.shape == x.shape and s.dtype == np.float32
+    val = _torch_e4m3(codes)
+    amax = np.abs(x).max(axis=1)
+    for t in range(x.shape[0]):
+        if amax[t] == 0:
+            assert s[t] == 1.0 and np.all(val[t] == 0), "all-zero row: scale 1, zero codes"
+            continue
+        # the scale is the row's amax over 448 to fp32 precision (subnormal scales
+        # keep only their absolute precision)
+        assert abs(float(s[t]) * 448.0 - amax[t]) <= 2.0 ** -23 * amax[t] + 448.0 * 2.0 ** -150
+        q = x[t] / float(s[t])
+        # the largest element lands on the top of the grid
+        assert np.max(np.abs(val[t])) == 448.0
+        # nearest grid point: error at most half an e4m3 step at |q| (plus the fp32
+        # rounding of the quotient, and the relative slack of a subnormal scale)
+        e = np.floor(np.log2(np.maximum(np.abs(q), 2.0 ** -6)))
+        half_step = 2.0 ** (e - 4)
+        slack = 2.0 ** -22 * np.abs(q) + (2.0 ** -7 * np.abs(q) if s[t] < 2.0 ** -126 else 0.0)
+        assert np.all(np.abs(val[t] - q) <= half_step + slack), f"row {t}: not the nearest code"
+        # sign kept (zeros included), order kept
+        assert np.array_equal(codes[t] >> 7, np.signbit(x[t]).astype(np.uint8))
+        order = np.argsort(x[t], kind="stable")
+        assert np.all(np.diff(val[t][order]) >= 0)
+
+
+def pin_row_quantise_exact_power_of_two():
+    """Closed form: a row whose elements are e4m3 grid points times 2^j, with 448*2^j
+    present, has scale exactly 2^j and quantises without error."""
+    rng = np.random.default_rng(62)
+    g = _e4m3_grid()
+    for j in (-20, -3, 0, 5, 40):
+        vals = rng.choice(g, size=32) * rng.choice([-1.0, 1.0], size=32)
+        vals[7] = 448.0
+        x = vals * 2.0 ** j
+        bits = torch.tensor(x[None, :], dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.all(_torch_bf16(bits)[0] == x)               # exact in bf16
+        codes, s = O.row_quantise(bits)
+        assert s[0] == 2.0 ** j
+        assert np.all(_torch_e4m3(codes)[0] * 2.0 ** j == x)
+
+
+def pin_row_quantise_vs_torch_route():
+    """The special case the method reduces to in torch: fp32 amax / 448, fp32
+    division, then torch's e4m3 cast (torch does not saturate, but every quotient here
+    is below 464, where rounding alone already gives 448)."""
+    bits = _quant_rows()
+    xt = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).float()
+    amax = xt.abs().amax(dim=1)
+    st = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    qt = xt / st[:, None]
+    assert float(qt.abs().max()) < 464.0
+    ref = qt.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    codes, s = O.row_quantise(bits)
+    assert np.array_equal(s, st.numpy())
+    assert np.array_equal(codes, ref)
+
+
+def pin_packed_rows_layout():
+    """Byte layout by brute force: row t of the packed tensor is the row's H codes
+    followed by struct.pack('<f', scale); unpacking inverts packing exactly."""
+    import struct
+
+    rng = np.random.default_rng(63)
+    T, H = 3, 8
+    codes = _rand_codes(rng, (T, H))
+    scale = np.float32([0.015625, 3.0e-5, 2.5])
+    p = O.pack_rows(codes, scale)
+    assert p.dtype == np.uint8 and p.shape == (T, H + 4)
+    flat = p.reshape(-1)
+    for t in range(T):
+        row = bytes(codes[t].tolist()) + struct.pack("<f", float(scale[t]))
+        assert bytes(flat[t * (H + 4):(t + 1) * (H + 4)].tolist()) == row
+    c2, s2 = O.unpack_rows(p)
+    assert np.array_equal(c2, codes) and np.array_equal(s2, scale) and s2.dtype == np.float32
+
+
+PINS = [pin_nbsd_layout, pin_encode_e4m3_vs_torch, pin_encode_e4m3_saturation, pin_row_quantise_invariants,
+        pin_row_quantise_exact_power_of_two, pin_row_quantise_vs_torch_route, pin_packed_rows_layout, pin_e4m3_exhaustive, pin_e4m3_spec_values, pin_ue8m0_exhaustive, pin_bf16_exhaustive,
         pin_full_bruteforce, pin_separate_bruteforce, pin_hand_example, pin_norm_vs_torch_rms_norm,
         pin_rope_complex_closed_form, pin_unit_rms_invariant, pin_pair_norm_invariant,
         pin_v_is_plain_projection, pin_separate_equals_fused_slice, pin_rows_subset]
@@ -355,7 +488,7 @@ def test_pin(pin):
 _orig = {name: getattr(O, name) for name in
          ("decode_e4m3", "decode_ue8m0", "decode_bf16", "dequant_activations", "dequant_weights",
           "project", "segments", "segment_sumsq", "inv_rms", "rotate_half", "apply_norm_rope",
-          "qkv_cte", "to_nbsd")}
+          "qkv_cte", "to_nbsd", "encode_e4m3", "row_quantise", "pack_rows", "unpack_rows")}
 
 
 def _e4m3_bias8(codes):
@@ -498,7 +631,81 @@ def _k_uses_gamma_q(*args, **kw):
     return _orig["qkv_cte"](*args, **kw)
 
 
+def _encode_truncate(v):
+    v = np.asarray(v, dtype=np.float64)
+    g = _e4m3_grid()
+    a = np.minimum(np.abs(v), 448.0)
+    idx = np.searchsorted(g, a, side="right") - 1
+    return (idx.astype(np.uint8) | (np.signbit(v).astype(np.uint8) << 7)).astype(np.uint8)
+
+
+def _encode_ties_away(v):
+    v = np.asarray(v, dtype=np.float64)
+    g = _e4m3_grid()
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.minimum(np.searchsorted(g, a, side="left"), 0x7E)
+    lo = np.maximum(hi - 1, 0)
+    code = np.where(g[hi] - a <= a - g[lo], hi, lo).astype(np.uint8)
+    return code | (np.signbit(v).astype(np.uint8) << 7)
+
+
+def _encode_no_saturation(v):
+    v = np.asarray(v, dtype=np.float64)
+    c = _orig["encode_e4m3"](v)
+    return np.where(np.abs(v) > 464.0, np.uint8(0x7F), c).astype(np.uint8)
+
+
+def _encode_drops_sign(v):
+    return _orig["encode_e4m3"](np.abs(np.asarray(v, dtype=np.float64)))
+
+
+def _quant_scale_127(x_bits):
+    x = O.decode_bf16(x_bits).astype(np.float32)
+    amax = np.abs(x).max(axis=1)
+    s = np.where(amax > 0, amax / np.float32(127.0), np.float32(1.0)).astype(np.float32)
+    return O.encode_e4m3((x / s[:, None]).astype(np.float64)), s
+
+
+def _quant_amax_whole_tensor(x_bits):
+    x = O.decode_bf16(x_bits).astype(np.float32)
+    amax = np.full(x.shape[0], np.abs(x).max(), dtype=np.float32)
+    s = (amax / np.float32(448.0)).astype(np.float32)
+    return O.encode_e4m3((x / s[:, None]).astype(np.float64)), s
+
+
+def _quant_multiply_by_448_over_amax(x_bits):
+    x = O.decode_bf16(x_bits).astype(np.float32)
+    amax = np.abs(x).max(axis=1)
+    with np.errstate(divide="ignore"):
+        r = np.where(amax > 0, np.float32(448.0) / amax, np.float32(1.0)).astype(np.float32)
+    s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    with np.errstate(invalid="ignore"):
+        q = (x * r[:, None]).astype(np.float32)
+    return O.encode_e4m3(q.astype(np.float64)), s
+
+
+def _pack_scale_first(codes, scale):
+    p = _orig["pack_rows"](codes, scale)
+    H = p.shape[1] - 4
+    return np.concatenate([p[:, H:], p[:, :H]], axis=1)
+
+
+def _pack_big_endian(codes, scale):
+    codes = np.asarray(codes, dtype=np.uint8)
+    tail = np.asarray(scale, dtype=">f4").reshape(-1, 1).view(np.uint8)
+    return np.concatenate([codes, tail], axis=1)
+
+
 MUTANTS = {
+    "encode_truncate": ("encode_e4m3", _encode_truncate),
+    "encode_ties_away": ("encode_e4m3", _encode_ties_away),
+    "encode_no_saturation": ("encode_e4m3", _encode_no_saturation),
+    "encode_drops_sign": ("encode_e4m3", _encode_drops_sign),
+    "quant_scale_127": ("row_quantise", _quant_scale_127),
+    "quant_amax_whole_tensor": ("row_quantise", _quant_amax_whole_tensor),
+    "quant_multiply_by_reciprocal": ("row_quantise", _quant_multiply_by_448_over_amax),
+    "pack_scale_first": ("pack_rows", _pack_scale_first),
+    "pack_big_endian": ("pack_rows", _pack_big_endian),
     "e4m3_bias8": ("decode_e4m3", _e4m3_bias8),
     "e4m3_subnormal_as_normal": ("decode_e4m3", _e4m3_subnormal_as_normal),
     "e4m3_unsigned": ("decode_e4m3", _e4m3_unsigned),

@@ -187,6 +187,27 @@ def rope_tables(call: Call, rows: int):
     return torch.cat([cos, cos], dim=1).contiguous(), torch.cat([sin, sin], dim=1).contiguous()
 
 
+def make_activations(call: Call) -> torch.Tensor:
+    """The bf16 activations [T, H] of a call (the producer's input): N(0, 1), with
+    round(outlier_frac * T) seeded rows carrying a seeded set of 64 channels x20."""
+    T, H, s = call.tokens, call.hidden, call.seed
+    a = torch.randn(T, H, generator=_gen(s, 0), dtype=torch.float32).to(torch.bfloat16)
+    n_out = int(round(call.outlier_frac * T))
+    if n_out > 0:
+        rows = torch.randperm(T, generator=_gen(s, 4))[:n_out]
+        chans = torch.randperm(H, generator=_gen(s, 5))[:64]
+        block = a[rows][:, chans].float() * 20.0
+        sub = a[rows]
+        sub[:, chans] = block.to(torch.bfloat16)
+        a[rows] = sub
+    return a
+
+
+def bf16_bits(x: torch.Tensor):
+    """A bf16 tensor's bit patterns as a numpy uint16 array (for the oracle)."""
+    return x.contiguous().view(torch.int16).numpy().view("uint16")
+
+
 def make_inputs(call: Call) -> Dict[str, Optional[torch.Tensor]]:
     """All inputs of one call as CPU tensors.
 
@@ -197,15 +218,7 @@ def make_inputs(call: Call) -> Dict[str, Optional[torch.Tensor]]:
     """
     T, H, I, d = call.tokens, call.hidden, call.width, call.d_head
     s = call.seed
-    a = torch.randn(T, H, generator=_gen(s, 0), dtype=torch.float32).to(torch.bfloat16)
-    n_out = int(round(call.outlier_frac * T))
-    if n_out > 0:
-        rows = torch.randperm(T, generator=_gen(s, 4))[:n_out]
-        chans = torch.randperm(H, generator=_gen(s, 5))[:64]
-        block = a[rows][:, chans].float() * 20.0
-        sub = a[rows]
-        sub[:, chans] = block.to(torch.bfloat16)
-        a[rows] = sub
+    a = make_activations(call)
     A, a_scale = row_quantise(a)
     del a
     w = torch.randn(I, H, generator=_gen(s, 1), dtype=torch.float32) * call.w_std
