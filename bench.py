@@ -52,6 +52,8 @@ def _args():
                    help="GEMM form: 256-row tiles on SM pairs, 128-row tiles on one SM, or the library's choice")
     p.add_argument("--layout", choices=["bsd", "nbsd"], default="bsd",
                    help="output layout: BSD [T, I] or NBSd [heads, T, d_head]")
+    p.add_argument("--input", choices=["fp8", "packed", "bf16"], default="fp8",
+                   help="what the step is fed: e4m3 rows + scales, packed [T, H+4] rows, or bf16 activations")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
@@ -227,7 +229,14 @@ def run_reference(args):
     return 0
 
 
-def _config(call, tile_n, flushed=True, layout="bsd"):
+_INPUT_NOTE = {
+    "fp8": "e4m3 codes [T, H] + fp32 row scales [T]",
+    "packed": "packed [T, H+4] rows (codes + fp32 scale tail), unpacked inside the step",
+    "bf16": "bf16 activations [T, H], row-quantised to e4m3 inside the step",
+}
+
+
+def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8"):
     return {
         "workload": (f"{call.name}: Wan2.2-style fused QKV self-attention projection, T={call.tokens} "
                      f"H={call.hidden} n_q={call.n_q_heads} n_kv={call.n_kv_heads} d_head={call.d_head} "
@@ -236,6 +245,7 @@ def _config(call, tile_n, flushed=True, layout="bsd"):
         "n_q_heads": call.n_q_heads, "n_kv_heads": call.n_kv_heads, "d_head": call.d_head,
         "tile_n": tile_n,
         "output_layout": "NBSd [heads, T, d_head]" if layout == "nbsd" else "BSD [T, I]",
+        "input": _INPUT_NOTE[input_kind],
         "l2": "flushed between timed steps (256 MB write, outside the step events)" if flushed
         else "not flushed",
     }
@@ -247,7 +257,8 @@ def run_ours(args):
 
     import workloads as wl
     from rope_tcgen05_mxfp8_gb300 import (QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA,
-                                          QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_SERIAL_PASSES, QKV_CTE_LAYOUT_BSD,
+                                          QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_SERIAL_PASSES, QKV_CTE_INPUT_BF16,
+                                          QKV_CTE_INPUT_PACKED, QKV_CTE_INPUT_ROW_FP8, QKV_CTE_LAYOUT_BSD,
                                           QKV_CTE_LAYOUT_NBSD, QkvCte)
     from rope_tcgen05_mxfp8_gb300 import build as b
 
@@ -272,9 +283,19 @@ def run_ours(args):
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     gemm_flag = {"auto": 0, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA}[args.gemm]
     layout = QKV_CTE_LAYOUT_NBSD if args.layout == "nbsd" else QKV_CTE_LAYOUT_BSD
+    input_layout = {"fp8": QKV_CTE_INPUT_ROW_FP8, "packed": QKV_CTE_INPUT_PACKED, "bf16": QKV_CTE_INPUT_BF16}[args.input]
+    # The step's activation input, resident on the device (and its host copy for e2e).
+    if args.input == "bf16":
+        a_host = wl.make_activations(call)
+    elif args.input == "packed":
+        a_host = torch.cat([inp["A"], inp["a_scale"].view(torch.uint8).reshape(call.tokens, 4)], dim=1)
+    else:
+        a_host = inp["A"]
+    a_in = a_host.to(dev)
+    a_scale_in = g["a_scale"] if args.input == "fp8" else None
     op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
                 rope=call.rope, eps=call.eps, tile_n=args.tile_n, flags=QKV_CTE_FLAG_PROFILE | gemm_flag, device=dev,
-                output_layout=layout)
+                output_layout=layout, input_layout=input_layout)
     tile_n = op.info.tile_n
     out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=dev)
     sumsq = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
@@ -282,7 +303,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        op(g["A"], g["a_scale"], g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"],
+        op(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"],
            out=out, sumsq=sumsq, stream=stream)
 
     for _ in range(max(args.warmup, 0)):
@@ -324,12 +345,12 @@ def run_ours(args):
     serial = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
                     rope=call.rope, eps=call.eps, tile_n=args.tile_n,
                     flags=QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES | gemm_flag, device=dev,
-                    output_layout=layout)
+                    output_layout=layout, input_layout=input_layout)
     ser = []
     for i in range(max(3, min(args.steps, 10))):
         if not args.no_flush:
             flush.zero_()
-        serial(g["A"], g["a_scale"], g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"],
+        serial(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"],
                g["sin"], out=out, sumsq=sumsq, stream=stream)
         ser.append(serial.pass_times())
     serial.status(stream)
@@ -350,8 +371,8 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        A_h = inp["A"].pin_memory()
-        s_h = inp["a_scale"].pin_memory()
+        A_h = a_host.pin_memory()
+        s_h = inp["a_scale"].pin_memory() if args.input == "fp8" else None
         O_h = torch.empty(call.tokens, call.width, dtype=torch.bfloat16).pin_memory()
         e2e_ev = []
         for i in range(args.warmup + args.steps):
@@ -359,8 +380,9 @@ def run_ours(args):
             if not args.no_flush:
                 flush.zero_()
             e0.record(stream)
-            g["A"].copy_(A_h, non_blocking=True)
-            g["a_scale"].copy_(s_h, non_blocking=True)
+            a_in.copy_(A_h, non_blocking=True)
+            if s_h is not None:
+                a_scale_in.copy_(s_h, non_blocking=True)
             step()
             O_h.copy_(out, non_blocking=True)
             e1.record(stream)
@@ -370,10 +392,11 @@ def run_ours(args):
         e2e_per_s, e2e_ms = replica_throughput(sum(a.elapsed_time(b2) for a, b2 in e2e_ev), flops * args.steps,
                                                world, device=dev)
         e2e = {"value": e2e_per_s / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(A_h.numel() * A_h.element_size() + s_h.numel() * s_h.element_size()),
+               "h2d_bytes_per_step": int(A_h.numel() * A_h.element_size()
+                                         + (s_h.numel() * s_h.element_size() if s_h is not None else 0)),
                "d2h_bytes_per_step": int(O_h.numel() * O_h.element_size()),
                "ms_per_step": e2e_ms / args.steps,
-               "note": "pinned host A codes + row scales in, full bf16 O out, through the C ABI"}
+               "note": f"pinned host input ({_INPUT_NOTE[args.input]}) in, full bf16 O out, through the C ABI"}
         op.status(stream)
 
     cpu = None
@@ -391,11 +414,22 @@ def run_ours(args):
                           f"({dt:.2f} s; float64 numpy, BLAS threads via {how})")}
 
     traffic = _k1_traffic(args.workload, tile_n, bool(op.info.cta_pair))
+    producer = None
+    if args.input != "fp8":
+        # bytes the producer step must move: read the input rows, write e4m3 codes + scales
+        in_row = 2 * call.hidden if args.input == "bf16" else call.hidden + 4
+        p_bytes = call.tokens * (in_row + call.hidden + 4)
+        producer = {"kernel": "row_quantize_kernel" if args.input == "bf16" else "unpack_rows_kernel",
+                    "bytes": p_bytes, "prep_ms": prep_ms,
+                    "GB/s": p_bytes / (prep_ms * 1e-3) / 1e9,
+                    "frac_of_hbm": p_bytes / (prep_ms * 1e-3) / 1e9 / hbm_gbs,
+                    "how": "prep_ms (CUDA events) covers the producer launch plus the small scale-repack/"
+                           "clear launch, so the rate is a lower bound for the producer alone"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; Wan2.2 480p shapes and distributions)",
-        "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout),
+        "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout, input_kind=args.input),
         "pct_nominal_dense_fp8_peak": 100.0 * value / (world * NOMINAL_FP8_TFLOPS),
         "pct_measured_fp8_peak": 100.0 * value / (world * fp8_peak),
         "passes_ms": {"prep": prep_ms, "gemm_epilogue": gemm_ms, "norm_rope_span": norm_span_ms,
@@ -416,7 +450,8 @@ def run_ours(args):
                                      f"{FP8_PER_BF16:g}")},
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": (3 if args.input == "fp8" else 4) * args.steps,
+        "producer": producer,
         "cpu_baseline": cpu,
     }
     if rank == 0:

@@ -33,7 +33,9 @@
  *   per-call scratch (repacked weight scales, the sum-of-squares accumulator, a device
  *   status word, per-panel completion counters, timing stamps and, when a norm or RoPE
  *   pass runs, the un-normalised Q and K columns in block floating point: about
- *   2.06*ceil(T/128)*128*(n_q + n_kv)*d_head bytes) and must not be shared by calls that overlap on the GPU. The norm/RoPE
+ *   2.06*ceil(T/128)*128*(n_q + n_kv)*d_head bytes; with a packed or bf16 input also
+ *   the e4m3 codes and row scales the producer step writes, T*(H + 4) bytes) and must
+ *   not be shared by calls that overlap on the GPU. The norm/RoPE
  *   kernel is launched as a programmatic dependent of the GEMM so the two overlap. qkv_cte_run is stream-ordered and asynchronous: it never
  *   synchronises. O must not alias any input.
  *
@@ -54,7 +56,7 @@
 extern "C" {
 #endif
 
-#define QKV_CTE_ABI_VERSION 1
+#define QKV_CTE_ABI_VERSION 2
 
 #define QKV_CTE_OK 0
 #define QKV_CTE_ERR_INVALID (-1)        /* null / inconsistent argument, mode-segment mismatch */
@@ -65,6 +67,18 @@ extern "C" {
 
 enum { QKV_CTE_MODE_FUSED = 0, QKV_CTE_MODE_SEPARATE = 1 };
 enum { QKV_CTE_LAYOUT_BSD = 0, QKV_CTE_LAYOUT_NBSD = 1 };
+
+/* What `A` of qkv_cte_run holds ([qkv_cte] "Interface" table, packed_hidden row, and
+ * its producer):
+ *   ROW_FP8: e4m3 codes [T, H] (16-byte aligned) with the fp32 row scales in a_scale;
+ *   PACKED : the packed rows [T, H + 4] (each row's H codes, then its fp32 scale,
+ *            little-endian; 4-byte aligned); a_scale must be NULL. The run first
+ *            unpacks them into the workspace (their pitch is not 16-byte aligned, so
+ *            the GEMM's TMA loads cannot read them in place);
+ *   BF16   : bf16 activations [T, H] (16-byte aligned); a_scale must be NULL. The run
+ *            first quantises them per row into the workspace, exactly as
+ *            qkv_cte_row_quantize does. */
+enum { QKV_CTE_INPUT_ROW_FP8 = 0, QKV_CTE_INPUT_PACKED = 1, QKV_CTE_INPUT_BF16 = 2 };
 
 /* Test hook: the GEMM's load warp issues nothing, so every bounded wait downstream
  * runs out and the kernel exits through its error path (status word set). */
@@ -96,7 +110,7 @@ typedef struct {
     float eps;             /* norm epsilon, >= 0 */
     uint32_t flags;        /* 0 or QKV_CTE_FLAG_* bits */
     int32_t tile_n;        /* GEMM N tile: 0 = automatic, else 128, 192, 240 or 256 */
-    int32_t reserved;      /* must be 0 */
+    int32_t input_layout;  /* QKV_CTE_INPUT_*: what A holds (0 = e4m3 codes + separate scales) */
 } qkv_cte_desc;
 
 typedef struct qkv_cte_plan_s* qkv_cte_plan_t;
@@ -115,7 +129,8 @@ typedef struct {
 /* Validate `desc` (host only, no CUDA call) and create a plan.
  * out            : receives the plan (set to NULL on error).
  * workspace_bytes: receives the device workspace size qkv_cte_run needs.
- * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values) or
+ * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values,
+ * unknown input layout) or
  * -2 (H % 128, d_head % 16, T > INT32_MAX, unknown tile_n). */
 int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes);
 
@@ -124,8 +139,10 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info);
 
 /* Run the whole path on `stream` (a cudaStream_t; NULL = legacy default stream).
  *
- * A          : uint8  [T, H]      e4m3 codes, row-major; 16-byte aligned
- * a_scale    : fp32   [T]         per-row dequant scale
+ * A          : per desc.input_layout (QKV_CTE_INPUT_*): uint8 [T, H] e4m3 codes, row-major,
+ *              16-byte aligned; or packed uint8 [T, H + 4] rows, 4-byte aligned; or bf16
+ *              [T, H], 16-byte aligned
+ * a_scale    : fp32   [T]         per-row dequant scale (ROW_FP8 input only; NULL otherwise)
  * W          : uint8  [I, H]      e4m3 codes, K-major (row i = output channel i); 16-byte aligned
  * w_sf       : uint8  [I, H/32]   UE8M0 block scales, row-major; 4-byte aligned
  * w_col_scale: fp32   [I] or NULL per-output-channel multiplier ("weight_scales"); 16-byte aligned
@@ -159,7 +176,8 @@ int qkv_cte_status(void* workspace, void* stream);
 
 /* Device times in milliseconds of the most recent run of `plan`, which must have been
  * created with QKV_CTE_FLAG_PROFILE. ms must hold 4 floats:
- *   ms[0] prep (scale repack and clears), from CUDA events around its launch;
+ *   ms[0] prep (the input's unpack or quantise step when it is packed or bf16, the
+ *         scale repack and clears), from CUDA events around those launches;
  *   ms[1] GEMM with its fused epilogue, and ms[2] norm + RoPE (0 when the call has
  *         neither): first-block start to last-block end, from %globaltimer stamps the
  *         kernels write into the workspace (the two passes overlap, so no CUDA event
@@ -168,6 +186,34 @@ int qkv_cte_status(void* workspace, void* stream);
  * Blocks until that run has finished; its workspace must still be valid. Returns 0, -1
  * (no flag, never run, null pointer) or -3. */
 int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms);
+
+/* The producer step on its own: bf16 activations -> ROW_MX rows ([qkv_cte] "Interface"
+ * table, packed_hidden row: per-row FP8 codes plus one fp32 dequant scale, made by the
+ * projection's producer; "Upstream behavior": the packed H + 4 layout).
+ *
+ * Per row t: amax = max_h |X[t, h]|; s = amax / 448 (1.0 for an all-zero row); code
+ * = e4m3(X[t, h] / s), the quotient an IEEE fp32 division, converted with round to
+ * nearest even and saturation to +-448 (the row's largest element maps to 448). X
+ * must be finite.
+ *
+ * X       : bf16 [T, H], 16-byte aligned
+ * A       : uint8 [T, H] e4m3 codes or NULL; 16-byte aligned
+ * a_scale : fp32 [T] dequant scales or NULL (given together with A); 4-byte aligned
+ * packed  : uint8 [T, H + 4] packed rows (codes, then the scale's 4 bytes,
+ *           little-endian) or NULL; 4-byte aligned
+ * At least one of A / packed; no output may overlap X or another output. H % 16 == 0.
+ * Stream-ordered and asynchronous. Returns 0, -1 (null or overlapping buffers, no
+ * output), -2 (H % 16, alignment, T > INT32_MAX), -3 or -4. tokens == 0 checks only
+ * tokens and hidden, launches nothing and returns 0 (every pointer may be NULL). */
+int qkv_cte_row_quantize(const uint16_t* X, int64_t tokens, int32_t hidden, uint8_t* A, float* a_scale,
+                         uint8_t* packed, void* stream);
+
+/* Packed rows [T, H + 4] (4-byte aligned) -> e4m3 codes A [T, H] (16-byte aligned) and
+ * fp32 scales a_scale [T] (4-byte aligned): the layout qkv_cte_run reads with
+ * QKV_CTE_INPUT_ROW_FP8. Byte-exact. H % 16 == 0; buffers must not overlap.
+ * Returns 0, -1, -2, -3 or -4 as qkv_cte_row_quantize (tokens == 0 likewise). */
+int qkv_cte_unpack_rows(const uint8_t* packed, int64_t tokens, int32_t hidden, uint8_t* A, float* a_scale,
+                        void* stream);
 
 /* Size of the scratch array behind qkv_cte_run_noalloc: 16 MiB on every GPU that
  * loads the library, held until the process exits. */

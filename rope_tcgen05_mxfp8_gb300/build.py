@@ -20,7 +20,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libqkvcte.so")
 
-SOURCES = ["qkv_cte_api.cu", "qkv_gemm_mxf8.cu", "qk_norm_rope.cu"]
+SOURCES = ["qkv_cte_api.cu", "qkv_gemm_mxf8.cu", "qk_norm_rope.cu", "row_quant.cu"]
 HEADERS = ["ptx.cuh", "internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -37,10 +37,12 @@ enum : uint32_t {
 //                            chunk k < k_end/16, idx = (t/128 * k_end/16 + k) * 128
 //                            + t%128; the 16 fp16 sit at qk_val[idx*16 ..] (32 bytes)
 //                            and the exponent at qk_exp[idx]
+//   [.., + T*H), [.., + 4T)  only for a packed or bf16 input: the e4m3 codes [T, H] and
+//                            fp32 row scales [T] the producer step writes for the GEMM
 constexpr size_t kStampOffset = 64;
 
 struct WorkspaceLayout {
-  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, qk_exp_off, total;
+  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, qk_exp_off, act_off, act_scale_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -169,5 +171,13 @@ cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtens
 // Launched right after K1 on the same stream as a programmatic dependent launch, so
 // its blocks start while K1 runs and take each row panel as soon as K1 marks it ready.
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap);
+
+// The producer step (row_quant.cu): bf16 [T, H] -> e4m3 codes [T, H] + fp32 scales [T]
+// and/or packed [T, H + 4] rows (either output may be null, not both); H % 16 == 0.
+cudaError_t launch_row_quantize(const uint16_t* X, int T, int H, uint8_t* codes, float* scale, uint8_t* packed,
+                                cudaStream_t s, int num_sms);
+// Packed [T, H + 4] -> codes [T, H] + scales [T]; H % 16 == 0.
+cudaError_t launch_unpack_rows(const uint8_t* packed, int T, int H, uint8_t* codes, float* scale, cudaStream_t s,
+                               int num_sms);
 
 }  // namespace qkvcte

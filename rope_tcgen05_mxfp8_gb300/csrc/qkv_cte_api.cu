@@ -181,7 +181,9 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   if ((d.flags & ~known_flags) != 0) return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
   if ((d.flags & QKV_CTE_FLAG_GEMM_CTA_PAIR) && (d.flags & QKV_CTE_FLAG_GEMM_SINGLE_CTA))
     return fail(QKV_CTE_ERR_INVALID, "QKV_CTE_FLAG_GEMM_CTA_PAIR and QKV_CTE_FLAG_GEMM_SINGLE_CTA exclude each other");
-  if (d.reserved != 0) return fail(QKV_CTE_ERR_INVALID, "reserved must be 0");
+  if (d.input_layout != QKV_CTE_INPUT_ROW_FP8 && d.input_layout != QKV_CTE_INPUT_PACKED &&
+      d.input_layout != QKV_CTE_INPUT_BF16)
+    return fail(QKV_CTE_ERR_INVALID, "unknown input layout %d", d.input_layout);
   const long long I = (long long)(d.n_q_heads + 2LL * d.n_kv_heads) * d.d_head;
   if (I > INT32_MAX / 2) return fail(QKV_CTE_ERR_UNSUPPORTED, "output width too large");
   const int tile_n = choose_tile_n(d, (int)I);
@@ -223,7 +225,10 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   const bool second_pass = d.norm || d.rope;
   const size_t hand_rows = second_pass ? (size_t)g.blocks128 * 128 : 0;
   w.qk_exp_off = w.qk_off + align_up(hand_rows * p->k_end * sizeof(uint16_t), 256);
-  w.total = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
+  w.act_off = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
+  const bool produced = d.input_layout != QKV_CTE_INPUT_ROW_FP8;
+  w.act_scale_off = w.act_off + (produced ? align_up((size_t)g.T * g.H, 256) : 0);
+  w.total = w.act_scale_off + (produced ? align_up((size_t)g.T * sizeof(float), 256) : 0);
   *workspace_bytes = w.total;
   *out = p;
   return ok();
@@ -280,8 +285,12 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
     }
     return ok();
   }
-  if (!A || !a_scale || !W || !w_sf || !O || !workspace)
-    return fail(QKV_CTE_ERR_INVALID, "A, a_scale, W, w_sf, O and workspace are required");
+  const bool produced = d.input_layout != QKV_CTE_INPUT_ROW_FP8;
+  if (!A || !W || !w_sf || !O || !workspace)
+    return fail(QKV_CTE_ERR_INVALID, "A, W, w_sf, O and workspace are required");
+  if (!produced && !a_scale) return fail(QKV_CTE_ERR_INVALID, "a_scale is required with separate FP8 rows");
+  if (produced && a_scale)
+    return fail(QKV_CTE_ERR_INVALID, "a_scale must be NULL with a packed or bf16 input (the scales come from it)");
   if (d.norm && !gamma_q) return fail(QKV_CTE_ERR_INVALID, "norm needs gamma_q");
   if (d.norm && d.n_kv_heads > 0 && !gamma_k) return fail(QKV_CTE_ERR_INVALID, "norm with a K segment needs gamma_k");
   if (gamma_k && !(d.norm && d.n_kv_heads > 0))
@@ -289,9 +298,10 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (gamma_q && !d.norm) return fail(QKV_CTE_ERR_INVALID, "gamma_q given but norm is off");
   if (d.rope && (!cos_table || !sin_table)) return fail(QKV_CTE_ERR_INVALID, "rope needs cos and sin tables");
   if (!d.rope && (cos_table || sin_table)) return fail(QKV_CTE_ERR_INVALID, "cos/sin given but rope is off");
-  if (!aligned(A, 16) || !aligned(W, 16) || !aligned(O, 32))
-    return fail(QKV_CTE_ERR_UNSUPPORTED, "A and W must be 16-byte aligned and O 32-byte aligned");
-  if (!aligned(a_scale, 4) || !aligned(w_sf, 4) || (sumsq && !aligned(sumsq, 4)) || (inv_rms && !aligned(inv_rms, 4)))
+  if (!aligned(A, d.input_layout == QKV_CTE_INPUT_PACKED ? 4 : 16) || !aligned(W, 16) || !aligned(O, 32))
+    return fail(QKV_CTE_ERR_UNSUPPORTED,
+                "A must be 16-byte aligned (4-byte for packed rows), W 16-byte and O 32-byte aligned");
+  if ((a_scale && !aligned(a_scale, 4)) || !aligned(w_sf, 4) || (sumsq && !aligned(sumsq, 4)) || (inv_rms && !aligned(inv_rms, 4)))
     return fail(QKV_CTE_ERR_UNSUPPORTED, "a_scale, w_sf, sumsq and inv_rms must be 4-byte aligned");
   if ((w_col_scale && !aligned(w_col_scale, 16)) || (bias && !aligned(bias, 16)) ||
       (gamma_q && !aligned(gamma_q, 16)) || (gamma_k && !aligned(gamma_k, 16)))
@@ -309,12 +319,16 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (!(dev.major == 10 && dev.minor == 3))
     return fail(QKV_CTE_ERR_ARCH, "device is sm_%d%d; this library is built for sm_103a", dev.major, dev.minor);
 
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  // With a packed or bf16 input the GEMM reads the codes and scales the producer
+  // step writes into the workspace.
+  const uint8_t* A_codes = produced ? ws + plan->ws.act_off : A;
+  const float* A_scale = produced ? reinterpret_cast<const float*>(ws + plan->ws.act_scale_off) : a_scale;
   CUtensorMap tmA, tmW;
-  if ((rc = encode_operand(&tmA, A, (uint64_t)g.T, (uint64_t)g.H, 128u, "A")) != QKV_CTE_OK) return rc;
+  if ((rc = encode_operand(&tmA, A_codes, (uint64_t)g.T, (uint64_t)g.H, 128u, "A")) != QKV_CTE_OK) return rc;
   const uint32_t w_box_rows = g.cta_pair ? (uint32_t)g.tile_n / 2 : (uint32_t)g.tile_n;
   if ((rc = encode_operand(&tmW, W, (uint64_t)g.I, (uint64_t)g.H, w_box_rows, "W")) != QKV_CTE_OK) return rc;
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws + plan->ws.status_off);
   const bool need_ss = d.norm || sumsq != nullptr;
   float* ss = sumsq ? sumsq : reinterpret_cast<float*>(ws + plan->ws.sumsq_off);
@@ -335,6 +349,14 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
       return fail(QKV_CTE_ERR_CUDA, "cudaEventRecord: %s", cudaGetErrorString(e));
   }
 
+  if (d.input_layout == QKV_CTE_INPUT_PACKED)
+    e = launch_unpack_rows(A, g.T, g.H, ws + plan->ws.act_off, reinterpret_cast<float*>(ws + plan->ws.act_scale_off),
+                           s, dev.sms);
+  else if (d.input_layout == QKV_CTE_INPUT_BF16)
+    e = launch_row_quantize(reinterpret_cast<const uint16_t*>(A), g.T, g.H, ws + plan->ws.act_off,
+                            reinterpret_cast<float*>(ws + plan->ws.act_scale_off), nullptr, s, dev.sms);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "producer launch: %s", cudaGetErrorString(e));
+
   uint32_t* ready = reinterpret_cast<uint32_t*>(ws + plan->ws.ready_off);
   unsigned long long* stamps = reinterpret_cast<unsigned long long*>(ws + kStampOffset);
   e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0, ready, status,
@@ -343,7 +365,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (prof) cudaEventRecord(plan->ev[1], s);
 
   GemmArgs ga;
-  ga.a_scale = a_scale;
+  ga.a_scale = A_scale;
   ga.w_col_scale = w_col_scale;
   ga.bias = bias;
   ga.sf_packed = sf_packed;
@@ -426,6 +448,80 @@ int qkv_cte_status(void* workspace, void* stream) {
               (word & kErrEpilogueTmemFullWait) ? " epilogue-accumulator-ready" : "",
               (word & kErrDrainWait) ? " drain" : "",
               (word & kErrNormReadyWait) ? " norm-panel-ready" : "");
+}
+
+namespace {
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (a == nullptr || b == nullptr || na == 0 || nb == 0) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+int check_rows(int64_t tokens, int32_t hidden, const char* who) {
+  if (tokens < 0) return fail(QKV_CTE_ERR_INVALID, "%s: tokens must be >= 0", who);
+  if (tokens > INT32_MAX) return fail(QKV_CTE_ERR_UNSUPPORTED, "%s: tokens > INT32_MAX", who);
+  if (hidden <= 0) return fail(QKV_CTE_ERR_INVALID, "%s: hidden must be > 0", who);
+  if (hidden % 16 != 0) return fail(QKV_CTE_ERR_UNSUPPORTED, "%s: hidden %d is not a multiple of 16", who, hidden);
+  return QKV_CTE_OK;
+}
+
+int check_device(DeviceInfo* dev) {
+  int rc = device_info(dev);
+  if (rc != QKV_CTE_OK) return rc;
+  if (!(dev->major == 10 && dev->minor == 3))
+    return fail(QKV_CTE_ERR_ARCH, "device is sm_%d%d; this library is built for sm_103a", dev->major, dev->minor);
+  return QKV_CTE_OK;
+}
+
+}  // namespace
+
+int qkv_cte_row_quantize(const uint16_t* X, int64_t tokens, int32_t hidden, uint8_t* A, float* a_scale,
+                         uint8_t* packed, void* stream) {
+  int rc = check_rows(tokens, hidden, "qkv_cte_row_quantize");
+  if (rc != QKV_CTE_OK) return rc;
+  if (tokens == 0) return ok();  // empty tensors may come as null pointers
+  if ((A == nullptr) != (a_scale == nullptr))
+    return fail(QKV_CTE_ERR_INVALID, "qkv_cte_row_quantize: give both A and a_scale, or neither");
+  if (A == nullptr && packed == nullptr)
+    return fail(QKV_CTE_ERR_INVALID, "qkv_cte_row_quantize: no output (A + a_scale and/or packed)");
+  if (X == nullptr) return fail(QKV_CTE_ERR_INVALID, "qkv_cte_row_quantize: null X");
+  if (!aligned(X, 16) || (A && !aligned(A, 16)) || (a_scale && !aligned(a_scale, 4)) || (packed && !aligned(packed, 4)))
+    return fail(QKV_CTE_ERR_UNSUPPORTED,
+                "qkv_cte_row_quantize: X and A must be 16-byte aligned, a_scale and packed 4-byte aligned");
+  const size_t T = (size_t)tokens, H = (size_t)hidden;
+  if (overlaps(X, T * H * 2, A, T * H) || overlaps(X, T * H * 2, a_scale, T * 4) ||
+      overlaps(X, T * H * 2, packed, T * (H + 4)) || overlaps(A, T * H, packed, T * (H + 4)) ||
+      overlaps(a_scale, T * 4, packed, T * (H + 4)) || overlaps(A, T * H, a_scale, T * 4))
+    return fail(QKV_CTE_ERR_INVALID, "qkv_cte_row_quantize: buffers overlap");
+  DeviceInfo dev;
+  if ((rc = check_device(&dev)) != QKV_CTE_OK) return rc;
+  cudaError_t e = launch_row_quantize(X, (int)tokens, hidden, A, a_scale, packed, static_cast<cudaStream_t>(stream),
+                                      dev.sms);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "row quantise launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int qkv_cte_unpack_rows(const uint8_t* packed, int64_t tokens, int32_t hidden, uint8_t* A, float* a_scale,
+                        void* stream) {
+  int rc = check_rows(tokens, hidden, "qkv_cte_unpack_rows");
+  if (rc != QKV_CTE_OK) return rc;
+  if (tokens == 0) return ok();
+  if (packed == nullptr || A == nullptr || a_scale == nullptr)
+    return fail(QKV_CTE_ERR_INVALID, "qkv_cte_unpack_rows: packed, A and a_scale are required");
+  if (!aligned(packed, 4) || !aligned(A, 16) || !aligned(a_scale, 4))
+    return fail(QKV_CTE_ERR_UNSUPPORTED,
+                "qkv_cte_unpack_rows: packed and a_scale must be 4-byte aligned, A 16-byte aligned");
+  const size_t T = (size_t)tokens, H = (size_t)hidden;
+  if (overlaps(packed, T * (H + 4), A, T * H) || overlaps(packed, T * (H + 4), a_scale, T * 4) ||
+      overlaps(A, T * H, a_scale, T * 4))
+    return fail(QKV_CTE_ERR_INVALID, "qkv_cte_unpack_rows: buffers overlap");
+  DeviceInfo dev;
+  if ((rc = check_device(&dev)) != QKV_CTE_OK) return rc;
+  cudaError_t e = launch_unpack_rows(packed, (int)tokens, hidden, A, a_scale, static_cast<cudaStream_t>(stream),
+                                     dev.sms);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "unpack launch: %s", cudaGetErrorString(e));
+  return ok();
 }
 
 }  // extern "C"

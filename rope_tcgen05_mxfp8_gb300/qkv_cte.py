@@ -25,6 +25,9 @@ QKV_CTE_MODE_FUSED = 0
 QKV_CTE_MODE_SEPARATE = 1
 QKV_CTE_LAYOUT_BSD = 0
 QKV_CTE_LAYOUT_NBSD = 1
+QKV_CTE_INPUT_ROW_FP8 = 0
+QKV_CTE_INPUT_PACKED = 1
+QKV_CTE_INPUT_BF16 = 2
 QKV_CTE_FLAG_TEST_STALL = 0x1
 QKV_CTE_FLAG_PROFILE = 0x2
 QKV_CTE_FLAG_SERIAL_PASSES = 0x4
@@ -32,7 +35,8 @@ QKV_CTE_FLAG_GEMM_CTA_PAIR = 0x8
 QKV_CTE_FLAG_GEMM_SINGLE_CTA = 0x10
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
-            "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info")
+            "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",
+            "qkv_cte_row_quantize", "qkv_cte_unpack_rows")
 QKV_CTE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -50,7 +54,7 @@ class qkv_cte_desc(ctypes.Structure):
         ("eps", ctypes.c_float),
         ("flags", ctypes.c_uint32),
         ("tile_n", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("input_layout", ctypes.c_int32),
     ]
 
 
@@ -97,6 +101,10 @@ def load() -> ctypes.CDLL:
     lib.qkv_cte_get_plan_info.restype = ctypes.c_int
     lib.qkv_cte_run_noalloc.argtypes = [P] * 15
     lib.qkv_cte_run_noalloc.restype = ctypes.c_int
+    lib.qkv_cte_row_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P, P]
+    lib.qkv_cte_row_quantize.restype = ctypes.c_int
+    lib.qkv_cte_unpack_rows.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
+    lib.qkv_cte_unpack_rows.restype = ctypes.c_int
     lib.qkv_cte_status.argtypes = [P, P]
     lib.qkv_cte_status.restype = ctypes.c_int
     lib.qkv_cte_pass_times.argtypes = [P, ctypes.POINTER(ctypes.c_float)]
@@ -126,11 +134,12 @@ def _check(rc: int) -> int:
 
 
 def make_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=1, rope=1, eps=1e-6,
-              mode=None, output_layout=QKV_CTE_LAYOUT_BSD, flags=0, tile_n=0) -> qkv_cte_desc:
+              mode=None, output_layout=QKV_CTE_LAYOUT_BSD, flags=0, tile_n=0,
+              input_layout=QKV_CTE_INPUT_ROW_FP8) -> qkv_cte_desc:
     if mode is None:
         mode = QKV_CTE_MODE_FUSED if n_kv_heads > 0 else QKV_CTE_MODE_SEPARATE
     return qkv_cte_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, mode, norm, rope, output_layout,
-                        eps, flags, tile_n, 0)
+                        eps, flags, tile_n, input_layout)
 
 
 def qkv_cte_plan(desc: qkv_cte_desc):
@@ -152,7 +161,8 @@ def qkv_cte_destroy(plan) -> None:
 
 
 _DTYPES = {
-    "A": (torch.uint8,), "W": (torch.uint8,), "w_sf": (torch.uint8,),
+    "A": (torch.uint8, torch.bfloat16, torch.int16, torch.uint16), "W": (torch.uint8,), "w_sf": (torch.uint8,),
+    "X": (torch.bfloat16, torch.int16, torch.uint16), "packed": (torch.uint8,),
     "a_scale": (torch.float32,), "w_col_scale": (torch.float32,),
     "bias": (torch.bfloat16, torch.int16, torch.uint16),
     "gamma_q": (torch.bfloat16, torch.int16, torch.uint16),
@@ -205,6 +215,37 @@ def qkv_cte_run_noalloc(plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, g
     return _check(load().qkv_cte_run_noalloc(plan, *args, ctypes.c_void_p(handle)))
 
 
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def qkv_cte_row_quantize(X, A=None, a_scale=None, packed=None, stream=None):
+    """bf16 X [T, H] -> e4m3 codes A [T, H] + fp32 a_scale [T] and/or packed [T, H + 4]
+    rows (the outputs given, or, with none given, A and a_scale allocated here).
+    Returns (A, a_scale, packed)."""
+    T, H = X.shape
+    if A is None and a_scale is None and packed is None:
+        A = torch.empty(T, H, dtype=torch.uint8, device=X.device)
+        a_scale = torch.empty(T, dtype=torch.float32, device=X.device)
+    _check(load().qkv_cte_row_quantize(_ptr("X", X), T, H, _ptr("A", A), _ptr("a_scale", a_scale),
+                                       _ptr("packed", packed), _stream_handle(stream)))
+    return A, a_scale, packed
+
+
+def qkv_cte_unpack_rows(packed, A=None, a_scale=None, stream=None):
+    """Packed [T, H + 4] rows -> (A uint8 [T, H], a_scale fp32 [T])."""
+    T, H = packed.shape[0], packed.shape[1] - 4
+    if A is None:
+        A = torch.empty(T, H, dtype=torch.uint8, device=packed.device)
+    if a_scale is None:
+        a_scale = torch.empty(T, dtype=torch.float32, device=packed.device)
+    _check(load().qkv_cte_unpack_rows(_ptr("packed", packed), T, H, _ptr("A", A), _ptr("a_scale", a_scale),
+                                      _stream_handle(stream)))
+    return A, a_scale
+
+
 def qkv_cte_status(workspace, stream=None) -> int:
     """Synchronise the stream and raise QkvCteError if a bounded device wait ran out."""
     if stream is None:
@@ -228,9 +269,11 @@ class QkvCte:
     """
 
     def __init__(self, tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=1, rope=1, eps=1e-6,
-                 tile_n=0, flags=0, device=None, output_layout=QKV_CTE_LAYOUT_BSD):
+                 tile_n=0, flags=0, device=None, output_layout=QKV_CTE_LAYOUT_BSD,
+                 input_layout=QKV_CTE_INPUT_ROW_FP8):
         self.desc = make_desc(tokens, hidden, n_q_heads, n_kv_heads, d_head, norm=norm, rope=rope,
-                              eps=eps, tile_n=tile_n, flags=flags, output_layout=output_layout)
+                              eps=eps, tile_n=tile_n, flags=flags, output_layout=output_layout,
+                              input_layout=input_layout)
         self.plan, self.workspace_bytes = qkv_cte_plan(self.desc)
         self.info = qkv_cte_get_plan_info(self.plan)
         self.width = (n_q_heads + 2 * n_kv_heads) * d_head

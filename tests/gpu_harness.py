@@ -22,23 +22,25 @@ def to_device(inp, dev):
     return {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
 
 
-def run_path(call, g, tile_n=0, flags=0, want_sumsq=True, want_inv=True, stream=None, out=None, nbsd=False):
+def run_path(call, g, tile_n=0, flags=0, want_sumsq=True, want_inv=True, stream=None, out=None, nbsd=False,
+             input_layout=0, A_in=None):
     """Run through the C ABI; the returned O is always viewed as BSD [T, I] (an NBSd
     result is permuted back, so the comparison sees every element where the oracle
-    puts it)."""
+    puts it). With a packed or bf16 input layout, A_in is that input on the device."""
     from rope_tcgen05_mxfp8_gb300 import QKV_CTE_LAYOUT_BSD, QKV_CTE_LAYOUT_NBSD
 
     dev = g["A"].device
     op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
                 rope=call.rope, eps=call.eps, tile_n=tile_n, flags=flags, device=dev,
-                output_layout=QKV_CTE_LAYOUT_NBSD if nbsd else QKV_CTE_LAYOUT_BSD)
+                output_layout=QKV_CTE_LAYOUT_NBSD if nbsd else QKV_CTE_LAYOUT_BSD, input_layout=input_layout)
     sumsq = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev) if want_sumsq else None
     inv = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev) if want_inv else None
     heads = call.width // call.d_head
     if out is None:
         shape = (heads, call.tokens, call.d_head) if nbsd else (call.tokens, call.width)
         out = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=dev)
-    op(g["A"], g["a_scale"], g["W"], g["w_sf"], g["bias"], g["gamma_q"] if call.norm else None,
+    A, a_scale = (g["A"], g["a_scale"]) if input_layout == 0 else (A_in, None)
+    op(A, a_scale, g["W"], g["w_sf"], g["bias"], g["gamma_q"] if call.norm else None,
        g["gamma_k"] if call.norm else None, g["cos"], g["sin"], out=out, w_col_scale=g["w_col_scale"],
        sumsq=sumsq, inv_rms=inv, stream=stream)
     if nbsd:

@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_version():
-    assert pkg.qkv_cte_version() == 1
+    assert pkg.qkv_cte_version() == 2
 
 
 def _plan_code(**kw):
@@ -48,9 +48,7 @@ def _plan_code(**kw):
     base.update(kw)
     desc = q.make_desc(**{k: v for k, v in base.items() if k in
                           ("tokens", "hidden", "n_q_heads", "n_kv_heads", "d_head", "norm", "rope", "eps",
-                           "mode", "output_layout", "flags", "tile_n")})
-    if "reserved" in kw:
-        desc.reserved = kw["reserved"]
+                           "mode", "output_layout", "flags", "tile_n", "input_layout")})
     try:
         plan, ws = q.qkv_cte_plan(desc)
     except q.QkvCteError as e:
@@ -84,7 +82,10 @@ def _plan_code(**kw):
     (dict(flags=0x80), -1),
     (dict(tile_n=100), -2),
     (dict(tile_n=240), 0),
-    (dict(reserved=3), -1),
+    (dict(input_layout=3), -1),
+    (dict(input_layout=-1), -1),
+    (dict(input_layout=1), 0),
+    (dict(input_layout=2), 0),
     (dict(n_kv_heads=0, mode=1, norm=1, rope=0), 0),
 ])
 def test_plan_validation(kw, code):
@@ -124,10 +125,12 @@ def test_error_message_is_recorded():
     assert "multiple of 128" in q.qkv_cte_last_error()
 
 
-def test_workspace_size_formula():
+@pytest.mark.parametrize("input_layout", [0, 1, 2])
+def test_workspace_size_formula(input_layout):
     for T, I_heads, tile in ((32760, (40, 40), 256), (1, (1, 1), 128), (4096, (40, 0), 240)):
         nq, nkv = I_heads
-        desc = q.make_desc(T, 5120, nq, nkv, 128, rope=0 if nkv == 0 else 1, tile_n=tile)
+        desc = q.make_desc(T, 5120, nq, nkv, 128, rope=0 if nkv == 0 else 1, tile_n=tile,
+                           input_layout=input_layout)
         plan, ws = q.qkv_cte_plan(desc)
         q.qkv_cte_destroy(plan)
         I = (nq + 2 * nkv) * 128
@@ -138,7 +141,9 @@ def test_workspace_size_formula():
         kq = (nq + nkv) * 128
         qk = -(-(rows * kq * 2) // 256) * 256 + -(-(rows * kq // 16) // 256) * 256  # hand-off
         ready = -(-(-(-T // 128) * 4) // 256) * 256        # per-panel counters
-        assert ws == 256 + ss + -(-sf // 256) * 256 + ready + qk
+        # a packed or bf16 input: the producer's codes [T, H] and row scales [T]
+        act = (-(-(T * 5120) // 256) * 256 + -(-(T * 4) // 256) * 256) if input_layout else 0
+        assert ws == 256 + ss + -(-sf // 256) * 256 + ready + qk + act
 
 
 def test_run_rejects_null_plan_without_launch():
@@ -179,6 +184,55 @@ def test_run_argument_checks_precede_any_cuda_call():
         assert rc == q.QKV_CTE_ERR_INVALID and "workspace" in q.qkv_cte_last_error()
     finally:
         q.qkv_cte_destroy(plan)
+
+
+def test_run_input_layout_checks():
+    """a_scale goes with separate FP8 rows only; packed rows need only 4-byte alignment."""
+    lib = pkg.load()
+    fake = ctypes.c_void_p(4096)
+    for layout in (1, 2):
+        plan, ws = q.qkv_cte_plan(q.make_desc(256, 512, 4, 4, 128, input_layout=layout))
+        try:
+            args = [fake] * 14
+            rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws), None)    # a_scale given
+            assert rc == q.QKV_CTE_ERR_INVALID and "a_scale must be NULL" in q.qkv_cte_last_error()
+            args[0] = ctypes.c_void_p(4100)                                    # A 4-byte aligned only
+            args[1] = None
+            rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws - 1), None)
+            if layout == 1:   # passes the alignment check, stops at the workspace size
+                assert rc == q.QKV_CTE_ERR_INVALID and "workspace" in q.qkv_cte_last_error()
+            else:
+                assert rc == q.QKV_CTE_ERR_UNSUPPORTED and "aligned" in q.qkv_cte_last_error()
+        finally:
+            q.qkv_cte_destroy(plan)
+    plan, ws = q.qkv_cte_plan(q.make_desc(256, 512, 4, 4, 128))
+    try:
+        args = [fake] * 14
+        args[1] = None
+        rc = lib.qkv_cte_run(plan, *args, ctypes.c_size_t(ws), None)
+        assert rc == q.QKV_CTE_ERR_INVALID and "a_scale is required" in q.qkv_cte_last_error()
+    finally:
+        q.qkv_cte_destroy(plan)
+
+
+def test_producer_entry_points_check_arguments_on_the_host():
+    lib = pkg.load()
+    f = ctypes.c_void_p(4096)
+    g = ctypes.c_void_p(1 << 40)
+    assert lib.qkv_cte_row_quantize(f, 4, 100, g, g, None, None) == q.QKV_CTE_ERR_UNSUPPORTED   # H % 16
+    assert lib.qkv_cte_row_quantize(f, -1, 128, g, g, None, None) == q.QKV_CTE_ERR_INVALID
+    assert lib.qkv_cte_row_quantize(f, 4, 128, None, None, None, None) == q.QKV_CTE_ERR_INVALID  # no output
+    assert lib.qkv_cte_row_quantize(f, 4, 128, g, None, None, None) == q.QKV_CTE_ERR_INVALID     # A without scale
+    assert lib.qkv_cte_row_quantize(ctypes.c_void_p(4098), 4, 128, g, g, None, None) == q.QKV_CTE_ERR_UNSUPPORTED
+    # X [4, 128] bf16 spans 1 KB from 4096; codes written into it overlap
+    assert lib.qkv_cte_row_quantize(f, 4, 128, ctypes.c_void_p(4096 + 512), g, None, None) == q.QKV_CTE_ERR_INVALID
+    assert "overlap" in q.qkv_cte_last_error()
+    assert lib.qkv_cte_row_quantize(None, 0, 128, g, g, None, None) == 0      # empty: nothing launched
+    assert lib.qkv_cte_unpack_rows(f, 4, 128, None, g, None) == q.QKV_CTE_ERR_INVALID
+    assert lib.qkv_cte_unpack_rows(f, 4, 120, g, g, None) == q.QKV_CTE_ERR_UNSUPPORTED
+    assert lib.qkv_cte_unpack_rows(ctypes.c_void_p(4098), 4, 128, g, ctypes.c_void_p(1 << 41), None) == \
+        q.QKV_CTE_ERR_UNSUPPORTED
+    assert lib.qkv_cte_unpack_rows(None, 0, 128, None, None, None) == 0
 
 
 def test_zero_tokens_launches_nothing():
