@@ -31,6 +31,10 @@ with the page's own section headings:
      to FP8 codes plus one fp32 dequant scale, optionally packed as [T, H + 4]
      rows (codes, then the scale's four bytes) ([qkv_cte] "Upstream behavior",
      packed H + 4 layout; "Interface" table, packed_hidden row).
+  6. The per-head qk-norm of the upstream kernel (RMS_NORM / LAYER_NORM with a
+     [d_head] gamma) as an alternative to the across-heads norm, and the offline
+     interleaved -> rotate-half lane permutation of the Q/K channels ([qkv_cte]
+     "Upstream behavior", per-head qk-norm bullet; "Design" 2, last paragraphs).
 
 Readings of points the page leaves open (each also listed in the design notes):
 
@@ -62,6 +66,10 @@ from __future__ import annotations
 import numpy as np
 
 SEG_Q, SEG_K, SEG_V = 0, 1, 2
+
+# qk-norm kinds: none; the across-heads RMSNorm ([qkv_cte] "Design" 1); the per-head
+# RMS_NORM / LAYER_NORM of the upstream kernel ([qkv_cte] "Upstream behavior").
+NORM_NONE, NORM_ACROSS_HEADS, NORM_HEAD_RMS, NORM_HEAD_LAYER = 0, 1, 2, 3
 
 
 # ---------------------------------------------------------------------------
@@ -191,6 +199,72 @@ def inv_rms(sumsq: np.ndarray, n_q_heads: int, n_kv_heads: int, d_head: int, eps
 # step 3: norm apply + rotate-half RoPE on one segment
 # ---------------------------------------------------------------------------
 
+def head_norm(x: np.ndarray, gamma, d_head: int, kind: int, eps: float) -> np.ndarray:
+    """Per-head qk-norm of one segment: every head's d_head lanes are normalised by
+    their own statistics, then multiplied by the per-head gamma [d_head] that all the
+    segment's heads share.
+
+      RMS_NORM:   y = x / sqrt(mean(x^2) + eps) * gamma
+      LAYER_NORM: y = (x - mean(x)) / sqrt(mean((x - mean(x))^2) + eps) * gamma
+
+    [qkv_cte] "Upstream behavior" (optional fused per-head qk-norm, RMS_NORM /
+    LAYER_NORM) and "Design" 1 (the per-head gamma is [1, d_head]; each head's slice
+    normalised by its own RMS). The page gives LAYER_NORM no bias term.
+    """
+    rows, width = x.shape
+    h = x.reshape(rows, width // d_head, d_head)
+    if kind == NORM_HEAD_LAYER:
+        h = h - h.mean(axis=2, keepdims=True)
+    inv = 1.0 / np.sqrt(np.mean(h ** 2, axis=2, keepdims=True) + eps)
+    return (h * inv * decode_bf16(gamma)[None, None, :]).reshape(rows, width)
+
+
+def rope_interleaved(y: np.ndarray, cos, sin, d_head: int) -> np.ndarray:
+    """RoPE in the interleaved-lane convention of Wan's checkpoint: lanes (2j, 2j+1)
+    of each head form pair j ([qkv_cte] "Design" 2: the caller converts it offline).
+    Tables are [rows, d_head] in the same convention (entries 2j and 2j+1 hold pair
+    j's cos / sin):
+      out[2j]   = y[2j]   * cos[2j]   - y[2j+1] * sin[2j]
+      out[2j+1] = y[2j+1] * cos[2j+1] + y[2j]   * sin[2j+1]
+    """
+    rows, width = y.shape
+    heads = width // d_head
+    h = y.reshape(rows, heads, d_head)
+    c = np.asarray(cos, dtype=np.float64)[:, None, :]
+    s_ = np.asarray(sin, dtype=np.float64)[:, None, :]
+    swapped = np.empty_like(h)
+    swapped[:, :, 0::2] = -h[:, :, 1::2]
+    swapped[:, :, 1::2] = h[:, :, 0::2]
+    return (h * c + swapped * s_).reshape(rows, width)
+
+
+def interleaved_to_rotate_half(d_head: int) -> np.ndarray:
+    """The lane permutation that turns the interleaved convention into rotate-half:
+    new lane i takes old lane perm[i], with perm[j] = 2j and perm[d/2 + j] = 2j + 1
+    for j < d/2, so pair (2j, 2j+1) becomes pair (j, j + d/2). [qkv_cte] "Design" 2
+    (the caller permutes the Q/K weights, bias, gamma and cos/sin caches once)."""
+    half = d_head // 2
+    perm = np.empty(d_head, dtype=np.int64)
+    perm[:half] = 2 * np.arange(half)
+    perm[half:] = 2 * np.arange(half) + 1
+    return perm
+
+
+def permute_qk_rows(x: np.ndarray, n_q_heads: int, n_kv_heads: int, d_head: int) -> np.ndarray:
+    """Apply ``interleaved_to_rotate_half`` to every Q and K head along axis 0 of x
+    (one entry per output channel: W [I, H], w_sf [I, H/32], bias [I], w_col_scale
+    [I]); the V channels are copied unchanged. A gamma of one segment is a call with
+    that segment's heads and n_kv_heads = 0; a cos/sin table [T, d] is permuted along
+    its columns (pass the transpose)."""
+    x = np.asarray(x)
+    perm = interleaved_to_rotate_half(d_head)
+    n_qk = n_q_heads + n_kv_heads
+    idx = np.arange(x.shape[0])
+    for h in range(n_qk):
+        idx[h * d_head:(h + 1) * d_head] = h * d_head + perm
+    return x[idx]
+
+
 def rotate_half(y: np.ndarray, d_head: int) -> np.ndarray:
     """[-y_hi, y_lo] per head: lane i pairs with lane i + d/2 ([qkv_cte] "Design" 2)."""
     rows, width = y.shape
@@ -210,7 +284,7 @@ def apply_norm_rope(x: np.ndarray, inv: np.ndarray, gamma, cos, sin, d_head: int
     """
     rows, width = x.shape
     y = x
-    if norm:
+    if norm == NORM_ACROSS_HEADS:
         y = x * inv[:, None] * decode_bf16(gamma)[None, :]
     if rope:
         heads = width // d_head
@@ -226,13 +300,17 @@ def apply_norm_rope(x: np.ndarray, inv: np.ndarray, gamma, cos, sin, d_head: int
 
 def qkv_cte(A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, *, n_q_heads: int,
             n_kv_heads: int, d_head: int, norm: int, rope: int, eps: float,
-            w_col_scale=None, rows=None):
+            w_col_scale=None, rows=None, rope_layout: str = "rotate_half"):
     """The fused projection for the given rows (all rows when ``rows`` is None).
 
+    norm is one of NORM_NONE, NORM_ACROSS_HEADS (gamma [n_heads * d_head] per
+    segment), NORM_HEAD_RMS or NORM_HEAD_LAYER (gamma [d_head] per segment).
+    rope_layout "interleaved" applies RoPE in the interleaved-lane convention
+    (``rope_interleaved``) instead of rotate-half, for checking the permutation.
     Rows are independent, so a row subset gives exactly the rows of the full
     result. Returns a dict of float64 arrays: O [rows, I] (Q/K normalised and
-    rotated, V as projected), sumsq [rows, 2], inv_rms [rows, 2] (zeros when the
-    norm is off).
+    rotated, V as projected), sumsq [rows, 2] (of the un-normalised projection, in
+    every mode), inv_rms [rows, 2] (zeros unless the norm is across heads).
     """
     if rows is not None:
         rows = np.asarray(rows)
@@ -243,14 +321,21 @@ def qkv_cte(A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, *, n_q_heads:
             sin = sin[rows]
     o = project(A, a_scale, W, w_sf, w_col_scale, bias)
     ss = segment_sumsq(o, n_q_heads, n_kv_heads, d_head)
-    inv = inv_rms(ss, n_q_heads, n_kv_heads, d_head, eps) if norm else np.zeros_like(ss)
+    across = norm == NORM_ACROSS_HEADS
+    inv = inv_rms(ss, n_q_heads, n_kv_heads, d_head, eps) if across else np.zeros_like(ss)
     out = o.copy()
     q, k, _ = segments(n_q_heads, n_kv_heads, d_head)
-    out[:, q[0]:q[1]] = apply_norm_rope(o[:, q[0]:q[1]], inv[:, SEG_Q], gamma_q, cos, sin,
-                                        d_head, norm, rope)
-    if n_kv_heads > 0:
-        out[:, k[0]:k[1]] = apply_norm_rope(o[:, k[0]:k[1]], inv[:, SEG_K], gamma_k, cos, sin,
-                                            d_head, norm, rope)
+    parts = [(q, SEG_Q, gamma_q)] + ([(k, SEG_K, gamma_k)] if n_kv_heads > 0 else [])
+    for (c0, c1), seg, gamma in parts:
+        x = o[:, c0:c1]
+        if norm in (NORM_HEAD_RMS, NORM_HEAD_LAYER):
+            x = head_norm(x, gamma, d_head, norm, eps)
+        if rope_layout == "interleaved":
+            y = apply_norm_rope(x, inv[:, seg], gamma, None, None, d_head, norm if across else 0, 0)
+            out[:, c0:c1] = rope_interleaved(y, cos, sin, d_head) if rope else y
+        else:
+            out[:, c0:c1] = apply_norm_rope(x, inv[:, seg], gamma, cos, sin, d_head, norm if across else 0,
+                                            rope)
     return dict(O=out, sumsq=ss, inv_rms=inv, projected=o)
 
 

@@ -469,7 +469,114 @@ def pin_packed_rows_layout():
     assert np.array_equal(c2, codes) and np.array_equal(s2, scale) and s2.dtype == np.float32
 
 
-PINS = [pin_nbsd_layout, pin_encode_e4m3_vs_torch, pin_encode_e4m3_saturation, pin_row_quantise_invariants,
+# --- per-head qk-norm and the interleaved -> rotate-half permutation ----------------
+
+def _head_case(seed, nq=3, nkv=2, d=8, T=4, H=64):
+    c, shape = _tiny_case(seed=seed, T=T, H=H, nq=nq, nkv=nkv, d=d)
+    rng = np.random.default_rng(seed + 500)
+    c["gamma_q"] = _rand_bf16_bits(rng, d, 1.0, 0.3)
+    c["gamma_k"] = _rand_bf16_bits(rng, d, 1.0, 0.3) if nkv else None
+    return c, shape
+
+
+def pin_head_norm_vs_torch():
+    """Per-head RMS_NORM and LAYER_NORM against torch's own fp64 rms_norm / layer_norm
+    over each head's d_head lanes with the [d_head] gamma as weight (no bias)."""
+    import torch.nn.functional as F
+
+    for kind in (O.NORM_HEAD_RMS, O.NORM_HEAD_LAYER):
+        c, shape = _head_case(seed=70 + kind)
+        nq, nkv, d = shape["n_q_heads"], shape["n_kv_heads"], shape["d_head"]
+        eps = 1e-5
+        res = _run(c, shape, norm=kind, rope=0, eps=eps)
+        o = torch.from_numpy(res["projected"])
+        T = o.shape[0]
+        for lo, hi, g in ((0, nq * d, c["gamma_q"]), (nq * d, (nq + nkv) * d, c["gamma_k"])):
+            x = o[:, lo:hi].reshape(T, -1, d)
+            w = torch.from_numpy(_torch_bf16(g))
+            ref = F.rms_norm(x, (d,), w, eps) if kind == O.NORM_HEAD_RMS else F.layer_norm(x, (d,), w, None, eps)
+            _close(res["O"][:, lo:hi], ref.reshape(T, -1).numpy(), rel=1e-12, what=f"head norm {kind}")
+        _close(res["O"][:, (nq + nkv) * d:], res["projected"][:, (nq + nkv) * d:], rel=0, what="V untouched")
+        _close(res["inv_rms"], np.zeros_like(res["inv_rms"]), rel=0, what="no across-heads inv_rms")
+
+
+def pin_head_norm_invariants():
+    """gamma = 1, no rotation: every head of Q and K has RMS 1 (RMS_NORM), or mean 0
+    and mean square 1 (LAYER_NORM), up to eps; one head per segment makes the per-head
+    RMS_NORM the across-heads norm (with the same gamma)."""
+    eps = 1e-9
+    for kind in (O.NORM_HEAD_RMS, O.NORM_HEAD_LAYER):
+        c, shape = _head_case(seed=80 + kind)
+        d = shape["d_head"]
+        ones = np.full(d, 0x3F80, dtype=np.uint16)
+        c["gamma_q"], c["gamma_k"] = ones, ones
+        res = _run(c, shape, norm=kind, rope=0, eps=eps)
+        qk = (shape["n_q_heads"] + shape["n_kv_heads"]) * d
+        h = res["O"][:, :qk].reshape(res["O"].shape[0], -1, d)
+        assert np.allclose(np.mean(h ** 2, axis=2), 1.0, rtol=1e-6)
+        if kind == O.NORM_HEAD_LAYER:
+            assert np.allclose(np.mean(h, axis=2), 0.0, atol=1e-9)
+    c, shape = _tiny_case(seed=85, T=5, H=64, nq=1, nkv=1, d=8)
+    per_head = _run(c, shape, norm=O.NORM_HEAD_RMS, rope=1)
+    across = _run(c, shape, norm=O.NORM_ACROSS_HEADS, rope=1)
+    _close(per_head["O"], across["O"], rel=1e-12, what="one head per segment")
+
+
+def pin_rope_interleaved_complex():
+    """Interleaved RoPE is the complex product of each lane pair (2j, 2j+1) with
+    e^{i theta_j} (tables carry theta_j at lanes 2j and 2j+1)."""
+    rng = np.random.default_rng(90)
+    T, heads, d = 3, 2, 8
+    y = rng.normal(size=(T, heads * d))
+    th = rng.uniform(-math.pi, math.pi, size=(T, d // 2))
+    cos, sin = np.repeat(np.cos(th), 2, axis=1), np.repeat(np.sin(th), 2, axis=1)
+    got = O.rope_interleaved(y, cos, sin, d).reshape(T, heads, d)
+    z = y.reshape(T, heads, d // 2, 2)
+    zc = (z[..., 0] + 1j * z[..., 1]) * np.exp(1j * th)[:, None, :]
+    _close(got[..., 0::2], zc.real, rel=1e-13, what="interleaved re")
+    _close(got[..., 1::2], zc.imag, rel=1e-13, what="interleaved im")
+
+
+def pin_permutation_layout():
+    """The permutation by hand for d = 8, and its application to labelled channels:
+    Q and K heads permuted head by head, V channels in place."""
+    assert O.interleaved_to_rotate_half(8).tolist() == [0, 2, 4, 6, 1, 3, 5, 7]
+    nq, nkv, d = 2, 1, 4
+    lab = np.arange((nq + 2 * nkv) * d)
+    got = O.permute_qk_rows(lab, nq, nkv, d).tolist()
+    assert got == [0, 2, 1, 3, 4, 6, 5, 7, 8, 10, 9, 11, 12, 13, 14, 15]
+
+
+def pin_interleaved_checkpoint_equivalence():
+    """The offline conversion the page prescribes: an interleaved-convention model
+    (weights, scales, bias, gamma, cos/sin in interleaved lane order, interleaved RoPE)
+    equals the rotate-half path run on the permuted tensors, up to the same
+    permutation of the Q/K output columns - for every norm kind."""
+    for norm in (O.NORM_ACROSS_HEADS, O.NORM_HEAD_RMS, O.NORM_HEAD_LAYER, O.NORM_NONE):
+        c, shape = (_head_case(seed=95 + norm) if norm in (O.NORM_HEAD_RMS, O.NORM_HEAD_LAYER)
+                    else _tiny_case(seed=95 + norm, T=4, H=64, nq=3, nkv=2, d=8))
+        nq, nkv, d = shape["n_q_heads"], shape["n_kv_heads"], shape["d_head"]
+        rng = np.random.default_rng(99 + norm)
+        th = rng.uniform(-math.pi, math.pi, size=(c["A"].shape[0], d // 2))
+        cos_il = np.repeat(np.cos(th), 2, axis=1).astype(np.float32)
+        sin_il = np.repeat(np.sin(th), 2, axis=1).astype(np.float32)
+        il = O.qkv_cte(c["A"], c["a_scale"], c["W"], c["w_sf"], c["bias"], c["gamma_q"], c["gamma_k"], cos_il,
+                       sin_il, norm=norm, rope=1, eps=1e-6, w_col_scale=c["w_col_scale"], rope_layout="interleaved",
+                       **shape)
+        per_head = norm in (O.NORM_HEAD_RMS, O.NORM_HEAD_LAYER)
+        pg = (lambda g, n: O.permute_qk_rows(g, 1, 0, d)) if per_head else (lambda g, n: O.permute_qk_rows(g, n, 0, d))
+        rh = O.qkv_cte(c["A"], c["a_scale"],
+                       O.permute_qk_rows(c["W"], nq, nkv, d), O.permute_qk_rows(c["w_sf"], nq, nkv, d),
+                       O.permute_qk_rows(c["bias"], nq, nkv, d), pg(c["gamma_q"], nq), pg(c["gamma_k"], nkv),
+                       O.permute_qk_rows(cos_il.T, 1, 0, d).T, O.permute_qk_rows(sin_il.T, 1, 0, d).T,
+                       norm=norm, rope=1, eps=1e-6, w_col_scale=O.permute_qk_rows(c["w_col_scale"], nq, nkv, d),
+                       **shape)
+        expect = O.permute_qk_rows(il["O"].T, nq, nkv, d).T
+        _close(rh["O"], expect, rel=1e-12, what=f"interleaved equivalence, norm {norm}")
+
+
+PINS = [pin_head_norm_vs_torch, pin_head_norm_invariants, pin_rope_interleaved_complex, pin_permutation_layout,
+        pin_interleaved_checkpoint_equivalence, pin_nbsd_layout, pin_encode_e4m3_vs_torch, pin_encode_e4m3_saturation, pin_row_quantise_invariants,
         pin_row_quantise_exact_power_of_two, pin_row_quantise_vs_torch_route, pin_packed_rows_layout, pin_e4m3_exhaustive, pin_e4m3_spec_values, pin_ue8m0_exhaustive, pin_bf16_exhaustive,
         pin_full_bruteforce, pin_separate_bruteforce, pin_hand_example, pin_norm_vs_torch_rms_norm,
         pin_rope_complex_closed_form, pin_unit_rms_invariant, pin_pair_norm_invariant,
@@ -488,7 +595,8 @@ def test_pin(pin):
 _orig = {name: getattr(O, name) for name in
          ("decode_e4m3", "decode_ue8m0", "decode_bf16", "dequant_activations", "dequant_weights",
           "project", "segments", "segment_sumsq", "inv_rms", "rotate_half", "apply_norm_rope",
-          "qkv_cte", "to_nbsd", "encode_e4m3", "row_quantise", "pack_rows", "unpack_rows")}
+          "qkv_cte", "to_nbsd", "encode_e4m3", "row_quantise", "pack_rows", "unpack_rows", "head_norm",
+          "rope_interleaved", "interleaved_to_rotate_half", "permute_qk_rows")}
 
 
 def _e4m3_bias8(codes):
@@ -676,7 +784,7 @@ def _quant_amax_whole_tensor(x_bits):
 def _quant_multiply_by_448_over_amax(x_bits):
     x = O.decode_bf16(x_bits).astype(np.float32)
     amax = np.abs(x).max(axis=1)
-    with np.errstate(divide="ignore"):
+    with np.errstate(divide="ignore", over="ignore"):
         r = np.where(amax > 0, np.float32(448.0) / amax, np.float32(1.0)).astype(np.float32)
     s = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
     with np.errstate(invalid="ignore"):
@@ -696,7 +804,50 @@ def _pack_big_endian(codes, scale):
     return np.concatenate([codes, tail], axis=1)
 
 
+def _head_norm_segment_stats(x, gamma, d, kind, eps):
+    rows, width = x.shape
+    h = x.reshape(rows, width // d, d)
+    if kind == O.NORM_HEAD_LAYER:
+        h = h - h.mean(axis=(1, 2), keepdims=True)
+    inv = 1.0 / np.sqrt(np.mean(h ** 2, axis=(1, 2), keepdims=True) + eps)
+    return (h * inv * O.decode_bf16(gamma)[None, None, :]).reshape(rows, width)
+
+
+def _head_norm_unbiased(x, gamma, d, kind, eps):
+    rows, width = x.shape
+    h = x.reshape(rows, width // d, d)
+    if kind == O.NORM_HEAD_LAYER:
+        h = h - h.mean(axis=2, keepdims=True)
+        inv = 1.0 / np.sqrt(np.sum(h ** 2, axis=2, keepdims=True) / (d - 1) + eps)
+    else:
+        inv = 1.0 / np.sqrt(np.mean(h ** 2, axis=2, keepdims=True) + eps)
+    return (h * inv * O.decode_bf16(gamma)[None, None, :]).reshape(rows, width)
+
+
+def _head_norm_layer_uncentred(x, gamma, d, kind, eps):
+    return _orig["head_norm"](x, gamma, d, O.NORM_HEAD_RMS, eps)
+
+
+def _rope_interleaved_sign(y, cos, sin, d):
+    return _orig["rope_interleaved"](y, cos, -np.asarray(sin), d)
+
+
+def _perm_odd_first(d):
+    half = d // 2
+    return np.concatenate([2 * np.arange(half) + 1, 2 * np.arange(half)])
+
+
+def _permute_v_too(x, nq, nkv, d):
+    return _orig["permute_qk_rows"](x, nq + nkv, nkv, d) if nkv else _orig["permute_qk_rows"](x, nq, nkv, d)
+
+
 MUTANTS = {
+    "head_norm_segment_stats": ("head_norm", _head_norm_segment_stats),
+    "head_norm_unbiased_var": ("head_norm", _head_norm_unbiased),
+    "head_norm_layer_uncentred": ("head_norm", _head_norm_layer_uncentred),
+    "rope_interleaved_sign": ("rope_interleaved", _rope_interleaved_sign),
+    "perm_odd_first": ("interleaved_to_rotate_half", _perm_odd_first),
+    "permute_v_too": ("permute_qk_rows", _permute_v_too),
     "encode_truncate": ("encode_e4m3", _encode_truncate),
     "encode_ties_away": ("encode_e4m3", _encode_ties_away),
     "encode_no_saturation": ("encode_e4m3", _encode_no_saturation),
