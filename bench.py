@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import dataclasses
 import json
 import os
 import statistics
@@ -54,6 +55,8 @@ def _args():
                    help="output layout: BSD [T, I] or NBSd [heads, T, d_head]")
     p.add_argument("--input", choices=["fp8", "packed", "bf16"], default="fp8",
                    help="what the step is fed: e4m3 rows + scales, packed [T, H+4] rows, or bf16 activations")
+    p.add_argument("--norm", choices=["across", "head_rms", "head_layer"], default="across",
+                   help="qk-norm: across heads (Wan), or the per-head RMS / LayerNorm finished in the GEMM epilogue")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
@@ -245,6 +248,8 @@ def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8"):
         "n_q_heads": call.n_q_heads, "n_kv_heads": call.n_kv_heads, "d_head": call.d_head,
         "tile_n": tile_n,
         "output_layout": "NBSd [heads, T, d_head]" if layout == "nbsd" else "BSD [T, I]",
+        "qk_norm": {0: "none", 1: "across heads (RMS)", 2: "per head RMS, in the GEMM epilogue",
+                    3: "per head LayerNorm, in the GEMM epilogue"}[call.norm],
         "input": _INPUT_NOTE[input_kind],
         "l2": "flushed between timed steps (256 MB write, outside the step events)" if flushed
         else "not flushed",
@@ -279,6 +284,8 @@ def run_ours(args):
         torch.cuda.synchronize(dev)
 
     call = wl.workload(args.workload)[0]
+    if args.norm != "across":
+        call = dataclasses.replace(call, norm={"head_rms": 2, "head_layer": 3}[args.norm])
     inp = wl.make_inputs(call)
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     gemm_flag = {"auto": 0, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA}[args.gemm]
@@ -450,7 +457,10 @@ def run_ours(args):
                                      f"{FP8_PER_BF16:g}")},
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": (3 if args.input == "fp8" else 4) * args.steps,
+        # prep + GEMM, the producer for a bf16 / packed input, the norm/RoPE pass unless the
+        # norm is per head (finished in the GEMM epilogue)
+        "gpu_launches": (2 + (args.input != "fp8") + (call.norm == 1 or (call.norm == 0 and call.rope == 1)))
+        * args.steps,
         "producer": producer,
         "cpu_baseline": cpu,
     }

@@ -66,6 +66,20 @@ extern "C" {
 #define QKV_CTE_ERR_DEVICE_TIMEOUT (-5) /* a bounded device wait ran out (see qkv_cte_status) */
 
 enum { QKV_CTE_MODE_FUSED = 0, QKV_CTE_MODE_SEPARATE = 1 };
+
+/* qk-norm of Q and K (desc.norm):
+ *   NONE         : no norm;
+ *   ACROSS_HEADS : one RMS per token over the whole Q (or K) segment, gamma [n_heads*d_head]
+ *                  per segment ([qkv_cte] "Design" 1; Wan's RMS_NORM_ACROSS_HEADS);
+ *   HEAD_RMS     : per head, x / sqrt(mean(x^2) + eps) * gamma, gamma [d_head] shared by the
+ *                  segment's heads;
+ *   HEAD_LAYER   : per head, (x - mean) / sqrt(mean((x - mean)^2) + eps) * gamma, gamma
+ *                  [d_head], no bias ([qkv_cte] "Upstream behavior": the per-head RMS_NORM /
+ *                  LAYER_NORM fused into the matmul's copy-out).
+ * The per-head kinds finish in the GEMM's epilogue (every N tile holds whole heads: the
+ * automatic tile_n is one d_head divides) and run no second pass; RoPE is applied after
+ * the norm in every kind. */
+enum { QKV_CTE_NORM_NONE = 0, QKV_CTE_NORM_ACROSS_HEADS = 1, QKV_CTE_NORM_HEAD_RMS = 2, QKV_CTE_NORM_HEAD_LAYER = 3 };
 enum { QKV_CTE_LAYOUT_BSD = 0, QKV_CTE_LAYOUT_NBSD = 1 };
 
 /* What `A` of qkv_cte_run holds ([qkv_cte] "Interface" table, packed_hidden row, and
@@ -103,7 +117,7 @@ typedef struct {
     int32_t n_kv_heads;    /* K/V heads; 0 for a single-segment (separate) call */
     int32_t d_head;        /* head dim; multiple of 16 */
     int32_t mode;          /* QKV_CTE_MODE_FUSED (n_kv >= 1) or QKV_CTE_MODE_SEPARATE (n_kv == 0) */
-    int32_t norm;          /* 1: across-heads RMSNorm on Q (and K); 0: none */
+    int32_t norm;          /* QKV_CTE_NORM_*: 0 none, 1 across heads, 2 per-head RMS, 3 per-head LayerNorm */
     int32_t rope;          /* 1: rotate-half RoPE on Q (and K); needs cos/sin */
     int32_t output_layout; /* QKV_CTE_LAYOUT_BSD: O[T, I]; QKV_CTE_LAYOUT_NBSD: O[I/d_head, T, d_head]
                               (heads in column order: Q heads, then K, then V) */
@@ -131,7 +145,8 @@ typedef struct {
  * workspace_bytes: receives the device workspace size qkv_cte_run needs.
  * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values,
  * unknown input layout) or
- * -2 (H % 128, d_head % 16, T > INT32_MAX, unknown tile_n). */
+ * -2 (H % 128, d_head % 16, T > INT32_MAX, unknown tile_n, a per-head norm with a tile_n that
+ * d_head does not divide). */
 int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes);
 
 /* Fill `info` for `plan`. Returns 0 or -1 (null pointer). */
@@ -147,15 +162,18 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info);
  * w_sf       : uint8  [I, H/32]   UE8M0 block scales, row-major; 4-byte aligned
  * w_col_scale: fp32   [I] or NULL per-output-channel multiplier ("weight_scales"); 16-byte aligned
  * bias       : bf16   [I] or NULL; 16-byte aligned
- * gamma_q    : bf16   [n_q*d_head] segment-wide Q gamma; required iff norm; 16-byte aligned
- * gamma_k    : bf16   [n_kv*d_head] K gamma; required iff norm and n_kv > 0, else NULL
+ * gamma_q    : bf16   Q gamma, required iff norm != NONE: [n_q*d_head] (across heads) or [d_head]
+ *              (per head); 16-byte aligned
+ * gamma_k    : bf16   K gamma, [n_kv*d_head] or [d_head]; required iff norm != NONE and n_kv > 0,
+ *              else NULL
  * cos_table, sin_table: fp32 [T, d_head] rotate-half tables; required iff rope, else NULL;
  *              32-byte aligned
  * O          : bf16 output, [T, I] (BSD) or [I/d_head, T, d_head] (NBSd: element (h, t, j)
  *              is column h*d_head + j of token t); 32-byte aligned; must not alias any input
  * sumsq      : fp32   [T, 2] or NULL: per-token sum of o^2 over the un-normalised Q and K
  *              segments ([qkv_cte] "Design" 1 step a; column 1 is 0 when n_kv == 0)
- * inv_rms    : fp32   [T, 2] or NULL: the rsqrt factors of step b (written iff norm)
+ * inv_rms    : fp32   [T, 2] or NULL: the rsqrt factors of step b (written iff norm is
+ *              ACROSS_HEADS; must be NULL with a per-head norm)
  * workspace  : device scratch of at least the planned size; 256-byte aligned
  * With tokens == 0 every tensor pointer may be NULL: no kernel is launched and only
  * the workspace's status word is reset (when a workspace is given).
@@ -214,6 +232,24 @@ int qkv_cte_row_quantize(const uint16_t* X, int64_t tokens, int32_t hidden, uint
  * Returns 0, -1, -2, -3 or -4 as qkv_cte_row_quantize (tokens == 0 likewise). */
 int qkv_cte_unpack_rows(const uint8_t* packed, int64_t tokens, int32_t hidden, uint8_t* A, float* a_scale,
                         void* stream);
+
+/* Offline conversion of an interleaved-RoPE checkpoint (lanes 2j, 2j+1 of a head form
+ * pair j, as in Wan's checkpoint) to the rotate-half lane order qkv_cte_run applies
+ * ([qkv_cte] "Design" 2: the caller permutes the Q/K weights, bias, gamma and cos/sin
+ * caches once). Copies `rows` rows of `row_bytes` bytes from src to dst; within each of
+ * the first (n_q_heads + n_kv_heads) heads of d_head rows, row i of the head takes
+ * row perm[i] with perm[j] = 2j, perm[d/2 + j] = 2j + 1; the remaining rows (V) are
+ * copied as they are. Byte-exact. Apply it to every per-output-channel tensor:
+ *   W codes  [I, H]     : rows = I, row_bytes = H
+ *   w_sf     [I, H/32]  : rows = I, row_bytes = H/32
+ *   bias, w_col_scale   : rows = I, row_bytes = 2 / 4
+ *   gamma               : across heads: rows = n*d, heads (n, 0); per head: rows = d, heads (1, 0)
+ *   cos/sin [T, d] fp32 : rows = T*d, row_bytes = 4, heads (T, 0) (each table row is one "head")
+ * src, dst: device buffers of rows*row_bytes bytes that do not overlap (not in place).
+ * Stream-ordered and asynchronous. Returns 0, -1 (bad counts, d_head odd, Q/K rows
+ * beyond `rows`, null or overlapping buffers), -2, -3 or -4. rows == 0 launches nothing. */
+int qkv_cte_interleaved_to_rotate_half(const void* src, void* dst, int64_t rows, int64_t row_bytes,
+                                       int32_t n_q_heads, int32_t n_kv_heads, int32_t d_head, void* stream);
 
 /* Size of the scratch array behind qkv_cte_run_noalloc: 16 MiB on every GPU that
  * loads the library, held until the process exits. */

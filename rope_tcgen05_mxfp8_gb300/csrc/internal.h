@@ -123,6 +123,15 @@ struct GemmArgs {
   int d_head;
   int nbsd;                  // O layout: 0 = BSD [T, I]; 1 = NBSd [I/d_head, T, d_head]
   uint32_t flags;
+  // Per-head qk-norm finished in the epilogue (every tile holds whole heads):
+  // 0 = off (Q/K go to the hand-off, or to O as projected), 2 = RMS, 3 = LayerNorm.
+  int head_norm;
+  int rope;                  // rotate-half RoPE in the epilogue (head_norm != 0 only)
+  float eps;
+  const uint16_t* gamma_q;   // [d_head] bf16 (head_norm != 0)
+  const uint16_t* gamma_k;   // [d_head] bf16, or null without a K segment
+  const float* cos_t;        // [T, d_head] fp32 (rope)
+  const float* sin_t;
 };
 
 // Element (row t, column c) of O in either layout (c and the 16 columns after it
@@ -170,12 +179,20 @@ cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtens
                         const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms);
 // Launched right after K1 on the same stream as a programmatic dependent launch, so
 // its blocks start while K1 runs and take each row panel as soon as K1 marks it ready.
+// K1 with the per-head qk-norm epilogue (qkv_gemm_mxf8_head.cu); launch_gemm calls it
+// when a.head_norm != 0.
+cudaError_t launch_gemm_head(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                             const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms);
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap);
 
 // The producer step (row_quant.cu): bf16 [T, H] -> e4m3 codes [T, H] + fp32 scales [T]
 // and/or packed [T, H + 4] rows (either output may be null, not both); H % 16 == 0.
 cudaError_t launch_row_quantize(const uint16_t* X, int T, int H, uint8_t* codes, float* scale, uint8_t* packed,
                                 cudaStream_t s, int num_sms);
+// Interleaved -> rotate-half lane order of the first qk_rows rows (whole heads of
+// d_head rows), the rest copied (rope_permute.cu); src and dst do not overlap.
+cudaError_t launch_permute_rows(const void* src, void* dst, long long rows, long long row_bytes, long long qk_rows,
+                                int d_head, cudaStream_t s, int num_sms);
 // Packed [T, H + 4] -> codes [T, H] + scales [T]; H % 16 == 0.
 cudaError_t launch_unpack_rows(const uint8_t* packed, int T, int H, uint8_t* codes, float* scale, cudaStream_t s,
                                int num_sms);

@@ -27,6 +27,7 @@ struct qkv_cte_plan_s {
   int ev_device = -1;
   bool ran = false;
   bool has_norm_pass = false;
+  bool second_pass = false;  // the norm/RoPE kernel runs (across-heads norm, or RoPE alone)
   const void* last_workspace = nullptr;
 };
 
@@ -137,9 +138,20 @@ int band_tiles(const GemmShape& g) {
   return n < 1 ? 1 : n;
 }
 
+bool per_head_norm(const qkv_cte_desc& d) {
+  return d.norm == QKV_CTE_NORM_HEAD_RMS || d.norm == QKV_CTE_NORM_HEAD_LAYER;
+}
+
 int choose_tile_n(const qkv_cte_desc& d, int I) {
   if (d.tile_n != 0) return d.tile_n;
   (void)I;
+  if (per_head_norm(d)) {
+    // The per-head epilogue needs whole heads in every tile: the widest built tile
+    // with two TMEM accumulator stages that d_head divides, else 256 (one stage).
+    for (int t : {240, 192, 128})
+      if (t % d.d_head == 0) return t;
+    return 256;
+  }
   return 240;  // two TMEM accumulator stages: the epilogue overlaps the next tile's MMAs
 }
 
@@ -171,7 +183,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   } else {
     return fail(QKV_CTE_ERR_INVALID, "unknown mode %d", d.mode);
   }
-  if (d.norm != 0 && d.norm != 1) return fail(QKV_CTE_ERR_INVALID, "norm must be 0 or 1");
+  if (d.norm < QKV_CTE_NORM_NONE || d.norm > QKV_CTE_NORM_HEAD_LAYER)
+    return fail(QKV_CTE_ERR_INVALID, "unknown norm %d", d.norm);
   if (d.rope != 0 && d.rope != 1) return fail(QKV_CTE_ERR_INVALID, "rope must be 0 or 1");
   if (!(d.eps >= 0.0f) || d.eps > 1e30f) return fail(QKV_CTE_ERR_INVALID, "eps must be finite and >= 0");
   if (d.output_layout != QKV_CTE_LAYOUT_BSD && d.output_layout != QKV_CTE_LAYOUT_NBSD)
@@ -188,6 +201,9 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   if (I > INT32_MAX / 2) return fail(QKV_CTE_ERR_UNSUPPORTED, "output width too large");
   const int tile_n = choose_tile_n(d, (int)I);
   if (!gemm_tile_supported(tile_n)) return fail(QKV_CTE_ERR_UNSUPPORTED, "tile_n %d not built", tile_n);
+  if (per_head_norm(d) && tile_n % d.d_head != 0)
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "per-head norm needs whole heads per tile: tile_n %d, d_head %d", tile_n,
+                d.d_head);
 
   qkv_cte_plan_s* p = new (std::nothrow) qkv_cte_plan_s();
   if (p == nullptr) return fail(QKV_CTE_ERR_INVALID, "out of host memory");
@@ -222,7 +238,10 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   w.sf_off = w.sumsq_off + align_up((size_t)g.T * 2 * sizeof(float), 256);
   w.ready_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
   w.qk_off = w.ready_off + align_up((size_t)g.blocks128 * sizeof(uint32_t), 256);
-  const bool second_pass = d.norm || d.rope;
+  // The norm/RoPE pass (and its hand-off) runs for the across-heads norm, or RoPE
+  // without a norm; the per-head norms finish in the GEMM's epilogue.
+  const bool second_pass = !per_head_norm(d) && (d.norm == QKV_CTE_NORM_ACROSS_HEADS || d.rope);
+  p->second_pass = second_pass;
   const size_t hand_rows = second_pass ? (size_t)g.blocks128 * 128 : 0;
   w.qk_exp_off = w.qk_off + align_up(hand_rows * p->k_end * sizeof(uint16_t), 256);
   w.act_off = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
@@ -296,6 +315,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (gamma_k && !(d.norm && d.n_kv_heads > 0))
     return fail(QKV_CTE_ERR_INVALID, "gamma_k given but the call has no normalised K segment");
   if (gamma_q && !d.norm) return fail(QKV_CTE_ERR_INVALID, "gamma_q given but norm is off");
+  if (inv_rms && per_head_norm(d))
+    return fail(QKV_CTE_ERR_INVALID, "inv_rms is an output of the across-heads norm only (per-head norm: NULL)");
   if (d.rope && (!cos_table || !sin_table)) return fail(QKV_CTE_ERR_INVALID, "rope needs cos and sin tables");
   if (!d.rope && (cos_table || sin_table)) return fail(QKV_CTE_ERR_INVALID, "cos/sin given but rope is off");
   if (!aligned(A, d.input_layout == QKV_CTE_INPUT_PACKED ? 4 : 16) || !aligned(W, 16) || !aligned(O, 32))
@@ -370,8 +391,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.bias = bias;
   ga.sf_packed = sf_packed;
   ga.O = O;
-  uint16_t* qk_val = (d.norm || d.rope) ? reinterpret_cast<uint16_t*>(ws + plan->ws.qk_off) : nullptr;
-  uint8_t* qk_exp = (d.norm || d.rope) ? ws + plan->ws.qk_exp_off : nullptr;
+  uint16_t* qk_val = plan->second_pass ? reinterpret_cast<uint16_t*>(ws + plan->ws.qk_off) : nullptr;
+  uint8_t* qk_exp = plan->second_pass ? ws + plan->ws.qk_exp_off : nullptr;
   ga.qk_val = qk_val;
   ga.qk_exp = qk_exp;
   ga.sumsq = need_ss ? ss : nullptr;
@@ -383,6 +404,13 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.flags = d.flags;
   ga.d_head = d.d_head;
   ga.nbsd = d.output_layout == QKV_CTE_LAYOUT_NBSD ? 1 : 0;
+  ga.head_norm = per_head_norm(d) ? d.norm : 0;
+  ga.rope = per_head_norm(d) ? d.rope : 0;
+  ga.eps = d.eps;
+  ga.gamma_q = gamma_q;
+  ga.gamma_k = gamma_k;
+  ga.cos_t = cos_table;
+  ga.sin_t = sin_table;
   CUtensorMap tmSF;
   if ((rc = encode_scales(&tmSF, sf_packed, g)) != QKV_CTE_OK) return rc;
   e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms);
@@ -411,12 +439,14 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.ready_target = 4u * (uint32_t)g.n_qk_tiles;
   na.status = status;
   na.stamps = stamps + 2;
-  e = launch_norm_rope(na, s, dev.sms, (d.flags & QKV_CTE_FLAG_SERIAL_PASSES) == 0);
-  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "norm/rope launch: %s", cudaGetErrorString(e));
+  if (plan->second_pass) {
+    e = launch_norm_rope(na, s, dev.sms, (d.flags & QKV_CTE_FLAG_SERIAL_PASSES) == 0);
+    if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "norm/rope launch: %s", cudaGetErrorString(e));
+  }
   if (prof) {
     cudaEventRecord(plan->ev[2], s);
     plan->ran = true;
-    plan->has_norm_pass = d.norm || d.rope;
+    plan->has_norm_pass = plan->second_pass;
     plan->last_workspace = workspace;
   }
   return ok();
@@ -521,6 +551,29 @@ int qkv_cte_unpack_rows(const uint8_t* packed, int64_t tokens, int32_t hidden, u
   cudaError_t e = launch_unpack_rows(packed, (int)tokens, hidden, A, a_scale, static_cast<cudaStream_t>(stream),
                                      dev.sms);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "unpack launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int qkv_cte_interleaved_to_rotate_half(const void* src, void* dst, int64_t rows, int64_t row_bytes,
+                                       int32_t n_q_heads, int32_t n_kv_heads, int32_t d_head, void* stream) {
+  const char* who = "qkv_cte_interleaved_to_rotate_half";
+  if (rows < 0 || row_bytes <= 0) return fail(QKV_CTE_ERR_INVALID, "%s: rows must be >= 0, row_bytes > 0", who);
+  if (d_head <= 0 || d_head % 2 != 0) return fail(QKV_CTE_ERR_INVALID, "%s: d_head must be even and > 0", who);
+  if (n_q_heads < 0 || n_kv_heads < 0) return fail(QKV_CTE_ERR_INVALID, "%s: negative head count", who);
+  const long long qk_rows = (long long)(n_q_heads + (long long)n_kv_heads) * d_head;
+  if (qk_rows > rows) return fail(QKV_CTE_ERR_INVALID, "%s: %lld Q/K rows exceed the %lld rows given", who,
+                                  qk_rows, (long long)rows);
+  if (rows > 0 && row_bytes > INT64_MAX / rows) return fail(QKV_CTE_ERR_UNSUPPORTED, "%s: size overflow", who);
+  if (rows == 0) return ok();
+  if (src == nullptr || dst == nullptr) return fail(QKV_CTE_ERR_INVALID, "%s: null buffer", who);
+  if (overlaps(src, (size_t)(rows * row_bytes), dst, (size_t)(rows * row_bytes)))
+    return fail(QKV_CTE_ERR_INVALID, "%s: src and dst overlap (the permutation is not in place)", who);
+  DeviceInfo dev;
+  int rc = check_device(&dev);
+  if (rc != QKV_CTE_OK) return rc;
+  cudaError_t e = launch_permute_rows(src, dst, rows, row_bytes, qk_rows, d_head, static_cast<cudaStream_t>(stream),
+                                      dev.sms);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "permute launch: %s", cudaGetErrorString(e));
   return ok();
 }
 

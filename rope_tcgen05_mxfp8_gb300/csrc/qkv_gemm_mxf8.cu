@@ -1,677 +1,11 @@
-// Kernel K1: O = dequant(A_fp8 @ W_fp8^T) * a_scale[t] * w_col_scale[i] + bias[i] -> bf16,
-// plus the per-token sum of o^2 over the Q and the K columns.
-//
-// Follows the `qkv_cte` kernel reference page: the projection O[S, I] = A[S, H] @ W[H, I]
-// (+ bias) ("Upstream behavior"), dequantised, bias-added and stored as each output
-// tile leaves the accumulator, with the across-heads norm's step a (a per-token
-// sum(x^2) over the whole Q segment and K segment of the un-normalised output,
-// "Design" 1) folded into that same copy-out.
-//
-// GB300 design (not the page's Trainium schedule):
-//   * persistent grid, one CTA per SM, tiles of 128 rows x tile_n columns, walked in
-//     bands of N tiles (V-only tiles first), row-panel-major inside a band, so the
-//     band's slab of W stays resident in L2 while A streams;
-//   * warp 0: TMA producer. Per K stage it loads a 128x128-byte A tile and a
-//     tile_n x 128-byte W tile (128-byte swizzle) plus the stage's repacked UE8M0
-//     block scales, all counted on one mbarrier;
-//   * warp 1: one thread issues tcgen05.cp for the block scales and four
-//     tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each, one UE8M0 scale per row of
-//     B per MMA, selected by the scale-factor byte id) into a TMEM fp32 accumulator;
-//   * warps 2-5: epilogue. tcgen05.ld the accumulator (one TMEM lane = one row per
-//     thread), apply the row scale / column scale / bias, accumulate the Q and K sums
-//     of squares in fp32 and add them to sumsq[T, 2] with one atomic per row and
-//     segment. V columns are stored as final bf16. Q and K columns go to a
-//     tile-major workspace hand-off when the norm/RoPE pass follows, in block
-//     floating point (fp16 with a power-of-two exponent per row and 16 columns: 11
-//     significant bits, any range), so the bf16 rounding happens once, at the end,
-//     and the stores coalesce whatever row a thread owns; else as bf16. With two accumulator stages
-//     the epilogue of tile j overlaps the MMAs of tile j+1. After each tile every
-//     epilogue warp fences its stores and bumps its row panel's ready counter; the
-//     norm/RoPE pass, launched as a programmatic dependent of this grid, starts on a
-//     panel once all its tiles are in.
-//   * A carries no MX scale of its own (its only scale is the fp32 row scale), so the
-//     A-side scale factors are the constant 2^0 (UE8M0 127), copied to TMEM once.
-// Every mbarrier wait is bounded; a wait that runs out records its role in the
-// status word and the CTA unwinds, waiting for its own copies and MMAs before it
-// releases TMEM.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "internal.h"
-#include "ptx.cuh"
+// Kernel K1 with the plain epilogue (Q/K to the norm/RoPE hand-off or as projected),
+// the scale repack / clear kernel, and the GEMM dispatch. The kernel templates and
+// their design notes are in qkv_gemm_mxf8.cuh.
+#include "qkv_gemm_mxf8.cuh"
 
 namespace qkvcte {
 
 namespace {
-
-constexpr int kBM = 128;       // rows per tile (the MMA's M)
-constexpr int kBK = 128;       // K elements (bytes of e4m3) per pipeline stage
-constexpr int kThreads = 192;  // producer warp, MMA warp, 4 epilogue warps
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr uint32_t kFlagTestStall = 0x1u;
-
-template <int BN>
-struct K1Cfg {
-  static constexpr int SF_CHUNKS = (BN + 127) / 128;
-  static constexpr int A_BYTES = kBM * kBK;
-  static constexpr int B_BYTES = BN * kBK;
-  static constexpr int SFB_BYTES = SF_CHUNKS * 512;
-  static constexpr int SFB_COLS = SF_CHUNKS * 4;
-  static constexpr int ACC_STAGES = (2 * BN + 4 + SFB_COLS <= 512) ? 2 : 1;
-  static constexpr int SFA_COL = ACC_STAGES * BN;
-  static constexpr int SFB_COL = SFA_COL + 4;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFB_BYTES;
-  static constexpr int SMEM_LIMIT = 232448;          // 227 KB opt-in per block
-  static constexpr int FIXED = 1024 + 512 + 256;      // alignment slack, A scales, barriers
-  static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr size_t SMEM = FIXED + static_cast<size_t>(STAGES) * STAGE_BYTES;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M=128 is a multiple of 16 up to 256");
-  static_assert(SFB_COL + SFB_COLS <= 512, "TMEM columns");
-  static_assert(STAGES >= 2, "pipeline depth");
-  static_assert(B_BYTES % 1024 == 0, "swizzle atoms");
-};
-
-__device__ __forceinline__ void record_failure(uint32_t* status, volatile int* abort_flag, uint32_t code) {
-  atomicOr(status, code);
-  *abort_flag = 1;
-}
-
-__device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
-  return __uint_as_float(bits16 << 16);
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// ---------------------------------------------------------------------------
-// Epilogue, shared by the single-CTA and CTA-pair kernels.
-//
-// One warp drains 32 rows (its TMEM lane quarter, one row per thread) of one
-// accumulator tile. Per 16 columns: o = acc * (a_scale * w_col_scale) + bias, the
-// Q/K sum of squares (a 16-column chunk never straddles a segment boundary: both
-// are multiples of 16), then one 32-byte store. Q/K chunks go to the hand-off in
-// block floating point (16 fp16 scaled by the chunk's power-of-two exponent,
-// tile-major, so the warp's store writes 1 KB of consecutive memory); V goes to O
-// as final bf16 (one full 32-byte sector per row), BSD or NBSd.
-// ---------------------------------------------------------------------------
-template <int BN>
-__device__ __forceinline__ void epilogue_drain(const GemmShape& g, const GemmArgs& a, uint32_t t_acc, int block128,
-                                               int row_in_block, int col_base, uint64_t pol_out, float& ss_q,
-                                               float& ss_k) {
-  const int row = block128 * 128 + row_in_block;
-  const bool row_ok = row < g.T;
-  const float ascale = row_ok ? a.a_scale[row] : 0.0f;
-  const int qk_chunks = a.k_end >> 4;
-  const size_t qk_row_idx = static_cast<size_t>(block128) * qk_chunks * 128 + row_in_block;
-  ss_q = 0.0f;
-  ss_k = 0.0f;
-#pragma unroll
-  for (int c0 = 0; c0 < BN; c0 += 32) {
-    uint32_t r[32];
-    const uint32_t taddr = t_acc + static_cast<uint32_t>(c0);
-    if (c0 + 32 <= BN)
-      tmem_ld_32x32b_x32(taddr, r);
-    else
-      tmem_ld_32x32b_x16(taddr, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (c0 + 16 * h >= BN) break;
-      const int col0 = col_base + c0 + 16 * h;
-      if (col0 >= g.I) break;  // ragged last N tile (uniform across the warp)
-      float sc[16];
-      if (a.w_col_scale != nullptr) {
-        const float4* p = reinterpret_cast<const float4*>(a.w_col_scale + col0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 v4 = __ldg(p + q);
-          sc[4 * q + 0] = ascale * v4.x;
-          sc[4 * q + 1] = ascale * v4.y;
-          sc[4 * q + 2] = ascale * v4.z;
-          sc[4 * q + 3] = ascale * v4.w;
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sc[j] = ascale;
-      }
-      float bias[16];
-      if (a.bias != nullptr) {
-        const uint4* p = reinterpret_cast<const uint4*>(a.bias + col0);
-        const uint4 b0 = __ldg(p), b1 = __ldg(p + 1);
-        const uint32_t w[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          bias[2 * j] = bf16_bits_to_float(w[j] & 0xFFFFu);
-          bias[2 * j + 1] = bf16_bits_to_float(w[j] >> 16);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) bias[j] = 0.0f;
-      }
-      float v[16];
-      float sq = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        v[j] = fmaf(__uint_as_float(r[16 * h + j]), sc[j], bias[j]);
-        sq = fmaf(v[j], v[j], sq);
-      }
-      if (col0 < a.q_end) ss_q += sq; else if (col0 < a.k_end) ss_k += sq;
-      if (a.qk_val != nullptr && col0 < a.k_end) {
-        // Q/K columns that the norm/RoPE pass will finish: the chunk's exponent
-        // E = floor(log2 max|v|) (clamped; 0 for zero or non-finite maxima) and
-        // v * 2^-E in fp16, so every value keeps 11 significant bits relative to
-        // the chunk maximum whatever its range.
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
-        const int field = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu);
-        int e = (field == 0 || field == 255) ? 0 : field - 127;
-        e = e < -126 ? -126 : (e > 126 ? 126 : e);
-        const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-        uint32_t hv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) hv[j] = pack_f16x2(v[2 * j] * down, v[2 * j + 1] * down);
-        const size_t idx = qk_row_idx + static_cast<size_t>(col0 >> 4) * 128;
-        st_global_v8_b32(a.qk_val + idx * 16, hv);
-        a.qk_exp[idx] = static_cast<uint8_t>(e + 127);
-      } else if (row_ok) {
-        uint32_t packed[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) packed[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
-        // final values nothing here reads again: first out of L2
-        st_global_v8_b32_hint(a.O + out_index(a.nbsd, g.T, g.I, a.d_head, row, col0), packed, pol_out);
-      }
-    }
-  }
-}
-
-// After the accumulator is released: add this warp's rows' sums of squares and, for
-// a tile holding Q/K columns, publish its 32 rows on the 128-row block's counter
-// once its stores and sums are visible.
-template <int BN>
-__device__ __forceinline__ void epilogue_publish(const GemmShape& g, const GemmArgs& a, int block128,
-                                                 int row_in_block, int col_base, bool qk_tile, float ss_q,
-                                                 float ss_k, int lane) {
-  const int row = block128 * 128 + row_in_block;
-  if (row < g.T && a.sumsq != nullptr) {
-    if (col_base < a.q_end) atomicAdd(&a.sumsq[2 * static_cast<size_t>(row)], ss_q);
-    if (col_base + BN > a.q_end && col_base < a.k_end) atomicAdd(&a.sumsq[2 * static_cast<size_t>(row) + 1], ss_k);
-  }
-  if (qk_tile) {
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) atomicAdd(a.ready + block128, 1u);
-  }
-}
-
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    qkv_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                         const GemmShape g, const GemmArgs a) {
-  using C = K1Cfg<BN>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + C::STAGES * C::A_BYTES;
-  uint8_t* sSFB = sB + C::STAGES * C::B_BYTES;
-  uint8_t* sSFA = sSFB + C::STAGES * C::SFB_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFA + 512);
-  uint64_t* empty = full + C::STAGES;
-  uint64_t* tfull = empty + C::STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&tfull[s]), 1);
-      mbar_init(smem_u32(&tempty[s]), 4);
-    }
-    mbar_init(smem_u32(drain), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmW);
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  if (warp >= 2) {
-    // A-side block scales: UE8M0 127 (= 1.0) for every row and K block.
-    reinterpret_cast<uint32_t*>(sSFA)[threadIdx.x - 64] = 0x7F7F7F7Fu;
-    fence_proxy_async_smem();
-  }
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // Every CTA of this persistent grid is resident: let the norm/RoPE pass launch now.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) atomicMin(&a.stamps[0], globaltimer_ns());
-
-  const int num_tiles = g.m_tiles * g.n_tiles;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      const uint64_t pol_stream = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      bool ok = (a.flags & kFlagTestStall) == 0;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        int m_blk, n_blk;
-        tile_coords(g, tile, m_blk, n_blk);
-        for (int kb = 0; kb < g.k_stages; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
-            record_failure(a.status, abort_flag, kErrProducerEmptyWait);
-            ok = false;
-            break;
-          }
-          const uint32_t fb = smem_u32(&full[stage]);
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-          tma_load_2d(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * kBK, m_blk * kBM, fb, pol_stream);
-          tma_load_2d(smem_u32(sB + stage * C::B_BYTES), &tmW, kb * kBK, n_blk * BN, fb, pol_keep);
-          bulk_load(smem_u32(sSFB + stage * C::SFB_BYTES),
-                    a.sf_packed + (static_cast<size_t>(n_blk) * g.k_stages + kb) * C::SFB_BYTES,
-                    C::SFB_BYTES, fb);
-          ++issued;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // Do not leave while our own copies may still be landing in shared memory:
-      // wait for the (at most STAGES) most recent loads.
-      const int pending = issued < C::STAGES ? issued : C::STAGES;
-      int s = stage;
-      uint32_t ph = phase;
-      for (int i = 0; i < pending; ++i) {
-        if (s == 0) {
-          s = C::STAGES - 1;
-          ph ^= 1u;
-        } else {
-          --s;
-        }
-        if (!mbar_wait_bounded(smem_u32(&full[s]), ph, nullptr, kWaitLimitNs)) {
-          record_failure(a.status, abort_flag, kErrDrainWait);
-          break;
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer ----------------
-      const uint32_t idesc = idesc_mxf8_e4m3(kBM, BN);
-      const uint32_t sfa_t = tmem_base + C::SFA_COL;
-      const uint32_t sfb_t = tmem_base + C::SFB_COL;
-      tc_copy_32x128b_x4(sfa_t, smem_desc_plain(smem_u32(sSFA)));
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
-          record_failure(a.status, abort_flag, kErrMmaTmemEmptyWait);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < g.k_stages; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
-            record_failure(a.status, abort_flag, kErrMmaFullWait);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sf_smem = smem_u32(sSFB + stage * C::SFB_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::SF_CHUNKS; ++c)
-            tc_copy_32x128b_x4(sfb_t + 4 * c, smem_desc_plain(sf_smem + 512 * c));
-          const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
-          const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
-#pragma unroll
-          for (int k = 0; k < kBK / 32; ++k) {
-            // +32 bytes along K inside the swizzle atom = +2 in the 16-byte address field
-            mma_mxf8(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t,
-                     (kb | k) != 0 ? 1u : 0u);
-          }
-          tc_commit(smem_u32(&empty[stage]));
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit(smem_u32(&tfull[acc]));
-        if (++acc == C::ACC_STAGES) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-      }
-      // Every tcgen05 operation issued above completes before TMEM is released.
-      tc_commit(smem_u32(drain));
-      if (!mbar_wait_bounded(smem_u32(drain), 0, nullptr, kWaitLimitNs))
-        record_failure(a.status, abort_flag, kErrDrainWait);
-    }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const uint64_t pol_out = policy_evict_first();
-    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-    const int row_in_block = quarter * 32 + lane;
-    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      int m_blk, n_blk;
-      tile_coords(g, tile, m_blk, n_blk);
-      bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) record_failure(a.status, abort_flag, kErrEpilogueTmemFullWait);
-        break;
-      }
-      tc_fence_after();
-      float ss_q, ss_k;
-      epilogue_drain<BN>(g, a, t_lane + static_cast<uint32_t>(acc * BN), m_blk, row_in_block, n_blk * BN, pol_out,
-                         ss_q, ss_k);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
-      epilogue_publish<BN>(g, a, m_blk, row_in_block, n_blk * BN, n_blk < g.n_qk_tiles, ss_q, ss_k, lane);
-      if (++acc == C::ACC_STAGES) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-    __syncwarp();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, C::TMEM_COLS);
-  }
-  if (threadIdx.x == 0) atomicMax(&a.stamps[1], globaltimer_ns());
-}
-
-// ---------------------------------------------------------------------------
-// CTA-pair variant: tiles of 256 rows x BN columns computed by a cluster of two CTAs
-// with M = 256 MMAs (tcgen05 cta_group::2). Each CTA loads its 128 rows of A, its
-// half of the W tile (BN/2 rows) and the scales of all BN columns; all loads count on
-// the leader's (rank 0) barrier. The leader's MMA thread copies the scales into both
-// CTAs' TMEM and issues the MMAs for both; commits arrive on both CTAs' barriers.
-// Each CTA's epilogue drains its own TMEM rows and releases the accumulator on the
-// leader's barrier. Per SM this halves the W bytes staged and read from shared
-// memory and the scale-factor copies per FLOP.
-// ---------------------------------------------------------------------------
-template <int BN>
-struct K1PairCfg {
-  static constexpr int HALF_N = BN / 2;
-  static constexpr int SF_CHUNKS = (BN + 127) / 128;
-  static constexpr int A_BYTES = kBM * kBK;
-  static constexpr int B_BYTES = HALF_N * kBK;
-  static constexpr int SFB_BYTES = SF_CHUNKS * 512;
-  static constexpr int SFB_COLS = SF_CHUNKS * 4;
-  static constexpr int ACC_STAGES = (2 * BN + 4 + SFB_COLS <= 512) ? 2 : 1;
-  static constexpr int SFA_COL = ACC_STAGES * BN;
-  static constexpr int SFB_COL = SFA_COL + 4;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFB_BYTES;
-  static constexpr int SMEM_LIMIT = 232448;
-  static constexpr int FIXED = 1024 + 512 + 256;
-  static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr size_t SMEM = FIXED + static_cast<size_t>(STAGES) * STAGE_BYTES;
-  static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "pair MMA N");
-  static_assert(HALF_N % 8 == 0, "W half tile in whole 8-row swizzle atoms");
-  static_assert(SFB_COL + SFB_COLS <= 512, "TMEM columns");
-  static_assert(STAGES >= 2, "pipeline depth");
-};
-
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
-    qkv_gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                              const __grid_constant__ CUtensorMap tmSF, const GemmShape g, const GemmArgs a) {
-  using C = K1PairCfg<BN>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + C::STAGES * C::A_BYTES;
-  uint8_t* sSFB = sB + C::STAGES * C::B_BYTES;
-  uint8_t* sSFA = sSFB + C::STAGES * C::SFB_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sSFA + 512);  // used in the leader
-  uint64_t* empty = full + C::STAGES;                         // both
-  uint64_t* tfull = empty + C::STAGES;                        // both
-  uint64_t* tempty = tfull + 2;                               // leader: 4 warps x 2 CTAs
-  uint64_t* drain = tempty + 2;                               // leader
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
-  const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1;
-  const int n_pairs = gridDim.x >> 1;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&tfull[s]), 1);
-      mbar_init(smem_u32(&tempty[s]), 8);
-    }
-    mbar_init(smem_u32(drain), 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-    prefetch_tmap(&tmA);
-    prefetch_tmap(&tmW);
-    prefetch_tmap(&tmSF);
-  }
-  if (warp == 1) {
-    tmem_alloc_pair(smem_u32(tmem_slot), C::TMEM_COLS);
-    tmem_relinquish_pair();
-  }
-  if (warp >= 2) {
-    reinterpret_cast<uint32_t*>(sSFA)[threadIdx.x - 64] = 0x7F7F7F7Fu;  // A-side scales: 2^0
-    fence_proxy_async_smem();
-  }
-  __syncwarp();
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // barriers, TMEM and A-side scales of both CTAs are ready
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (threadIdx.x == 0) atomicMin(&a.stamps[0], globaltimer_ns());
-
-  const int num_tiles = g.m_tiles * g.n_tiles;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer (both CTAs) ----------------
-      const uint64_t pol_stream = policy_evict_first();
-      const uint64_t pol_keep = policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      int issued = 0;
-      bool ok = (a.flags & kFlagTestStall) == 0;
-      for (int tile = pair; ok && tile < num_tiles; tile += n_pairs) {
-        int m_blk, n_blk;
-        tile_coords(g, tile, m_blk, n_blk);
-        for (int kb = 0; kb < g.k_stages; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
-            record_failure(a.status, abort_flag, kErrProducerEmptyWait);
-            ok = false;
-            break;
-          }
-          const uint32_t fb_local = smem_u32(&full[stage]);
-          if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::STAGE_BYTES);
-          const uint32_t fb = mapa_shared(fb_local, 0);
-          tma_load_2d_pair(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * kBK,
-                           m_blk * 2 * kBM + static_cast<int>(rank) * kBM, fb, pol_stream);
-          tma_load_2d_pair(smem_u32(sB + stage * C::B_BYTES), &tmW, kb * kBK,
-                           n_blk * BN + static_cast<int>(rank) * C::HALF_N, fb, pol_keep);
-          tma_load_2d_pair(smem_u32(sSFB + stage * C::SFB_BYTES), &tmSF, 0, n_blk * g.k_stages + kb, fb, pol_keep);
-          ++issued;
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      // The leader's barrier counts both CTAs' copies: before leaving, the leader
-      // waits for the most recent ones to land (the peer's too).
-      if (leader) {
-        const int pending = issued < C::STAGES ? issued : C::STAGES;
-        int s = stage;
-        uint32_t ph = phase;
-        for (int i = 0; i < pending; ++i) {
-          if (s == 0) {
-            s = C::STAGES - 1;
-            ph ^= 1u;
-          } else {
-            --s;
-          }
-          if (!mbar_wait_bounded(smem_u32(&full[s]), ph, nullptr, kWaitLimitNs)) {
-            record_failure(a.status, abort_flag, kErrDrainWait);
-            break;
-          }
-        }
-      }
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0 && leader) {
-      // ---------------- MMA issuer (leader only, for both CTAs) ----------------
-      const uint32_t idesc = idesc_mxf8_e4m3(2 * kBM, BN);
-      const uint32_t sfa_t = tmem_base + C::SFA_COL;
-      const uint32_t sfb_t = tmem_base + C::SFB_COL;
-      tc_copy_32x128b_x4_pair(sfa_t, smem_desc_plain(smem_u32(sSFA)));
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int tile = pair; ok && tile < num_tiles; tile += n_pairs) {
-        if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
-          record_failure(a.status, abort_flag, kErrMmaTmemEmptyWait);
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < g.k_stages; ++kb) {
-          if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
-            record_failure(a.status, abort_flag, kErrMmaFullWait);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sf_smem = smem_u32(sSFB + stage * C::SFB_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::SF_CHUNKS; ++c)
-            tc_copy_32x128b_x4_pair(sfb_t + 4 * c, smem_desc_plain(sf_smem + 512 * c));
-          const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
-          const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
-#pragma unroll
-          for (int k = 0; k < kBK / 32; ++k)
-            mma_mxf8_pair(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t,
-                          (kb | k) != 0 ? 1u : 0u);
-          tc_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        tc_commit_pair_multicast(smem_u32(&tfull[acc]), 0x3);
-        if (++acc == C::ACC_STAGES) {
-          acc = 0;
-          acc_phase ^= 1u;
-        }
-      }
-      tc_commit_pair(smem_u32(drain));
-      if (!mbar_wait_bounded(smem_u32(drain), 0, nullptr, kWaitLimitNs))
-        record_failure(a.status, abort_flag, kErrDrainWait);
-    }
-    __syncwarp();
-  } else {
-    // ---------------- epilogue (warps 2..5, both CTAs) ----------------
-    const uint64_t pol_out = policy_evict_first();
-    const int quarter = warp & 3;
-    const int row_in_block = quarter * 32 + lane;
-    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int tile = pair; tile < num_tiles; tile += n_pairs) {
-      int m_blk, n_blk;
-      tile_coords(g, tile, m_blk, n_blk);
-      bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) {
-        if (lane == 0) record_failure(a.status, abort_flag, kErrEpilogueTmemFullWait);
-        break;
-      }
-      tc_fence_after();
-      const int block128 = m_blk * 2 + static_cast<int>(rank);
-      // A 128-row half wholly past T (T mod 256 in (0, 128]) has nothing to store.
-      const bool live = block128 * kBM < g.T;
-      float ss_q = 0.0f, ss_k = 0.0f;
-      if (live)
-        epilogue_drain<BN>(g, a, t_lane + static_cast<uint32_t>(acc * BN), block128, row_in_block, n_blk * BN,
-                           pol_out, ss_q, ss_k);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
-      if (live)
-        epilogue_publish<BN>(g, a, block128, row_in_block, n_blk * BN, n_blk < g.n_qk_tiles, ss_q, ss_k, lane);
-      if (++acc == C::ACC_STAGES) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-    __syncwarp();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  cluster_sync();  // no MMA, copy or remote arrive still targets either CTA
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
-  }
-  if (threadIdx.x == 0) atomicMax(&a.stamps[1], globaltimer_ns());
-}
 
 // Repack W's UE8M0 scales [I, H/32] into, per (N tile, K stage), SF_CHUNKS blocks of
 // 512 bytes: byte 16*r + 4*c + kb of block `chunk` is the scale of output column
@@ -712,46 +46,6 @@ __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __re
   }
 }
 
-template <int BN>
-cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                          const GemmArgs& a, cudaStream_t s, int num_sms) {
-  using C = K1Cfg<BN>;
-  auto kern = qkv_gemm_mxf8_kernel<BN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM));
-  if (e != cudaSuccess) return e;
-  const int tiles = g.m_tiles * g.n_tiles;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, C::SMEM, s>>>(tmA, tmW, g, a);
-  return cudaGetLastError();
-}
-
-template <int BN>
-cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                               const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms) {
-  using C = K1PairCfg<BN>;
-  auto kern = qkv_gemm_mxf8_pair_kernel<BN>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(C::SMEM));
-  if (e != cudaSuccess) return e;
-  const int tiles = g.m_tiles * g.n_tiles;
-  const int pairs = num_sms / 2;
-  const int grid = 2 * (tiles < pairs ? tiles : pairs);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, tmSF, g, a);
-}
-
 }  // namespace
 
 bool gemm_tile_supported(int tile_n) {
@@ -787,20 +81,21 @@ cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_pac
 
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                         const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms) {
+  if (a.head_norm != 0) return launch_gemm_head(g, tmA, tmW, tmSF, a, s, num_sms);
   if (g.cta_pair) {
     switch (g.tile_n) {
-      case 128: return launch_gemm_pair_t<128>(g, tmA, tmW, tmSF, a, s, num_sms);
-      case 192: return launch_gemm_pair_t<192>(g, tmA, tmW, tmSF, a, s, num_sms);
-      case 240: return launch_gemm_pair_t<240>(g, tmA, tmW, tmSF, a, s, num_sms);
-      case 256: return launch_gemm_pair_t<256>(g, tmA, tmW, tmSF, a, s, num_sms);
+      case 128: return launch_gemm_pair_t<128, false>(g, tmA, tmW, tmSF, a, s, num_sms);
+      case 192: return launch_gemm_pair_t<192, false>(g, tmA, tmW, tmSF, a, s, num_sms);
+      case 240: return launch_gemm_pair_t<240, false>(g, tmA, tmW, tmSF, a, s, num_sms);
+      case 256: return launch_gemm_pair_t<256, false>(g, tmA, tmW, tmSF, a, s, num_sms);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (g.tile_n) {
-    case 128: return launch_gemm_t<128>(g, tmA, tmW, a, s, num_sms);
-    case 192: return launch_gemm_t<192>(g, tmA, tmW, a, s, num_sms);
-    case 240: return launch_gemm_t<240>(g, tmA, tmW, a, s, num_sms);
-    case 256: return launch_gemm_t<256>(g, tmA, tmW, a, s, num_sms);
+    case 128: return launch_gemm_t<128, false>(g, tmA, tmW, a, s, num_sms);
+    case 192: return launch_gemm_t<192, false>(g, tmA, tmW, a, s, num_sms);
+    case 240: return launch_gemm_t<240, false>(g, tmA, tmW, a, s, num_sms);
+    case 256: return launch_gemm_t<256, false>(g, tmA, tmW, a, s, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -25,6 +25,10 @@ QKV_CTE_MODE_FUSED = 0
 QKV_CTE_MODE_SEPARATE = 1
 QKV_CTE_LAYOUT_BSD = 0
 QKV_CTE_LAYOUT_NBSD = 1
+QKV_CTE_NORM_NONE = 0
+QKV_CTE_NORM_ACROSS_HEADS = 1
+QKV_CTE_NORM_HEAD_RMS = 2
+QKV_CTE_NORM_HEAD_LAYER = 3
 QKV_CTE_INPUT_ROW_FP8 = 0
 QKV_CTE_INPUT_PACKED = 1
 QKV_CTE_INPUT_BF16 = 2
@@ -36,7 +40,7 @@ QKV_CTE_FLAG_GEMM_SINGLE_CTA = 0x10
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
             "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",
-            "qkv_cte_row_quantize", "qkv_cte_unpack_rows")
+            "qkv_cte_row_quantize", "qkv_cte_unpack_rows", "qkv_cte_interleaved_to_rotate_half")
 QKV_CTE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -105,6 +109,9 @@ def load() -> ctypes.CDLL:
     lib.qkv_cte_row_quantize.restype = ctypes.c_int
     lib.qkv_cte_unpack_rows.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
     lib.qkv_cte_unpack_rows.restype = ctypes.c_int
+    lib.qkv_cte_interleaved_to_rotate_half.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                                       ctypes.c_int32, ctypes.c_int32, P]
+    lib.qkv_cte_interleaved_to_rotate_half.restype = ctypes.c_int
     lib.qkv_cte_status.argtypes = [P, P]
     lib.qkv_cte_status.restype = ctypes.c_int
     lib.qkv_cte_pass_times.argtypes = [P, ctypes.POINTER(ctypes.c_float)]
@@ -244,6 +251,24 @@ def qkv_cte_unpack_rows(packed, A=None, a_scale=None, stream=None):
     _check(load().qkv_cte_unpack_rows(_ptr("packed", packed), T, H, _ptr("A", A), _ptr("a_scale", a_scale),
                                       _stream_handle(stream)))
     return A, a_scale
+
+
+def qkv_cte_interleaved_to_rotate_half(src, n_q_heads, n_kv_heads, d_head, dst=None, stream=None):
+    """Permute the Q/K rows of a per-output-channel tensor (first dimension = rows)
+    from the interleaved to the rotate-half lane order; returns dst (allocated here
+    when not given). See qkv_cte.h for how to lay out each tensor as rows."""
+    if not (src.is_cuda and src.is_contiguous()):
+        raise ValueError("src: must be a contiguous CUDA tensor")
+    if dst is None:
+        dst = torch.empty_like(src)
+    if not (dst.is_cuda and dst.is_contiguous()) or dst.numel() * dst.element_size() != src.numel() * src.element_size():
+        raise ValueError("dst: must be a contiguous CUDA tensor of src's size")
+    rows = src.shape[0] if src.dim() > 0 else 0
+    row_bytes = (src.numel() * src.element_size()) // rows if rows else 1
+    _check(load().qkv_cte_interleaved_to_rotate_half(ctypes.c_void_p(src.data_ptr()), ctypes.c_void_p(dst.data_ptr()),
+                                                     rows, row_bytes, n_q_heads, n_kv_heads, d_head,
+                                                     _stream_handle(stream)))
+    return dst
 
 
 def qkv_cte_status(workspace, stream=None) -> int:

@@ -34,7 +34,9 @@ def run_path(call, g, tile_n=0, flags=0, want_sumsq=True, want_inv=True, stream=
                 rope=call.rope, eps=call.eps, tile_n=tile_n, flags=flags, device=dev,
                 output_layout=QKV_CTE_LAYOUT_NBSD if nbsd else QKV_CTE_LAYOUT_BSD, input_layout=input_layout)
     sumsq = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev) if want_sumsq else None
-    inv = torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev) if want_inv else None
+    # inv_rms is an output of the across-heads norm only
+    inv = (torch.full((call.tokens, 2), float("nan"), dtype=torch.float32, device=dev)
+           if want_inv and call.norm in (0, 1) else None)
     heads = call.width // call.d_head
     if out is None:
         shape = (heads, call.tokens, call.d_head) if nbsd else (call.tokens, call.width)
@@ -83,7 +85,7 @@ def check_outputs(call, inp, out, sumsq, inv, rows=None, name="case"):
             assert np.all(rel <= SS_REL), f"{name}: sumsq[{c}] max rel err {np.nanmax(rel):.3e}"
         if call.n_kv_heads == 0:
             assert np.all(s[:, 1] == 0), f"{name}: sumsq K column should be 0 without a K segment"
-    if inv is not None and call.norm:
+    if inv is not None and call.norm == 1:
         v = inv.index_select(0, idx_dev).cpu().double().numpy()
         for c in segs:
             rel = np.abs(v[:, c] - ref["inv_rms"][:, c]) / np.abs(ref["inv_rms"][:, c])

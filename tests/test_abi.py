@@ -73,7 +73,11 @@ def _plan_code(**kw):
     (dict(n_kv_heads=0, mode=0), -1),
     (dict(n_kv_heads=2, mode=1), -1),
     (dict(mode=7), -1),
-    (dict(norm=2), -1),
+    (dict(norm=4), -1),
+    (dict(norm=2), 0),
+    (dict(norm=3), 0),
+    (dict(norm=2, tile_n=240), -2),     # per-head norm: 128-wide heads do not divide a 240 tile
+    (dict(norm=3, tile_n=256), 0),
     (dict(rope=-1), -1),
     (dict(eps=-1.0), -1),
     (dict(eps=float("nan")), -1),
@@ -90,6 +94,28 @@ def _plan_code(**kw):
 ])
 def test_plan_validation(kw, code):
     assert _plan_code(**kw) == code
+
+
+def test_per_head_norm_chooses_a_tile_of_whole_heads():
+    for d, tile in ((128, 128), (64, 192), (16, 240), (256, 256), (48, 240), (32, 192)):
+        plan, ws = q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, d, norm=2))
+        try:
+            info = q.qkv_cte_get_plan_info(plan)
+            assert info.tile_n == tile and info.tile_n % d == 0
+        finally:
+            q.qkv_cte_destroy(plan)
+
+
+def test_per_head_norm_has_no_hand_off():
+    """The per-head kinds finish in the GEMM epilogue: no Q/K hand-off in the workspace."""
+    T = 1000
+    plan_a, ws_a = q.qkv_cte_plan(q.make_desc(T, 512, 4, 4, 128, norm=1, tile_n=128))
+    plan_h, ws_h = q.qkv_cte_plan(q.make_desc(T, 512, 4, 4, 128, norm=2, tile_n=128))
+    q.qkv_cte_destroy(plan_a)
+    q.qkv_cte_destroy(plan_h)
+    rows = -(-T // 128) * 128
+    kq = 8 * 128
+    assert ws_a - ws_h == -(-(rows * kq * 2) // 256) * 256 + -(-(rows * kq // 16) // 256) * 256
 
 
 def test_plan_info_reports_the_choices():

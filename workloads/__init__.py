@@ -231,6 +231,9 @@ def make_inputs(call: Call) -> Dict[str, Optional[torch.Tensor]]:
     g = torch.randn(I, generator=_gen(s, 3)) * call.gamma_std + 1.0
     nq = call.n_q_heads * d
     nk = call.n_kv_heads * d
+    if call.norm in (2, 3):  # per-head norms: one [d_head] gamma per segment
+        g = torch.cat([g[:d], g[nq:nq + d]])
+        nq, nk = d, (d if call.n_kv_heads > 0 else 0)
     gamma_q = _bf16_bits(g[:nq])
     gamma_k = _bf16_bits(g[nq:nq + nk]) if nk > 0 else None
     w_col_scale = None
