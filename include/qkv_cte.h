@@ -115,7 +115,7 @@ typedef struct {
     int32_t hidden;        /* H, contraction length; multiple of 128 */
     int32_t n_q_heads;     /* Q heads in this call (>= 1) */
     int32_t n_kv_heads;    /* K/V heads; 0 for a single-segment (separate) call */
-    int32_t d_head;        /* head dim; multiple of 16 */
+    int32_t d_head;        /* head dim; multiple of 16, of 32 when a norm or RoPE runs */
     int32_t mode;          /* QKV_CTE_MODE_FUSED (n_kv >= 1) or QKV_CTE_MODE_SEPARATE (n_kv == 0) */
     int32_t norm;          /* QKV_CTE_NORM_*: 0 none, 1 across heads, 2 per-head RMS, 3 per-head LayerNorm */
     int32_t rope;          /* 1: rotate-half RoPE on Q (and K); needs cos/sin */
@@ -145,8 +145,8 @@ typedef struct {
  * workspace_bytes: receives the device workspace size qkv_cte_run needs.
  * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values,
  * unknown input layout) or
- * -2 (H % 128, d_head % 16, T > INT32_MAX, unknown tile_n, a per-head norm with a tile_n that
- * d_head does not divide). */
+ * -2 (H % 128, d_head % 16, d_head % 32 with a norm or RoPE, T > INT32_MAX, unknown tile_n,
+ * a per-head norm with a tile_n that d_head does not divide). */
 int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes);
 
 /* Fill `info` for `plan`. Returns 0 or -1 (null pointer). */

@@ -199,6 +199,11 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
     return fail(QKV_CTE_ERR_INVALID, "unknown input layout %d", d.input_layout);
   const long long I = (long long)(d.n_q_heads + 2LL * d.n_kv_heads) * d.d_head;
   if (I > INT32_MAX / 2) return fail(QKV_CTE_ERR_UNSUPPORTED, "output width too large");
+  // The norm/RoPE pass and the per-head epilogue work on 16-column chunks paired with
+  // the chunk d_head/2 away (the rotate-half partner), so d_head/2 must be a multiple
+  // of 16 whenever either of them runs.
+  if ((d.norm != QKV_CTE_NORM_NONE || d.rope) && d.d_head % 32 != 0)
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "a norm or RoPE needs d_head %% 32 == 0 (got %d)", d.d_head);
   const int tile_n = choose_tile_n(d, (int)I);
   if (!gemm_tile_supported(tile_n)) return fail(QKV_CTE_ERR_UNSUPPORTED, "tile_n %d not built", tile_n);
   if (per_head_norm(d) && tile_n % d.d_head != 0)

@@ -74,6 +74,10 @@ def _plan_code(**kw):
     (dict(n_kv_heads=2, mode=1), -1),
     (dict(mode=7), -1),
     (dict(norm=4), -1),
+    (dict(d_head=48), -2),                       # norm + RoPE pair chunks d/2 apart: d % 32
+    (dict(d_head=16, norm=0, rope=1), -2),
+    (dict(d_head=80, norm=2, rope=0), -2),
+    (dict(d_head=48, norm=0, rope=0), 0),        # plain projection: d % 16 is enough
     (dict(norm=2), 0),
     (dict(norm=3), 0),
     (dict(norm=2, tile_n=240), -2),     # per-head norm: 128-wide heads do not divide a 240 tile
@@ -97,13 +101,19 @@ def test_plan_validation(kw, code):
 
 
 def test_per_head_norm_chooses_a_tile_of_whole_heads():
-    for d, tile in ((128, 128), (64, 192), (16, 240), (256, 256), (48, 240), (32, 192)):
+    for d, tile in ((128, 128), (64, 192), (256, 256), (32, 192), (96, 192)):
         plan, ws = q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, d, norm=2))
         try:
             info = q.qkv_cte_get_plan_info(plan)
             assert info.tile_n == tile and info.tile_n % d == 0
         finally:
             q.qkv_cte_destroy(plan)
+
+
+def test_per_head_norm_rejects_heads_no_tile_holds():
+    with pytest.raises(q.QkvCteError) as ei:
+        q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, 160, norm=2))
+    assert ei.value.code == q.QKV_CTE_ERR_UNSUPPORTED and "whole heads" in str(ei.value)
 
 
 def test_per_head_norm_has_no_hand_off():

@@ -316,3 +316,18 @@ def test_nbsd_wan480p_sampled_matches_bsd():
     op_b, out_b, _, _ = run_path(call, g)
     op_b.status()
     assert_same_to_rounding(call, out_n, out_b, name="nbsd_vs_bsd_wan480p")
+
+
+@pytest.mark.parametrize("norm", [1, 2, 3])
+def test_d_head_32(norm):
+    """The smallest head the norm/RoPE pairing takes: d/2 = 16, one chunk per half."""
+    call = wl.custom_call(name=f"d32_n{norm}", tokens=300, hidden=256, n_q_heads=6, n_kv_heads=3, d_head=32,
+                          norm=norm, rope=1, seed=71 + norm, has_w_col_scale=True)
+    _case(call)
+
+
+def test_d_head_48_plain_projection():
+    """d % 32 != 0 is refused with a norm or RoPE, but a plain projection takes it."""
+    call = wl.custom_call(name="d48_plain", tokens=257, hidden=384, n_q_heads=3, n_kv_heads=2, d_head=48,
+                          norm=0, rope=0, seed=81, has_w_col_scale=True)
+    _case(call)
