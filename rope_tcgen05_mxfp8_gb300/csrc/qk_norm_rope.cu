@@ -10,15 +10,16 @@
 // On one GPU every head is local, so the page's cross-rank AllReduce of the sums is
 // the identity: K1 already summed over every column tile of the row. The pass is
 // launched as a programmatic dependent of K1: its blocks run beside K1's persistent
-// CTAs and take each 32-row unit once K1's counter says the unit's 128-row panel is
+// CTAs and take each task's rows once K1's counter says their 128-row panel is
 // complete (a bounded acquire wait), so it mostly hides under the GEMM. The page writes
 // the un-normalised Q/K into the output and re-reads it; here K1 hands them over in
 // block floating point (fp16 with a power-of-two exponent per row and 16 columns, in
 // a tile-major workspace buffer), so the result is rounded to bf16 once, here. This
-// pass is HBM-bound. Lanes map to rows: a warp reads the hand-off with 1 KB
-// coalesced loads (four heads' worth in flight at once), keeps its row's cos/sin
-// chunk and inv_rms in registers across all heads, reads gamma as warp-wide
-// broadcasts, and writes one full 32-byte sector of O per row and half-head.
+// pass is HBM-bound. A warp covers a few rows and the whole low half of a head: lane
+// (r, q) owns row r and the 16-column chunk q of the low half (plus its partner d/2
+// away), so the lanes of one row store whole 128-byte lines of O (d = 128) and read
+// the tile-major hand-off in 256-byte runs; four heads' loads are in flight at once,
+// each lane keeps its cos/sin chunk and inv_rms in registers across all heads.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -124,36 +125,48 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 constexpr int kHeadBatch = 4;   // heads whose hand-off loads are in flight together
 constexpr int kHeadGroup = 20;  // heads per warp task (a multiple of kHeadBatch)
 
-// One warp task = 32 consecutive rows (one per lane) x one 16-column chunk c of the
-// low half of up to kHeadGroup heads, with its partner chunk d/2 away (the rotation
-// pairs lane j with lane j + d/2 inside each head). Small tasks keep the warps
-// evenly loaded to the end.
+// Rows per warp task: the low half of a head is d/32 chunks of 16 columns, one lane
+// each, and a task takes the largest power of two of rows that fits 32 lanes (so a
+// task never crosses a 128-row panel). Lanes past rows * chunks idle.
+__host__ __device__ inline int task_rows(int d_head) {
+  const int per_row = d_head / 32;
+  int r = 32 / per_row;
+  while (r & (r - 1)) r &= r - 1;
+  return r;
+}
+
+// One warp task = task_rows(d) consecutive rows x the whole low half of up to
+// kHeadGroup heads, each lane with its chunk's partner d/2 away (the rotation pairs
+// lane j with lane j + d/2 inside each head). Small tasks keep the warps evenly
+// loaded to the end.
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeArgs p) {
   if (threadIdx.x == 0) atomicMin(&p.stamps[0], now_ns());
   const int lane = threadIdx.x & 31;
   const int d = p.d_head;
   const int half = d / 2;
-  const int chunks = d / 32;  // 16-column chunks in the low half of a head
+  const int per_row = d / 32;  // lanes per row: the 16-column chunks of the low half
+  const int rows = task_rows(d);
+  const int lr = lane / per_row;          // this lane's row inside the task
+  const int c = lane - lr * per_row;      // this lane's chunk of the low half
+  const bool lane_on = lr < rows;
   const int heads = p.n_q + p.n_kv;
   const int qk_chunks = heads * d / 16;
   const int groups = (heads + kHeadGroup - 1) / kHeadGroup;
-  const long long units = (p.T + 31) / 32;
-  const long long tasks = units * chunks * groups;
+  const long long units = (p.T + rows - 1) / rows;
+  const long long tasks = units * groups;
   const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
   // Read-once hand-off and write-once output: first out of L2, so the GEMM's
   // L2-resident weight band running beside this pass keeps its place.
   const uint64_t once = evict_first_policy();
   for (long long task = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); task < tasks;
        task += warps) {
-    const int u = static_cast<int>(task / (chunks * groups));
-    const int rem = static_cast<int>(task - static_cast<long long>(u) * chunks * groups);
-    const int c = rem / groups;
-    const int grp = rem - c * groups;
+    const int u = static_cast<int>(task / groups);
+    const int grp = static_cast<int>(task - static_cast<long long>(u) * groups);
     const int h_begin = grp * kHeadGroup;
     const int h_end = min(heads, h_begin + kHeadGroup);
-    const int row0 = u * 32;
-    const int t = row0 + lane;
-    const bool row_ok = t < p.T;
+    const int row0 = u * rows;
+    const int t = lane_on ? row0 + lr : row0;  // idle lanes shadow the task's first row
+    const bool row_ok = lane_on && t < p.T;
     const int panel = row0 >> 7;
     int ok = 1;
     if (lane == 0) ok = wait_panel_ready(p.ready + panel, p.ready_target) ? 1 : 0;
@@ -163,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
       break;
     }
     (void)ld_acquire(p.ready + panel);  // each lane acquires the panel's publication
-    const int tr = row_ok ? t : p.T - 1;
+    const int tr = t < p.T ? t : p.T - 1;
 
     float inv_q = 1.0f, inv_k = 1.0f;
     if (p.norm) {
@@ -184,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
       load8_nc(sr + half, sh);
       load8_nc(sr + half + 8, sh + 8);
     }
-    const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (row0 & 127) + lane;
+    const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (t & 127);
     for (int hg0 = h_begin; hg0 < h_end; hg0 += kHeadBatch) {
       RawChunk raw_lo[kHeadBatch], raw_hi[kHeadBatch];
 #pragma unroll
@@ -249,7 +262,9 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const NormRopeAr
 
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap) {
   if (!a.norm && !a.rope) return cudaSuccess;
-  const long long tasks = static_cast<long long>((a.T + 31) / 32) * (a.d_head / 32) *
+  if (a.d_head < 32 || a.d_head % 32 != 0) return cudaErrorInvalidValue;
+  const int rows = task_rows(a.d_head);
+  const long long tasks = static_cast<long long>((a.T + rows - 1) / rows) *
                           ((a.n_q + a.n_kv + kHeadGroup - 1) / kHeadGroup);
   if (tasks == 0) return cudaSuccess;
   // Overlapped with the GEMM, the grid is kept to what fits beside each GEMM CTA
