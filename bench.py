@@ -51,6 +51,8 @@ def _args():
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--gemm", choices=["auto", "pair", "single"], default="auto",
                    help="GEMM form: 256-row tiles on SM pairs, 128-row tiles on one SM, or the library's choice")
+    p.add_argument("--norm-in-gemm", action="store_true",
+                   help="run the norm/RoPE work inside the GEMM's epilogue warps instead of its own kernel")
     p.add_argument("--layout", choices=["bsd", "nbsd"], default="bsd",
                    help="output layout: BSD [T, I] or NBSd [heads, T, d_head]")
     p.add_argument("--input", choices=["fp8", "packed", "bf16"], default="fp8",
@@ -239,7 +241,7 @@ _INPUT_NOTE = {
 }
 
 
-def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8"):
+def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8", op_norm_in_gemm=False):
     return {
         "workload": (f"{call.name}: Wan2.2-style fused QKV self-attention projection, T={call.tokens} "
                      f"H={call.hidden} n_q={call.n_q_heads} n_kv={call.n_kv_heads} d_head={call.d_head} "
@@ -248,6 +250,7 @@ def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8"):
         "n_q_heads": call.n_q_heads, "n_kv_heads": call.n_kv_heads, "d_head": call.d_head,
         "tile_n": tile_n,
         "output_layout": "NBSd [heads, T, d_head]" if layout == "nbsd" else "BSD [T, I]",
+        "norm_rope_work": "inside the GEMM's epilogue warps" if op_norm_in_gemm else "its own kernel, overlapped with the GEMM",
         "qk_norm": {0: "none", 1: "across heads (RMS)", 2: "per head RMS, in the GEMM epilogue",
                     3: "per head LayerNorm, in the GEMM epilogue"}[call.norm],
         "input": _INPUT_NOTE[input_kind],
@@ -289,6 +292,10 @@ def run_ours(args):
     inp = wl.make_inputs(call)
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     gemm_flag = {"auto": 0, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA}[args.gemm]
+    if args.norm_in_gemm:
+        from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_NORM_IN_GEMM
+
+        gemm_flag |= QKV_CTE_FLAG_NORM_IN_GEMM
     layout = QKV_CTE_LAYOUT_NBSD if args.layout == "nbsd" else QKV_CTE_LAYOUT_BSD
     input_layout = {"fp8": QKV_CTE_INPUT_ROW_FP8, "packed": QKV_CTE_INPUT_PACKED, "bf16": QKV_CTE_INPUT_BF16}[args.input]
     # The step's activation input, resident on the device (and its host copy for e2e).
@@ -436,7 +443,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; Wan2.2 480p shapes and distributions)",
-        "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout, input_kind=args.input),
+        "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout, input_kind=args.input,
+                          op_norm_in_gemm=bool(op.info.norm_in_gemm)),
         "pct_nominal_dense_fp8_peak": 100.0 * value / (world * NOMINAL_FP8_TFLOPS),
         "pct_measured_fp8_peak": 100.0 * value / (world * fp8_peak),
         "passes_ms": {"prep": prep_ms, "gemm_epilogue": gemm_ms, "norm_rope_span": norm_span_ms,
@@ -457,9 +465,10 @@ def run_ours(args):
                                      f"{FP8_PER_BF16:g}")},
         "clocks": clocks,
         "e2e": e2e,
-        # prep + GEMM, the producer for a bf16 / packed input, the norm/RoPE pass unless the
-        # norm is per head (finished in the GEMM epilogue)
-        "gpu_launches": (2 + (args.input != "fp8") + (call.norm == 1 or (call.norm == 0 and call.rope == 1)))
+        # prep + GEMM, the producer for a bf16 / packed input, and the norm/RoPE pass when
+        # it is a kernel of its own (not per head, not run by the GEMM's epilogue warps)
+        "gpu_launches": (2 + (args.input != "fp8")
+                         + ((call.norm == 1 or (call.norm == 0 and call.rope == 1)) and not op.info.norm_in_gemm))
         * args.steps,
         "producer": producer,
         "cpu_baseline": cpu,

@@ -100,14 +100,21 @@ enum { QKV_CTE_INPUT_ROW_FP8 = 0, QKV_CTE_INPUT_PACKED = 1, QKV_CTE_INPUT_BF16 =
 /* Record CUDA events between the launches of each run so qkv_cte_pass_times() can
  * report per-pass device times. */
 #define QKV_CTE_FLAG_PROFILE 0x2u
-/* Launch the norm/RoPE pass after the GEMM has finished instead of overlapping the two
- * (same results; used to time each pass on its own). */
+/* Launch the norm/RoPE pass as its own kernel after the GEMM has finished instead of
+ * overlapping the two (same results; used to time each pass on its own). */
 #define QKV_CTE_FLAG_SERIAL_PASSES 0x4u
 /* GEMM form: tiles of 256 rows on a pair of SMs (M = 256 MMAs; each SM stages half
  * of the weight tile), or tiles of 128 rows on one SM. Neither flag: the library
  * chooses. Both: -1. */
 #define QKV_CTE_FLAG_GEMM_CTA_PAIR 0x8u
 #define QKV_CTE_FLAG_GEMM_SINGLE_CTA 0x10u
+/* Run the norm/RoPE work inside the CTA-pair GEMM's epilogue warps, between tiles (one
+ * kernel), instead of as a kernel of its own overlapped with the GEMM through a
+ * programmatic dependent launch (the default). Same results; measured slower at the Wan
+ * shapes (the norm work slows the GEMM just as much from inside it, and what is left
+ * when the tiles are done runs as a tail). Ignored without the pair form or with
+ * QKV_CTE_FLAG_SERIAL_PASSES. */
+#define QKV_CTE_FLAG_NORM_IN_GEMM 0x20u
 
 /* Problem description ([qkv_cte] "Interface" argument table, flattened to scalars). */
 typedef struct {
@@ -136,7 +143,8 @@ typedef struct {
     int32_t n_tiles;         /* N tiles */
     int32_t n_bands;         /* bands of N tiles in the GEMM's tile order */
     int32_t cta_pair;        /* 1: 256-row tiles on SM pairs; 0: 128-row tiles */
-    int32_t reserved;
+    int32_t norm_in_gemm;    /* 1: the norm/RoPE work runs inside the GEMM's epilogue warps (one
+                                kernel); 0: as a kernel of its own, or there is none */
     int64_t workspace_bytes; /* as returned by qkv_cte_plan */
 } qkv_cte_plan_info;
 
@@ -196,10 +204,11 @@ int qkv_cte_status(void* workspace, void* stream);
  * created with QKV_CTE_FLAG_PROFILE. ms must hold 4 floats:
  *   ms[0] prep (the input's unpack or quantise step when it is packed or bf16, the
  *         scale repack and clears), from CUDA events around those launches;
- *   ms[1] GEMM with its fused epilogue, and ms[2] norm + RoPE (0 when the call has
- *         neither): first-block start to last-block end, from %globaltimer stamps the
- *         kernels write into the workspace (the two passes overlap, so no CUDA event
- *         can separate them);
+ *   ms[1] GEMM with its fused epilogue (including the norm/RoPE work when it runs in
+ *         the GEMM's epilogue warps), and ms[2] norm + RoPE (0 when the call has
+ *         neither): first start to last end of that work, from %globaltimer stamps the
+ *         kernels write into the workspace (the two overlap, so no CUDA event can
+ *         separate them);
  *   ms[3] the whole run, from CUDA events.
  * Blocks until that run has finished; its workspace must still be valid. Returns 0, -1
  * (no flag, never run, null pointer) or -3. */

@@ -20,9 +20,10 @@ enum : uint32_t {
 };
 
 // Workspace layout (all offsets 256-byte aligned):
-//   [0, 256)                 status word (offset 0) and, at kStampOffset, four uint64
-//                            %globaltimer stamps:
-//                            K1 first start, K1 last end, K2 first start, K2 last end
+//   [0, 256)                 status word (offset 0); at kStampOffset four uint64
+//                            %globaltimer stamps: K1 first start, K1 last end, norm/RoPE
+//                            first start, norm/RoPE last end; at kTaskCounterOffset the
+//                            norm/RoPE task counter of the fused GEMM
 //   [256, 256 + ss_bytes)    fp32 [T, 2] sum-of-squares accumulator (used when the
 //                            caller passes no sumsq buffer)
 //   [.., + sf_bytes)         W's UE8M0 scales repacked per (N tile, K stage) in the
@@ -40,6 +41,7 @@ enum : uint32_t {
 //   [.., + T*H), [.., + 4T)  only for a packed or bf16 input: the e4m3 codes [T, H] and
 //                            fp32 row scales [T] the producer step writes for the GEMM
 constexpr size_t kStampOffset = 64;
+constexpr size_t kTaskCounterOffset = 128;  // uint32: next norm/RoPE task the GEMM's epilogue warps claim
 
 struct WorkspaceLayout {
   size_t status_off, sumsq_off, sf_off, ready_off, qk_off, qk_exp_off, act_off, act_scale_off, total;
@@ -162,6 +164,7 @@ struct NormRopeArgs {
   uint32_t ready_target;     // 4 * K1's Q/K tiles: the panel's Q and K are final
   unsigned long long* stamps;  // [0] first block start (min), [1] last block end (max)
   uint32_t* status;
+  uint32_t* task_next;       // next unclaimed task (the GEMM's epilogue warps claim them)
 };
 
 // Supported N tiles (compile-time instantiations of K1).
@@ -172,17 +175,26 @@ size_t gemm_smem_bytes(int tile_n);
 // Launchers. Each returns cudaSuccess or the launch error.
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
                         size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
-                        cudaStream_t s, int num_sms);
-// tmSF: the repacked scales as a uint32 [n_tiles * k_stages, sf_chunks * 128] map with
-// one-row boxes (used by the CTA-pair kernel).
+                        uint32_t* task_next, cudaStream_t s, int num_sms);
+// K1. tmSF: the repacked scales as a uint32 [n_tiles * k_stages, sf_chunks * 128] map
+// with one-row boxes (used by the CTA-pair kernel). With `fused` (CTA-pair form only)
+// the epilogue warps also run the norm/RoPE tasks of `*fused` between tiles, and no
+// separate pass is launched.
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                        const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms);
-// Launched right after K1 on the same stream as a programmatic dependent launch, so
-// its blocks start while K1 runs and take each row panel as soon as K1 marks it ready.
+                        const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms,
+                        const NormRopeArgs* fused);
 // K1 with the per-head qk-norm epilogue (qkv_gemm_mxf8_head.cu); launch_gemm calls it
 // when a.head_norm != 0.
 cudaError_t launch_gemm_head(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                              const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms);
+// K1 (CTA-pair form) with the norm/RoPE tasks run by its epilogue warps
+// (qkv_gemm_mxf8_fused.cu); launch_gemm calls it when given `fused`.
+cudaError_t launch_gemm_fused(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
+                              const CUtensorMap& tmSF, const GemmArgs& a, const NormRopeArgs& nr, cudaStream_t s,
+                              int num_sms);
+// K2, the norm/RoPE pass as its own kernel. With `overlap` it is launched right after
+// K1 on the same stream as a programmatic dependent launch, so its blocks start while
+// K1 runs and take each row panel as soon as K1 marks it ready.
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap);
 
 // The producer step (row_quant.cu): bf16 [T, H] -> e4m3 codes [T, H] + fp32 scales [T]

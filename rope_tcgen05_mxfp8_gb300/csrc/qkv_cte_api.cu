@@ -27,7 +27,8 @@ struct qkv_cte_plan_s {
   int ev_device = -1;
   bool ran = false;
   bool has_norm_pass = false;
-  bool second_pass = false;  // the norm/RoPE kernel runs (across-heads norm, or RoPE alone)
+  bool second_pass = false;  // the norm/RoPE work runs (across-heads norm, or RoPE alone)
+  bool fused_norm = false;   // ... inside the CTA-pair GEMM's epilogue warps
   const void* last_workspace = nullptr;
 };
 
@@ -190,7 +191,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   if (d.output_layout != QKV_CTE_LAYOUT_BSD && d.output_layout != QKV_CTE_LAYOUT_NBSD)
     return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
   const uint32_t known_flags = QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES |
-                               QKV_CTE_FLAG_GEMM_CTA_PAIR | QKV_CTE_FLAG_GEMM_SINGLE_CTA;
+                               QKV_CTE_FLAG_GEMM_CTA_PAIR | QKV_CTE_FLAG_GEMM_SINGLE_CTA |
+                               QKV_CTE_FLAG_NORM_IN_GEMM;
   if ((d.flags & ~known_flags) != 0) return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
   if ((d.flags & QKV_CTE_FLAG_GEMM_CTA_PAIR) && (d.flags & QKV_CTE_FLAG_GEMM_SINGLE_CTA))
     return fail(QKV_CTE_ERR_INVALID, "QKV_CTE_FLAG_GEMM_CTA_PAIR and QKV_CTE_FLAG_GEMM_SINGLE_CTA exclude each other");
@@ -247,6 +249,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   // without a norm; the per-head norms finish in the GEMM's epilogue.
   const bool second_pass = !per_head_norm(d) && (d.norm == QKV_CTE_NORM_ACROSS_HEADS || d.rope);
   p->second_pass = second_pass;
+  p->fused_norm = second_pass && g.cta_pair && (d.flags & QKV_CTE_FLAG_NORM_IN_GEMM) &&
+                  !(d.flags & QKV_CTE_FLAG_SERIAL_PASSES);
   const size_t hand_rows = second_pass ? (size_t)g.blocks128 * 128 : 0;
   w.qk_exp_off = w.qk_off + align_up(hand_rows * p->k_end * sizeof(uint16_t), 256);
   w.act_off = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
@@ -265,7 +269,7 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info) {
   info->n_tiles = plan->g.n_tiles;
   info->n_bands = plan->g.n_bands;
   info->cta_pair = plan->g.cta_pair;
-  info->reserved = 0;
+  info->norm_in_gemm = plan->fused_norm ? 1 : 0;
   info->workspace_bytes = (int64_t)plan->ws.total;
   return ok();
 }
@@ -385,8 +389,9 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
 
   uint32_t* ready = reinterpret_cast<uint32_t*>(ws + plan->ws.ready_off);
   unsigned long long* stamps = reinterpret_cast<unsigned long long*>(ws + kStampOffset);
+  uint32_t* task_next = reinterpret_cast<uint32_t*>(ws + kTaskCounterOffset);
   e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0, ready, status,
-                  stamps, s, dev.sms);
+                  stamps, task_next, s, dev.sms);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
   if (prof) cudaEventRecord(plan->ev[1], s);
 
@@ -416,11 +421,6 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.gamma_k = gamma_k;
   ga.cos_t = cos_table;
   ga.sin_t = sin_table;
-  CUtensorMap tmSF;
-  if ((rc = encode_scales(&tmSF, sf_packed, g)) != QKV_CTE_OK) return rc;
-  e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms);
-  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
-
   NormRopeArgs na;
   na.T = g.T;
   na.I = g.I;
@@ -444,7 +444,16 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.ready_target = 4u * (uint32_t)g.n_qk_tiles;
   na.status = status;
   na.stamps = stamps + 2;
-  if (plan->second_pass) {
+  na.task_next = task_next;
+  CUtensorMap tmSF;
+  if ((rc = encode_scales(&tmSF, sf_packed, g)) != QKV_CTE_OK) return rc;
+  // On request the norm/RoPE tasks run inside the CTA-pair GEMM's epilogue warps;
+  // otherwise as their own kernel, overlapped with the GEMM (or after it, serialised).
+  const bool fused = plan->second_pass && plan->fused_norm;
+  e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms, fused ? &na : nullptr);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+
+  if (plan->second_pass && !fused) {
     e = launch_norm_rope(na, s, dev.sms, (d.flags & QKV_CTE_FLAG_SERIAL_PASSES) == 0);
     if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "norm/rope launch: %s", cudaGetErrorString(e));
   }

@@ -44,6 +44,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "qk_norm_rope.cuh"
 
 namespace qkvcte {
 
@@ -638,10 +639,105 @@ struct K1PairCfg {
   static_assert(STAGES >= 2, "pipeline depth");
 };
 
-template <int BN, bool kHead>
+// ---------------------------------------------------------------------------
+// Norm/RoPE tasks run by the epilogue warps of the fused kernel (the work of K2,
+// qk_norm_rope.cuh). A warp claims tasks from a grid-wide counter in panel order and
+// runs one only once K1's counter shows its panel complete; it does this only while
+// its next accumulator is not ready, so draining a tile always comes first and the
+// MMAs never wait for norm work (a task is a few microseconds, a tile's MMAs about
+// thirteen). When its tiles are done the warp finishes the tasks left. Used on
+// request (QKV_CTE_FLAG_NORM_IN_GEMM): the norm work slows the GEMM as much from
+// inside it as from a kernel of its own beside it, and adds a tail.
+// ---------------------------------------------------------------------------
+// Heads per fused task: short, so a drain is never held up long, yet long enough to
+// spread a row's cos/sin loads over several heads (measured at the 480p shape: 4 heads
+// 2.04 ms, 10 heads 1.93 ms, 20 heads 2.04 ms per call).
+constexpr int kFusedHeadGroup = 10;
+
+struct FusedWork {
+  long long pending = -1;  // claimed, not yet run
+  bool done = false;       // the counter is exhausted
+  bool started = false;
+};
+
+__device__ __forceinline__ void fused_claim(const NormRopeArgs& nr, long long n_tasks, FusedWork& w) {
+  uint32_t t = 0;
+  if ((threadIdx.x & 31) == 0) t = atomicAdd(nr.task_next, 1u);
+  t = __shfl_sync(0xffffffffu, t, 0);
+  if (static_cast<long long>(t) >= n_tasks) {
+    w.done = true;
+    w.pending = -1;
+  } else {
+    w.pending = static_cast<long long>(t);
+  }
+}
+
+// Run the pending task if its panel is complete; returns whether it ran.
+__device__ __forceinline__ bool fused_try(const NormRopeArgs& nr, FusedWork& w, uint64_t once) {
+  const int panel = nrp::task_panel(nr, w.pending, kFusedHeadGroup);
+  int ready = 0;
+  if ((threadIdx.x & 31) == 0) ready = nrp::ld_acquire(nr.ready + panel) >= nr.ready_target ? 1 : 0;
+  ready = __shfl_sync(0xffffffffu, ready, 0);
+  if (!ready) return false;
+  if (!w.started) {
+    w.started = true;
+    if ((threadIdx.x & 31) == 0) atomicMin(&nr.stamps[0], globaltimer_ns());
+  }
+  nrp::run_task(nr, w.pending, kFusedHeadGroup, once);
+  w.pending = -1;
+  return true;
+}
+
+// Wait (bounded) for the accumulator barrier, running norm tasks meanwhile.
+__device__ __forceinline__ bool fused_wait_acc(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                               const NormRopeArgs& nr, long long n_tasks, FusedWork& w,
+                                               uint64_t once) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    int ready = 0;
+    if ((threadIdx.x & 31) == 0) ready = mbar_test_wait(bar, parity) ? 1 : 0;
+    ready = __shfl_sync(0xffffffffu, ready, 0);
+    if (ready) return mbar_wait_bounded(bar, parity, abort_flag, kWaitLimitNs);  // completes at once, per lane
+    if (*abort_flag) return false;
+    bool ran = false;
+    if (!w.done) {
+      if (w.pending < 0) fused_claim(nr, n_tasks, w);
+      if (w.pending >= 0) ran = fused_try(nr, w, once);
+    }
+    if (!ran) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      __nanosleep(64);
+    }
+  }
+}
+
+// After the warp's last tile: the tasks left (each panel wait bounded).
+__device__ __forceinline__ void fused_finish(const NormRopeArgs& nr, long long n_tasks, FusedWork& w,
+                                             volatile int* abort_flag, uint32_t* status, uint64_t once) {
+  uint64_t t0 = globaltimer_ns();
+  while (!w.done && !*abort_flag) {
+    if (w.pending < 0) {
+      fused_claim(nr, n_tasks, w);
+      if (w.done) break;
+    }
+    if (fused_try(nr, w, once)) {
+      t0 = globaltimer_ns();
+      continue;
+    }
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if ((threadIdx.x & 31) == 0) atomicOr(status, kErrNormReadyWait);
+      break;
+    }
+    __nanosleep(256);
+  }
+  if (w.started && (threadIdx.x & 31) == 0) atomicMax(&nr.stamps[1], globaltimer_ns());
+}
+
+template <int BN, bool kHead, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
-                              const __grid_constant__ CUtensorMap tmSF, const GemmShape g, const GemmArgs a) {
+                              const __grid_constant__ CUtensorMap tmSF, const GemmShape g, const GemmArgs a,
+                              const __grid_constant__ NormRopeArgs nr) {
   using C = K1PairCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -815,10 +911,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
     int acc = 0;
     uint32_t acc_phase = 0;
+    FusedWork fw;
+    const long long n_tasks = kFused ? nrp::task_count(nr, kFusedHeadGroup) : 0;
+    const uint64_t once = kFused ? nrp::evict_first_policy() : 0;
     for (int tile = pair; tile < num_tiles; tile += n_pairs) {
       int m_blk, n_blk;
       tile_coords(g, tile, m_blk, n_blk);
-      bool ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs);
+      bool ok;
+      if constexpr (kFused)
+        ok = fused_wait_acc(smem_u32(&tfull[acc]), acc_phase, abort_flag, nr, n_tasks, fw, once);
+      else
+        ok = mbar_wait_bounded(smem_u32(&tfull[acc]), acc_phase, abort_flag, kWaitLimitNs);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) {
         if (lane == 0) record_failure(a.status, abort_flag, kErrEpilogueTmemFullWait);
@@ -842,6 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc_phase ^= 1u;
       }
     }
+    if constexpr (kFused) fused_finish(nr, n_tasks, fw, abort_flag, a.status, once);
     __syncwarp();
   }
 
@@ -870,11 +974,12 @@ cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUte
   return cudaGetLastError();
 }
 
-template <int BN, bool kHead>
+template <int BN, bool kHead, bool kFused>
 cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
-                               const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms) {
+                               const CUtensorMap& tmSF, const GemmArgs& a, const NormRopeArgs& nr, cudaStream_t s,
+                               int num_sms) {
   using C = K1PairCfg<BN>;
-  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kHead>;
+  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kHead, kFused>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
@@ -893,7 +998,7 @@ cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, tmSF, g, a);
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, tmSF, g, a, nr);
 }
 
 }  // namespace

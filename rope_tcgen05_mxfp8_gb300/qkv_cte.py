@@ -37,6 +37,7 @@ QKV_CTE_FLAG_PROFILE = 0x2
 QKV_CTE_FLAG_SERIAL_PASSES = 0x4
 QKV_CTE_FLAG_GEMM_CTA_PAIR = 0x8
 QKV_CTE_FLAG_GEMM_SINGLE_CTA = 0x10
+QKV_CTE_FLAG_NORM_IN_GEMM = 0x20
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
             "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",
@@ -69,7 +70,7 @@ class qkv_cte_plan_info(ctypes.Structure):
         ("n_tiles", ctypes.c_int32),
         ("n_bands", ctypes.c_int32),
         ("cta_pair", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("norm_in_gemm", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
     ]
 

@@ -116,6 +116,28 @@ def test_per_head_norm_rejects_heads_no_tile_holds():
     assert ei.value.code == q.QKV_CTE_ERR_UNSUPPORTED and "whole heads" in str(ei.value)
 
 
+def test_norm_runs_in_the_gemm_only_on_request():
+    F = q.QKV_CTE_FLAG_NORM_IN_GEMM
+    cases = (
+        (dict(tokens=1000), 0),                                   # default: its own kernel
+        (dict(tokens=1000, flags=F), 1),
+        (dict(tokens=1000, flags=F | q.QKV_CTE_FLAG_SERIAL_PASSES), 0),
+        (dict(tokens=1000, flags=F | q.QKV_CTE_FLAG_GEMM_SINGLE_CTA), 0),
+        (dict(tokens=100, flags=F), 0),                           # one 128-row block: single-CTA form
+        (dict(tokens=1000, norm=0, rope=0, flags=F), 0),          # nothing to run
+        (dict(tokens=1000, norm=2, flags=F), 0),                  # per head: finished in the epilogue itself
+        (dict(tokens=1000, norm=0, rope=1, flags=F), 1),
+    )
+    for kw, expect in cases:
+        args = dict(hidden=512, n_q_heads=4, n_kv_heads=4, d_head=128)
+        args.update(kw)
+        plan, ws = q.qkv_cte_plan(q.make_desc(**args))
+        try:
+            assert q.qkv_cte_get_plan_info(plan).norm_in_gemm == expect, kw
+        finally:
+            q.qkv_cte_destroy(plan)
+
+
 def test_per_head_norm_has_no_hand_off():
     """The per-head kinds finish in the GEMM epilogue: no Q/K hand-off in the workspace."""
     T = 1000

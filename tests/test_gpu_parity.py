@@ -331,3 +331,72 @@ def test_d_head_48_plain_projection():
     call = wl.custom_call(name="d48_plain", tokens=257, hidden=384, n_q_heads=3, n_kv_heads=2, d_head=48,
                           norm=0, rope=0, seed=81, has_w_col_scale=True)
     _case(call)
+
+
+# --- the norm/RoPE work inside the GEMM's epilogue warps (on request) vs its own kernel
+
+@pytest.mark.parametrize("name", ["edge", "short"])
+def test_norm_in_gemm_and_separate_pass_agree(name):
+    """With QKV_CTE_FLAG_NORM_IN_GEMM the pair GEMM runs the norm/RoPE tasks in its
+    epilogue warps; by default the same work is a kernel of its own overlapped with
+    the GEMM. Both are correct and agree to rounding."""
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_NORM_IN_GEMM
+
+    if name == "edge":
+        call = wl.custom_call(name="fuse_edge", tokens=1000, hidden=1024, n_q_heads=3, n_kv_heads=2, d_head=128,
+                              seed=79, has_w_col_scale=True)
+    else:
+        call = wl.workload("short")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op_f, out_f, ss_f, inv_f = run_path(call, g, flags=QKV_CTE_FLAG_NORM_IN_GEMM)
+    op_s, out_s, ss_s, inv_s = run_path(call, g)
+    assert op_f.info.norm_in_gemm == 1 and op_s.info.norm_in_gemm == 0
+    op_f.status()
+    op_s.status()
+    check_outputs(call, inp, out_f, ss_f, inv_f, name=f"{name}_in_gemm")
+    check_outputs(call, inp, out_s, ss_s, inv_s, name=f"{name}_separate")
+    assert_same_to_rounding(call, out_f, out_s, name=f"{name}_in_gemm_vs_separate")
+
+
+def test_norm_in_gemm_wan480p_sampled():
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_NORM_IN_GEMM
+
+    call = wl.workload("wan480p")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_NORM_IN_GEMM)
+    op.status()
+    check_outputs(call, inp, out, ss, inv, rows=sampled_rows(call), name="in_gemm_wan480p")
+
+
+@pytest.mark.parametrize("norm,rope", [(1, 0), (0, 1)])
+def test_norm_in_gemm_partial_work(norm, rope):
+    """Norm without RoPE and RoPE without norm through the in-GEMM tasks, NBSd output."""
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_NORM_IN_GEMM
+
+    call = wl.custom_call(name=f"fuse_n{norm}_r{rope}", tokens=700, hidden=512, n_q_heads=4, n_kv_heads=2,
+                          d_head=64, norm=norm, rope=rope, seed=83 + norm, has_w_col_scale=True)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_NORM_IN_GEMM, nbsd=True)
+    assert op.info.norm_in_gemm == 1
+    op.status()
+    check_outputs(call, inp, out, ss, inv, name=call.name)
+
+
+def test_norm_in_gemm_bounded_wait_reports_timeout():
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_NORM_IN_GEMM
+
+    call = wl.workload("tiny")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_GEMM_CTA_PAIR |
+                                QKV_CTE_FLAG_NORM_IN_GEMM)
+    assert op.info.norm_in_gemm == 1
+    with pytest.raises(QkvCteError) as ei:
+        op.status()
+    assert ei.value.code == QKV_CTE_ERR_DEVICE_TIMEOUT
+    op2, out2, ss2, inv2 = run_path(call, g, flags=QKV_CTE_FLAG_NORM_IN_GEMM)
+    op2.status()
+    check_outputs(call, inp, out2, ss2, inv2, name="in_gemm_after_timeout")
