@@ -60,6 +60,7 @@ def _args():
     p.add_argument("--norm", choices=["across", "head_rms", "head_layer"], default="across",
                    help="qk-norm: across heads (Wan), or the per-head RMS / LayerNorm finished in the GEMM epilogue")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-chunk", type=int, default=0, help="row chunk of the host-streaming e2e leg (0: the library's 2048)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
     p.add_argument("--cpu-rows", type=int, default=4096, help="oracle row sample for cpu_baseline")
@@ -385,6 +386,9 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
+        # End to end through the host-streaming entry point: the step's activations
+        # come from pinned host memory and all of O goes back to pinned host memory,
+        # in row chunks with the copies overlapped with the computation.
         A_h = a_host.pin_memory()
         s_h = inp["a_scale"].pin_memory() if args.input == "fp8" else None
         O_h = torch.empty(call.tokens, call.width, dtype=torch.bfloat16).pin_memory()
@@ -394,11 +398,8 @@ def run_ours(args):
             if not args.no_flush:
                 flush.zero_()
             e0.record(stream)
-            a_in.copy_(A_h, non_blocking=True)
-            if s_h is not None:
-                a_scale_in.copy_(s_h, non_blocking=True)
-            step()
-            O_h.copy_(out, non_blocking=True)
+            op.run_host(A_h, s_h, g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"], O_h,
+                        w_col_scale=g["w_col_scale"], sumsq=sumsq, chunk_rows=args.e2e_chunk, stream=stream)
             e1.record(stream)
             if i >= args.warmup:
                 e2e_ev.append((e0, e1))
@@ -410,8 +411,10 @@ def run_ours(args):
                                          + (s_h.numel() * s_h.element_size() if s_h is not None else 0)),
                "d2h_bytes_per_step": int(O_h.numel() * O_h.element_size()),
                "ms_per_step": e2e_ms / args.steps,
-               "note": f"pinned host input ({_INPUT_NOTE[args.input]}) in, full bf16 O out, through the C ABI"}
-        op.status(stream)
+               "chunk_rows": args.e2e_chunk or 2048,
+               "note": (f"qkv_cte_run_host: pinned host input ({_INPUT_NOTE[args.input]}) in, full bf16 O out, "
+                        "row chunks with upload / compute / readback overlapped")}
+        op.host_status(stream)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

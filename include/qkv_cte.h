@@ -260,6 +260,35 @@ int qkv_cte_unpack_rows(const uint8_t* packed, int64_t tokens, int32_t hidden, u
 int qkv_cte_interleaved_to_rotate_half(const void* src, void* dst, int64_t rows, int64_t row_bytes,
                                        int32_t n_q_heads, int32_t n_kv_heads, int32_t d_head, void* stream);
 
+/* qkv_cte_run on activations in pinned HOST memory, writing O to pinned host memory,
+ * with the copies overlapped with the computation. Rows are independent, so the
+ * tokens are cut into chunks of `chunk_rows` (0: 2048; rounded up to a multiple of
+ * 256) and three streams are pipelined: the upload of chunk i+1 (an internal stream),
+ * the path on chunk i (on `stream`) and the readback of chunk i-1 (an internal
+ * stream), through two staging slots in `scratch`. The call is stream-ordered: work
+ * enqueued on `stream` afterwards sees all of O written to the host.
+ *
+ * A_host       : pinned host, [T, H] e4m3 codes, [T, H+4] packed rows or [T, H] bf16 (desc.input_layout)
+ * a_scale_host : pinned host fp32 [T] with separate FP8 rows, else NULL
+ * W .. sin_table: DEVICE tensors as for qkv_cte_run (weights and tables stay resident)
+ * O_host       : pinned host output, [T, I] or [I/d_head, T, d_head] (desc.output_layout)
+ * sumsq, inv_rms: DEVICE [T, 2] or NULL, as for qkv_cte_run
+ * scratch      : device memory of qkv_cte_host_scratch_bytes(plan, chunk_rows); 256-byte
+ *                aligned; its first word is the status word qkv_cte_status reads (the OR of
+ *                every chunk's status)
+ * Returns 0, -1, -2 (host memory not pinned, alignment), -3 or -4. A plan used here
+ * keeps two streams and a plan per chunk size until qkv_cte_destroy; calls on one plan
+ * must not overlap. */
+int qkv_cte_run_host(qkv_cte_plan_t plan, const void* A_host, const float* a_scale_host, const uint8_t* W,
+                     const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias,
+                     const uint16_t* gamma_q, const uint16_t* gamma_k, const float* cos_table,
+                     const float* sin_table, uint16_t* O_host, float* sumsq, float* inv_rms, void* scratch,
+                     size_t scratch_bytes, int32_t chunk_rows, void* stream);
+
+/* Device scratch bytes qkv_cte_run_host needs for `plan` and `chunk_rows` (0 for an
+ * empty problem). Host only (creates the per-chunk plans). Returns 0 or -1/-2. */
+int qkv_cte_host_scratch_bytes(qkv_cte_plan_t plan, int32_t chunk_rows, size_t* bytes);
+
 /* Size of the scratch array behind qkv_cte_run_noalloc: 16 MiB on every GPU that
  * loads the library, held until the process exits. */
 #define QKV_CTE_NOALLOC_SCRATCH_BYTES (16u << 20)

@@ -14,5 +14,6 @@ from .qkv_cte import (  # noqa: F401
     QKV_CTE_MODE_FUSED, QKV_CTE_MODE_SEPARATE, QKV_CTE_NOALLOC_SCRATCH_BYTES, QKV_CTE_OK, QkvCte, QkvCteError, library_path, load,
     make_desc, qkv_cte_desc, qkv_cte_destroy, qkv_cte_get_plan_info, qkv_cte_last_error, qkv_cte_pass_times, qkv_cte_plan, qkv_cte_run, qkv_cte_run_noalloc,
     qkv_cte_row_quantize, qkv_cte_unpack_rows, qkv_cte_interleaved_to_rotate_half,
+    qkv_cte_run_host, qkv_cte_host_scratch_bytes,
     qkv_cte_status, qkv_cte_version,
 )

@@ -197,6 +197,9 @@ cudaError_t launch_gemm_fused(const GemmShape& g, const CUtensorMap& tmA, const 
 // K1 runs and take each row panel as soon as K1 marks it ready.
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap);
 
+// dst |= src on the stream (qkv_gemm_mxf8.cu): the status of a run made of chunks.
+cudaError_t launch_status_or(const uint32_t* src, uint32_t* dst, cudaStream_t s);
+
 // The producer step (row_quant.cu): bf16 [T, H] -> e4m3 codes [T, H] + fp32 scales [T]
 // and/or packed [T, H + 4] rows (either output may be null, not both); H % 16 == 0.
 cudaError_t launch_row_quantize(const uint16_t* X, int T, int H, uint8_t* codes, float* scale, uint8_t* packed,

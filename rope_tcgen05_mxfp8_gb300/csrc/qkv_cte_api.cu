@@ -30,6 +30,15 @@ struct qkv_cte_plan_s {
   bool second_pass = false;  // the norm/RoPE work runs (across-heads norm, or RoPE alone)
   bool fused_norm = false;   // ... inside the CTA-pair GEMM's epilogue warps
   const void* last_workspace = nullptr;
+  // qkv_cte_run_host: plans for one chunk and for the shorter last chunk, the copy
+  // streams and the events that order staging buffers (created on first use)
+  qkv_cte_plan_s* chunk_plan = nullptr;
+  qkv_cte_plan_s* tail_plan = nullptr;
+  int chunk_rows = 0;
+  int host_device = -1;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t ev_start = nullptr;
+  cudaEvent_t ev_in[2] = {nullptr, nullptr}, ev_done[2] = {nullptr, nullptr}, ev_out[2] = {nullptr, nullptr};
 };
 
 namespace {
@@ -278,6 +287,13 @@ void qkv_cte_destroy(qkv_cte_plan_t plan) {
   if (plan == nullptr) return;
   for (cudaEvent_t e : plan->ev)
     if (e != nullptr) cudaEventDestroy(e);
+  qkv_cte_destroy(plan->chunk_plan);
+  qkv_cte_destroy(plan->tail_plan);
+  for (cudaEvent_t e : {plan->ev_start, plan->ev_in[0], plan->ev_in[1], plan->ev_done[0], plan->ev_done[1],
+                        plan->ev_out[0], plan->ev_out[1]})
+    if (e != nullptr) cudaEventDestroy(e);
+  if (plan->h2d != nullptr) cudaStreamDestroy(plan->h2d);
+  if (plan->d2h != nullptr) cudaStreamDestroy(plan->d2h);
   delete plan;
 }
 
@@ -592,6 +608,217 @@ int qkv_cte_interleaved_to_rotate_half(const void* src, void* dst, int64_t rows,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Host-streaming entry point
+//
+// The activations come from (and the output goes to) pinned host memory. Rows are
+// independent, so the call cuts them into chunks and pipelines three streams: the
+// upload of chunk i+1, the path on chunk i (on the caller's stream) and the readback
+// of chunk i-1, with two staging slots on the device ordered by events. On Grace the
+// link moves ~0.2 TB/s each way, so at the Wan shapes the readback of O bounds the
+// call and the upload and the computation hide under it.
+// ---------------------------------------------------------------------------
+
+namespace {
+
+int input_row_bytes(const qkv_cte_desc& d) {
+  if (d.input_layout == QKV_CTE_INPUT_PACKED) return d.hidden + 4;
+  if (d.input_layout == QKV_CTE_INPUT_BF16) return 2 * d.hidden;
+  return d.hidden;
+}
+
+int effective_chunk_rows(const qkv_cte_plan_s* p, int32_t chunk_rows) {
+  // default: 2048 rows (measured at 480p: 5.55 ms per call, against 5.68 with 4096 and
+  // 5.96 with 8192; the readback of O alone takes ~5.2 ms)
+  long long r = chunk_rows > 0 ? chunk_rows : 2048;
+  r = (r + 255) / 256 * 256;  // whole 256-row tiles of the CTA-pair GEMM
+  if (r > p->g.T) r = p->g.T;
+  return static_cast<int>(r);
+}
+
+struct HostScratch {
+  size_t status, a[2], s[2], o[2], ws, total;
+};
+
+HostScratch host_scratch_layout(const qkv_cte_plan_s* p, int rows, size_t chunk_ws) {
+  HostScratch h;
+  h.status = 0;
+  size_t off = 256;
+  const size_t a_bytes = align_up((size_t)rows * input_row_bytes(p->d), 256);
+  const size_t s_bytes = align_up((size_t)rows * sizeof(float), 256);
+  const size_t o_bytes = align_up((size_t)rows * p->g.I * sizeof(uint16_t), 256);
+  for (int i = 0; i < 2; ++i) {
+    h.a[i] = off;
+    off += a_bytes;
+    h.s[i] = off;
+    off += s_bytes;
+    h.o[i] = off;
+    off += o_bytes;
+  }
+  h.ws = off;
+  h.total = off + align_up(chunk_ws, 256);
+  return h;
+}
+
+// The plans for chunks of `rows` tokens (and the tail), created once per chunk size.
+int ensure_chunk_plans(qkv_cte_plan_s* p, int rows) {
+  if (p->chunk_plan != nullptr && p->chunk_rows == rows) return QKV_CTE_OK;
+  qkv_cte_destroy(p->chunk_plan);
+  qkv_cte_destroy(p->tail_plan);
+  p->chunk_plan = p->tail_plan = nullptr;
+  p->chunk_rows = 0;
+  qkv_cte_desc cd = p->d;
+  cd.flags &= ~QKV_CTE_FLAG_PROFILE;
+  cd.tokens = rows;
+  size_t ws = 0;
+  int rc = qkv_cte_plan(&p->chunk_plan, &cd, &ws);
+  if (rc != QKV_CTE_OK) return rc;
+  const int tail = p->g.T % rows;
+  if (tail != 0) {
+    cd.tokens = tail;
+    rc = qkv_cte_plan(&p->tail_plan, &cd, &ws);
+    if (rc != QKV_CTE_OK) return rc;
+  }
+  p->chunk_rows = rows;
+  return QKV_CTE_OK;
+}
+
+int ensure_host_streams(qkv_cte_plan_s* p) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (p->h2d != nullptr) {
+    if (p->host_device != dev) return fail(QKV_CTE_ERR_INVALID, "a plan used with host buffers must stay on one device");
+    return QKV_CTE_OK;
+  }
+  e = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking);
+  for (cudaEvent_t* ev : {&p->ev_start, &p->ev_in[0], &p->ev_in[1], &p->ev_done[0], &p->ev_done[1], &p->ev_out[0],
+                          &p->ev_out[1]})
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "stream/event creation: %s", cudaGetErrorString(e));
+  p->host_device = dev;
+  return QKV_CTE_OK;
+}
+
+bool pinned_host(const void* ptr) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
+}  // namespace
+
+extern "C" int qkv_cte_host_scratch_bytes(qkv_cte_plan_t plan, int32_t chunk_rows, size_t* bytes) {
+  if (plan == nullptr || bytes == nullptr) return fail(QKV_CTE_ERR_INVALID, "null argument");
+  *bytes = 0;
+  if (plan->g.T == 0) return ok();
+  const int rows = effective_chunk_rows(plan, chunk_rows);
+  const int rc = ensure_chunk_plans(plan, rows);
+  if (rc != QKV_CTE_OK) return rc;
+  *bytes = host_scratch_layout(plan, rows, plan->chunk_plan->ws.total).total;
+  return ok();
+}
+
+extern "C" int qkv_cte_run_host(qkv_cte_plan_t plan, const void* A_host, const float* a_scale_host, const uint8_t* W,
+                                const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias,
+                                const uint16_t* gamma_q, const uint16_t* gamma_k, const float* cos_table,
+                                const float* sin_table, uint16_t* O_host, float* sumsq, float* inv_rms, void* scratch,
+                                size_t scratch_bytes, int32_t chunk_rows, void* stream) {
+  if (plan == nullptr) return fail(QKV_CTE_ERR_INVALID, "null plan");
+  const qkv_cte_desc& d = plan->d;
+  const int T = plan->g.T;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (scratch != nullptr) {
+      cudaError_t e = cudaMemsetAsync(scratch, 0, sizeof(uint32_t), s);
+      if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
+    }
+    return ok();
+  }
+  const bool row_fp8 = d.input_layout == QKV_CTE_INPUT_ROW_FP8;
+  if (!A_host || !O_host || !scratch) return fail(QKV_CTE_ERR_INVALID, "A_host, O_host and scratch are required");
+  if (row_fp8 != (a_scale_host != nullptr))
+    return fail(QKV_CTE_ERR_INVALID, "a_scale_host is required with separate FP8 rows and must be NULL otherwise");
+  if (!pinned_host(A_host) || !pinned_host(O_host) || (a_scale_host && !pinned_host(a_scale_host)))
+    return fail(QKV_CTE_ERR_UNSUPPORTED,
+                "A_host, a_scale_host and O_host must be pinned host memory (cudaHostAlloc / cudaHostRegister)");
+  if (!aligned(scratch, 256)) return fail(QKV_CTE_ERR_UNSUPPORTED, "scratch must be 256-byte aligned");
+  const int rows = effective_chunk_rows(plan, chunk_rows);
+  int rc = ensure_chunk_plans(plan, rows);
+  if (rc != QKV_CTE_OK) return rc;
+  const HostScratch hs = host_scratch_layout(plan, rows, plan->chunk_plan->ws.total);
+  if (scratch_bytes < hs.total)
+    return fail(QKV_CTE_ERR_INVALID, "scratch of %zu bytes is smaller than the %zu this chunk size needs",
+                scratch_bytes, hs.total);
+  if ((rc = ensure_host_streams(plan)) != QKV_CTE_OK) return rc;
+
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  uint32_t* status = reinterpret_cast<uint32_t*>(sc + hs.status);
+  const size_t in_row = (size_t)input_row_bytes(d);
+  const int I = plan->g.I;
+  const int dh = d.d_head;
+  const bool nbsd = d.output_layout == QKV_CTE_LAYOUT_NBSD;
+  const int heads = I / dh;
+  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+  if (e == cudaSuccess) e = cudaEventRecord(plan->ev_start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->h2d, plan->ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->d2h, plan->ev_start, 0);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "stream ordering: %s", cudaGetErrorString(e));
+  const int chunks = (T + rows - 1) / rows;
+  for (int i = 0; i < chunks; ++i) {
+    const int slot = i & 1;
+    const int r0 = i * rows;
+    const int n = T - r0 < rows ? T - r0 : rows;
+    qkv_cte_plan_s* cp = n == rows ? plan->chunk_plan : plan->tail_plan;
+    uint8_t* a_dev = sc + hs.a[slot];
+    float* s_dev = reinterpret_cast<float*>(sc + hs.s[slot]);
+    uint16_t* o_dev = reinterpret_cast<uint16_t*>(sc + hs.o[slot]);
+    // upload: the slot is free once the path on chunk i-2 has read it
+    if (i >= 2) e = cudaStreamWaitEvent(plan->h2d, plan->ev_done[slot], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(a_dev, static_cast<const uint8_t*>(A_host) + (size_t)r0 * in_row, (size_t)n * in_row,
+                          cudaMemcpyHostToDevice, plan->h2d);
+    if (e == cudaSuccess && row_fp8)
+      e = cudaMemcpyAsync(s_dev, a_scale_host + r0, (size_t)n * sizeof(float), cudaMemcpyHostToDevice, plan->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(plan->ev_in[slot], plan->h2d);
+    // the path on this chunk, on the caller's stream, once its rows are in and the
+    // output slot's previous readback (chunk i-2) is done
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, plan->ev_in[slot], 0);
+    if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(s, plan->ev_out[slot], 0);
+    if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "chunk %d upload: %s", i, cudaGetErrorString(e));
+    rc = qkv_cte_run(cp, a_dev, row_fp8 ? s_dev : nullptr, W, w_sf, w_col_scale, bias, gamma_q, gamma_k,
+                     cos_table ? cos_table + (size_t)r0 * dh : nullptr, sin_table ? sin_table + (size_t)r0 * dh : nullptr,
+                     o_dev, sumsq ? sumsq + 2 * (size_t)r0 : nullptr, inv_rms ? inv_rms + 2 * (size_t)r0 : nullptr,
+                     sc + hs.ws, hs.total - hs.ws, s);
+    if (rc != QKV_CTE_OK) return rc;
+    e = launch_status_or(reinterpret_cast<const uint32_t*>(sc + hs.ws), status, s);
+    if (e == cudaSuccess) e = cudaEventRecord(plan->ev_done[slot], s);
+    // readback of the chunk's output
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(plan->d2h, plan->ev_done[slot], 0);
+    if (e == cudaSuccess) {
+      if (!nbsd) {
+        e = cudaMemcpyAsync(O_host + (size_t)r0 * I, o_dev, (size_t)n * I * sizeof(uint16_t), cudaMemcpyDeviceToHost,
+                            plan->d2h);
+      } else {  // NBSd: each head's rows of this chunk go to that head's block of O
+        e = cudaMemcpy2DAsync(O_host + (size_t)r0 * dh, (size_t)T * dh * sizeof(uint16_t), o_dev,
+                              (size_t)n * dh * sizeof(uint16_t), (size_t)n * dh * sizeof(uint16_t), heads,
+                              cudaMemcpyDeviceToHost, plan->d2h);
+      }
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(plan->ev_out[slot], plan->d2h);
+    if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "chunk %d readback: %s", i, cudaGetErrorString(e));
+  }
+  // the caller's stream resumes once every readback is done
+  e = cudaStreamWaitEvent(s, plan->ev_out[(chunks - 1) & 1], 0);
+  if (e == cudaSuccess && chunks > 1) e = cudaStreamWaitEvent(s, plan->ev_out[chunks & 1], 0);
+  if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "stream ordering: %s", cudaGetErrorString(e));
+  return ok();
+}
 
 // ---------------------------------------------------------------------------
 // Allocation-free entry point

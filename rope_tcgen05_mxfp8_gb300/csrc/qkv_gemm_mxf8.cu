@@ -48,7 +48,17 @@ __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __re
   }
 }
 
+// dst |= src: one chunk's status word into the status word of a run made of chunks.
+__global__ void status_or_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst) {
+  if (threadIdx.x == 0) *dst |= *src;
+}
+
 }  // namespace
+
+cudaError_t launch_status_or(const uint32_t* src, uint32_t* dst, cudaStream_t s) {
+  status_or_kernel<<<1, 32, 0, s>>>(src, dst);
+  return cudaGetLastError();
+}
 
 bool gemm_tile_supported(int tile_n) {
   return tile_n == 128 || tile_n == 192 || tile_n == 240 || tile_n == 256;

@@ -41,7 +41,8 @@ QKV_CTE_FLAG_NORM_IN_GEMM = 0x20
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
             "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",
-            "qkv_cte_row_quantize", "qkv_cte_unpack_rows", "qkv_cte_interleaved_to_rotate_half")
+            "qkv_cte_row_quantize", "qkv_cte_unpack_rows", "qkv_cte_interleaved_to_rotate_half",
+            "qkv_cte_run_host", "qkv_cte_host_scratch_bytes")
 QKV_CTE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -113,6 +114,10 @@ def load() -> ctypes.CDLL:
     lib.qkv_cte_interleaved_to_rotate_half.argtypes = [P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
                                                        ctypes.c_int32, ctypes.c_int32, P]
     lib.qkv_cte_interleaved_to_rotate_half.restype = ctypes.c_int
+    lib.qkv_cte_run_host.argtypes = [P] * 15 + [ctypes.c_size_t, ctypes.c_int32, P]
+    lib.qkv_cte_run_host.restype = ctypes.c_int
+    lib.qkv_cte_host_scratch_bytes.argtypes = [P, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.qkv_cte_host_scratch_bytes.restype = ctypes.c_int
     lib.qkv_cte_status.argtypes = [P, P]
     lib.qkv_cte_status.restype = ctypes.c_int
     lib.qkv_cte_pass_times.argtypes = [P, ctypes.POINTER(ctypes.c_float)]
@@ -272,6 +277,35 @@ def qkv_cte_interleaved_to_rotate_half(src, n_q_heads, n_kv_heads, d_head, dst=N
     return dst
 
 
+def _host_ptr(name: str, t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name}: expected a pinned CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def qkv_cte_host_scratch_bytes(plan, chunk_rows=0) -> int:
+    n = ctypes.c_size_t()
+    _check(load().qkv_cte_host_scratch_bytes(plan, chunk_rows, ctypes.byref(n)))
+    return n.value
+
+
+def qkv_cte_run_host(plan, A_host, a_scale_host, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos, sin, O_host,
+                     sumsq, inv_rms, scratch, chunk_rows=0, stream=None) -> int:
+    """The path on pinned host activations, writing O to pinned host memory, with the
+    copies overlapped with the computation (see qkv_cte.h)."""
+    ws_bytes = scratch.numel() * scratch.element_size() if scratch is not None else 0
+    args = [_host_ptr("A_host", A_host), _host_ptr("a_scale_host", a_scale_host), _ptr("W", W), _ptr("w_sf", w_sf),
+            _ptr("w_col_scale", w_col_scale), _ptr("bias", bias), _ptr("gamma_q", gamma_q),
+            _ptr("gamma_k", gamma_k), _ptr("cos", cos), _ptr("sin", sin), _host_ptr("O_host", O_host),
+            _ptr("sumsq", sumsq), _ptr("inv_rms", inv_rms), _ptr("workspace", scratch)]
+    return _check(load().qkv_cte_run_host(plan, *args, ctypes.c_size_t(ws_bytes), chunk_rows,
+                                          _stream_handle(stream)))
+
+
 def qkv_cte_status(workspace, stream=None) -> int:
     """Synchronise the stream and raise QkvCteError if a bounded device wait ran out."""
     if stream is None:
@@ -317,6 +351,20 @@ class QkvCte:
         qkv_cte_run(self.plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos, sin, out,
                     sumsq, inv_rms, self.workspace, stream)
         return out
+
+    def run_host(self, A_host, a_scale_host, W, w_sf, bias, gamma_q, gamma_k, cos, sin, O_host, w_col_scale=None,
+                 sumsq=None, inv_rms=None, chunk_rows=0, stream=None):
+        """qkv_cte_run_host with a scratch buffer kept per chunk size."""
+        n = qkv_cte_host_scratch_bytes(self.plan, chunk_rows)
+        if getattr(self, "_host_scratch", None) is None or self._host_scratch.numel() < max(n, 256):
+            dev = self.workspace.device
+            self._host_scratch = torch.zeros(max(n, 256), dtype=torch.uint8, device=dev)
+        qkv_cte_run_host(self.plan, A_host, a_scale_host, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos, sin,
+                         O_host, sumsq, inv_rms, self._host_scratch, chunk_rows, stream)
+        return O_host
+
+    def host_status(self, stream=None):
+        return qkv_cte_status(self._host_scratch, stream)
 
     def status(self, stream=None):
         return qkv_cte_status(self.workspace, stream)

@@ -65,8 +65,7 @@ def check_outputs(call, inp, out, sumsq, inv, rows=None, name="case"):
     """Compare the GPU outputs with the oracle on `rows` (all rows when None)."""
     ref = O.qkv_cte_from_inputs(call, inp, rows=rows)
     idx = torch.arange(call.tokens) if rows is None else torch.as_tensor(rows)
-    idx_dev = idx.to(out.device)
-    got = out.index_select(0, idx_dev).float().cpu().double().numpy()
+    got = out.index_select(0, idx.to(out.device)).float().cpu().double().numpy()
     r = ref["O"]
     err = np.abs(got - r)
     bad = ~(err <= REL * np.abs(r) + ABS)      # NaN in got counts as bad
@@ -79,14 +78,14 @@ def check_outputs(call, inp, out, sumsq, inv, rows=None, name="case"):
         raise AssertionError(msg + _diag(name, got, r, bad))
     segs = [0] + ([1] if call.n_kv_heads > 0 else [])
     if sumsq is not None:
-        s = sumsq.index_select(0, idx_dev).cpu().double().numpy()
+        s = sumsq.index_select(0, idx.to(sumsq.device)).cpu().double().numpy()
         for c in segs:
             rel = np.abs(s[:, c] - ref["sumsq"][:, c]) / np.maximum(np.abs(ref["sumsq"][:, c]), 1e-30)
             assert np.all(rel <= SS_REL), f"{name}: sumsq[{c}] max rel err {np.nanmax(rel):.3e}"
         if call.n_kv_heads == 0:
             assert np.all(s[:, 1] == 0), f"{name}: sumsq K column should be 0 without a K segment"
     if inv is not None and call.norm == 1:
-        v = inv.index_select(0, idx_dev).cpu().double().numpy()
+        v = inv.index_select(0, idx.to(inv.device)).cpu().double().numpy()
         for c in segs:
             rel = np.abs(v[:, c] - ref["inv_rms"][:, c]) / np.abs(ref["inv_rms"][:, c])
             assert np.all(rel <= SS_REL), f"{name}: inv_rms[{c}] max rel err {np.nanmax(rel):.3e}"

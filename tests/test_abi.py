@@ -303,3 +303,42 @@ def test_zero_tokens_launches_nothing():
         assert rc == 0
     finally:
         q.qkv_cte_destroy(plan)
+
+
+def test_host_scratch_bytes_formula():
+    """Two staging slots (input rows, row scales, output rows) plus one chunk's workspace."""
+    T, H, nq, nkv, d = 10000, 512, 4, 4, 128
+    I = (nq + 2 * nkv) * d
+    align = lambda x: -(-x // 256) * 256
+    for layout, in_row in ((0, H), (1, H + 4), (2, 2 * H)):
+        plan, ws = q.qkv_cte_plan(q.make_desc(T, H, nq, nkv, d, input_layout=layout))
+        cplan, cws = q.qkv_cte_plan(q.make_desc(1024, H, nq, nkv, d, input_layout=layout))
+        try:
+            n = q.qkv_cte_host_scratch_bytes(plan, 1000)   # rounded up to 1024 rows
+            slot = align(1024 * in_row) + align(1024 * 4) + align(1024 * I * 2)
+            assert n == 256 + 2 * slot + align(cws)
+            assert q.qkv_cte_host_scratch_bytes(plan, 10 ** 6) > n     # capped at T rows
+        finally:
+            q.qkv_cte_destroy(plan)
+            q.qkv_cte_destroy(cplan)
+
+
+def test_run_host_argument_checks_precede_any_copy():
+    lib = pkg.load()
+    plan, ws = q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, 128))
+    try:
+        P = ctypes.c_void_p
+        f = P(4096)
+        args = [f] * 14
+        args[0] = None
+        rc = lib.qkv_cte_run_host(plan, *args, ctypes.c_size_t(1 << 30), 0, None)
+        assert rc == q.QKV_CTE_ERR_INVALID and "required" in q.qkv_cte_last_error()
+        args = [f] * 14
+        args[1] = None      # separate FP8 rows need their scales
+        rc = lib.qkv_cte_run_host(plan, *args, ctypes.c_size_t(1 << 30), 0, None)
+        assert rc == q.QKV_CTE_ERR_INVALID and "a_scale_host" in q.qkv_cte_last_error()
+        args = [f] * 14     # not pinned host memory (here: no device at all)
+        rc = lib.qkv_cte_run_host(plan, *args, ctypes.c_size_t(1 << 30), 0, None)
+        assert rc == q.QKV_CTE_ERR_UNSUPPORTED and "pinned" in q.qkv_cte_last_error()
+    finally:
+        q.qkv_cte_destroy(plan)
