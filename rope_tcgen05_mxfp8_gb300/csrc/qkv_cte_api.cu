@@ -242,6 +242,10 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   g.m_tiles = g.cta_pair ? (g.T + 255) / 256 : g.blocks128;
   g.n_tiles = (g.I + tile_n - 1) / tile_n;
   g.k_stages = g.H / 128;
+  if ((long long)g.m_tiles * g.n_tiles > INT32_MAX) {
+    delete p;
+    return fail(QKV_CTE_ERR_UNSUPPORTED, "%d x %d output tiles exceed INT32_MAX", g.m_tiles, g.n_tiles);
+  }
   g.sf_chunks = gemm_sf_chunks(tile_n);
   p->q_end = d.n_q_heads * d.d_head;
   p->k_end = p->q_end + d.n_kv_heads * d.d_head;

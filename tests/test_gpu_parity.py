@@ -400,3 +400,43 @@ def test_norm_in_gemm_bounded_wait_reports_timeout():
     op2, out2, ss2, inv2 = run_path(call, g, flags=QKV_CTE_FLAG_NORM_IN_GEMM)
     op2.status()
     check_outputs(call, inp, out2, ss2, inv2, name="in_gemm_after_timeout")
+
+
+# --- degenerate and extreme shapes -------------------------------------------------
+
+@pytest.mark.parametrize("gemm", ["pair", "single"])
+def test_single_k_stage(gemm):
+    """H = 128: one 128-byte K stage per tile (the pipeline ring barely turns)."""
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA
+
+    call = wl.custom_call(name=f"h128_{gemm}", tokens=700, hidden=128, n_q_heads=3, n_kv_heads=2, d_head=128,
+                          seed=91, has_w_col_scale=True)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    flags = QKV_CTE_FLAG_GEMM_CTA_PAIR if gemm == "pair" else QKV_CTE_FLAG_GEMM_SINGLE_CTA
+    op, out, ss, inv = run_path(call, g, flags=flags)
+    op.status()
+    check_outputs(call, inp, out, ss, inv, name=call.name)
+
+
+@pytest.mark.parametrize("norm,rope", [(1, 1), (2, 0), (3, 1)])
+def test_single_head_separate_call(norm, rope):
+    """One Q head, no K/V: the smallest separate-mode call."""
+    call = wl.custom_call(name=f"onehead_n{norm}", tokens=257, hidden=256, n_q_heads=1, n_kv_heads=0, d_head=128,
+                          norm=norm, rope=rope, seed=93 + norm)
+    _case(call)
+
+
+def test_large_token_count_sampled():
+    """131072 tokens at the Wan layout (4x the 480p rows; ~15 GB on the device), on
+    sampled rows: index arithmetic past 2^31 bytes in every buffer."""
+    base = wl.workload("wan480p")[0]
+    call = wl.custom_call(name="t131072", tokens=131072, hidden=base.hidden, n_q_heads=base.n_q_heads,
+                          n_kv_heads=base.n_kv_heads, d_head=base.d_head, rope_grid=(88, 30, 52),
+                          outlier_frac=base.outlier_frac, seed=131)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g)
+    op.status()
+    rows = np.unique(np.concatenate([sampled_rows(call, 2048), [0, call.tokens - 1]]))
+    check_outputs(call, inp, out, ss, inv, rows=rows, name=call.name)
