@@ -26,6 +26,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "fp32x2.cuh"
 #include "internal.h"
 
 namespace qkvcte {
@@ -81,9 +82,9 @@ __device__ __forceinline__ void decode16(const RawChunk& r, float* f) {
   const float up = __uint_as_float(static_cast<uint32_t>(r.e) << 23);  // 2^(e - 127)
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&r.w[j]));
-    f[2 * j] = p.x * up;
-    f[2 * j + 1] = p.y * up;
+    const float2 p = fmul2(__half22float2(*reinterpret_cast<const __half2*>(&r.w[j])), make_float2(up, up));
+    f[2 * j] = p.x;
+    f[2 * j + 1] = p.y;
   }
 }
 
@@ -169,6 +170,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
       inv_k = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr) + 1] / static_cast<float>(p.n_kv * d) + p.eps);
   }
   float cl[16], ch[16], sl[16], sh[16];
+  float nsl[16];  // -sin of the low half: the rotation is one mul and one fma per lane pair
   if (p.rope) {
     const float* cr = p.cos_t + static_cast<size_t>(tr) * d + c * 16;
     const float* sr = p.sin_t + static_cast<size_t>(tr) * d + c * 16;
@@ -180,6 +182,8 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
     load8_nc(sr + 8, sl + 8);
     load8_nc(sr + half, sh);
     load8_nc(sr + half + 8, sh + 8);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) nsl[j] = -sl[j];
   }
   const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (t & 127);
   for (int hg0 = h_begin; hg0 < h_end; hg0 += kHeadBatch) {
@@ -208,24 +212,42 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
       if (p.norm) {
         const uint16_t* gamma = seg ? p.gamma_k : p.gamma_q;
         const float inv = seg ? inv_k : inv_q;
+        const float2 inv2 = make_float2(inv, inv);
         float g[8];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off) + q), g);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) lo[8 * q + j] *= inv * g[j];
+          for (int j = 0; j < 4; ++j) {
+            const float2 y = fmul2(make_float2(lo[8 * q + 2 * j], lo[8 * q + 2 * j + 1]),
+                                   fmul2(inv2, make_float2(g[2 * j], g[2 * j + 1])));
+            lo[8 * q + 2 * j] = y.x;
+            lo[8 * q + 2 * j + 1] = y.y;
+          }
           unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + off + half) + q), g);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) hi[8 * q + j] *= inv * g[j];
+          for (int j = 0; j < 4; ++j) {
+            const float2 y = fmul2(make_float2(hi[8 * q + 2 * j], hi[8 * q + 2 * j + 1]),
+                                   fmul2(inv2, make_float2(g[2 * j], g[2 * j + 1])));
+            hi[8 * q + 2 * j] = y.x;
+            hi[8 * q + 2 * j + 1] = y.y;
+          }
         }
       }
       if (p.rope) {
+        // a = lo*cos_lo - hi*sin_lo, b = hi*cos_hi + lo*sin_hi, two lanes per instruction
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float a = lo[j] * cl[j] - hi[j] * sl[j];
-          const float b = hi[j] * ch[j] + lo[j] * sh[j];
-          lo[j] = a;
-          hi[j] = b;
+        for (int j = 0; j < 8; ++j) {
+          const float2 l2 = make_float2(lo[2 * j], lo[2 * j + 1]);
+          const float2 h2 = make_float2(hi[2 * j], hi[2 * j + 1]);
+          const float2 a = ffma2(h2, make_float2(nsl[2 * j], nsl[2 * j + 1]),
+                                 fmul2(l2, make_float2(cl[2 * j], cl[2 * j + 1])));
+          const float2 b = ffma2(l2, make_float2(sh[2 * j], sh[2 * j + 1]),
+                                 fmul2(h2, make_float2(ch[2 * j], ch[2 * j + 1])));
+          lo[2 * j] = a.x;
+          lo[2 * j + 1] = a.y;
+          hi[2 * j] = b.x;
+          hi[2 * j + 1] = b.y;
         }
       }
       if (row_ok) {

@@ -44,6 +44,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "fp32x2.cuh"
 #include "qk_norm_rope.cuh"
 
 namespace qkvcte {
@@ -329,12 +330,16 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
         for (int j = 0; j < 16; ++j) bias[j] = 0.0f;
       }
       float v[16];
-      float sq = 0.0f;
+      float2 sq2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        v[j] = fmaf(__uint_as_float(r[16 * h + j]), sc[j], bias[j]);
-        sq = fmaf(v[j], v[j], sq);
+      for (int j = 0; j < 8; ++j) {
+        const float2 o = ffma2(make_float2(__uint_as_float(r[16 * h + 2 * j]), __uint_as_float(r[16 * h + 2 * j + 1])),
+                               make_float2(sc[2 * j], sc[2 * j + 1]), make_float2(bias[2 * j], bias[2 * j + 1]));
+        v[2 * j] = o.x;
+        v[2 * j + 1] = o.y;
+        sq2 = ffma2(o, o, sq2);
       }
+      const float sq = sq2.x + sq2.y;
       if (col0 < a.q_end) ss_q += sq; else if (col0 < a.k_end) ss_k += sq;
       if (a.qk_val != nullptr && col0 < a.k_end) {
         // Q/K columns that the norm/RoPE pass will finish: the chunk's exponent
@@ -350,7 +355,10 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
         const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
         uint32_t hv[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) hv[j] = pack_f16x2(v[2 * j] * down, v[2 * j + 1] * down);
+        for (int j = 0; j < 8; ++j) {
+          const float2 x = fmul2(make_float2(v[2 * j], v[2 * j + 1]), make_float2(down, down));
+          hv[j] = pack_f16x2(x.x, x.y);
+        }
         const size_t idx = qk_row_idx + static_cast<size_t>(col0 >> 4) * 128;
         st_global_v8_b32(a.qk_val + idx * 16, hv);
         a.qk_exp[idx] = static_cast<uint8_t>(e + 127);
