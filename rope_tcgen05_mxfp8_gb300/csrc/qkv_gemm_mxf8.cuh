@@ -465,7 +465,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer ----------------
-      const uint64_t pol_stream = policy_evict_first();
+      // A's row panel is read by every CTA working on the band at about the same time:
+      // evict-first let it go before the last reader came (1.70 GB of DRAM reads per
+      // 480p launch instead of 0.64 GB) and cost ~1 % of the GEMM's time
+      const uint64_t pol_stream = policy_evict_normal();
       const uint64_t pol_keep = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
@@ -806,7 +809,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer (both CTAs) ----------------
-      const uint64_t pol_stream = policy_evict_first();
+      // A's row panel is read by every CTA working on the band at about the same time:
+      // evict-first let it go before the last reader came (1.70 GB of DRAM reads per
+      // 480p launch instead of 0.64 GB) and cost ~1 % of the GEMM's time
+      const uint64_t pol_stream = policy_evict_normal();
       const uint64_t pol_keep = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
