@@ -76,9 +76,9 @@ enum { QKV_CTE_MODE_FUSED = 0, QKV_CTE_MODE_SEPARATE = 1 };
  *   HEAD_LAYER   : per head, (x - mean) / sqrt(mean((x - mean)^2) + eps) * gamma, gamma
  *                  [d_head], no bias ([qkv_cte] "Upstream behavior": the per-head RMS_NORM /
  *                  LAYER_NORM fused into the matmul's copy-out).
- * The per-head kinds finish in the GEMM's epilogue (every N tile holds whole heads: the
- * automatic tile_n is one d_head divides) and run no second pass; RoPE is applied after
- * the norm in every kind. */
+ * The per-head kinds are finished by the norm/RoPE pass from per-(row, head) statistics
+ * the GEMM writes (or, with QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE, in the GEMM's epilogue
+ * with tiles of whole heads); RoPE is applied after the norm in every kind. */
 enum { QKV_CTE_NORM_NONE = 0, QKV_CTE_NORM_ACROSS_HEADS = 1, QKV_CTE_NORM_HEAD_RMS = 2, QKV_CTE_NORM_HEAD_LAYER = 3 };
 enum { QKV_CTE_LAYOUT_BSD = 0, QKV_CTE_LAYOUT_NBSD = 1 };
 
@@ -115,6 +115,12 @@ enum { QKV_CTE_INPUT_ROW_FP8 = 0, QKV_CTE_INPUT_PACKED = 1, QKV_CTE_INPUT_BF16 =
  * when the tiles are done runs as a tail). Ignored without the pair form or with
  * QKV_CTE_FLAG_SERIAL_PASSES. */
 #define QKV_CTE_FLAG_NORM_IN_GEMM 0x20u
+/* Per-head norms (QKV_CTE_NORM_HEAD_RMS / _LAYER): finish the norm and RoPE in the GEMM's
+ * epilogue while each tile is in TMEM (tiles of whole heads, no second pass) instead
+ * of the default: the GEMM writes per-(row, head) statistics (RMS: sum of squares;
+ * LayerNorm: each tile part's mean and centred sum of squares) and the norm/RoPE pass
+ * finishes from them, which keeps the GEMM's wide tiles. Same results to rounding. */
+#define QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE 0x40u
 
 /* Problem description ([qkv_cte] "Interface" argument table, flattened to scalars). */
 typedef struct {
@@ -154,7 +160,7 @@ typedef struct {
  * Returns 0, -1 (null pointer, bad head counts, mode/segment mismatch, flag values,
  * unknown input layout) or
  * -2 (H % 128, d_head % 16, d_head % 32 with a norm or RoPE, T > INT32_MAX, unknown tile_n,
- * a per-head norm with a tile_n that d_head does not divide). */
+ * a per-head norm in the epilogue with a tile_n that d_head does not divide). */
 int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspace_bytes);
 
 /* Fill `info` for `plan`. Returns 0 or -1 (null pointer). */

@@ -20,8 +20,8 @@ BUILD = os.path.join(ROOT, "_build")
 LIBDIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libqkvcte.so")
 
-SOURCES = ["qkv_cte_api.cu", "qkv_gemm_mxf8.cu", "qkv_gemm_mxf8_head.cu", "qkv_gemm_mxf8_fused.cu", "qk_norm_rope.cu", "row_quant.cu", "rope_permute.cu"]
-HEADERS = ["ptx.cuh", "internal.h", "qkv_gemm_mxf8.cuh", "qk_norm_rope.cuh", "fp32x2.cuh"]
+SOURCES = ["qkv_cte_api.cu", "qkv_gemm_mxf8.cu", "qkv_gemm_mxf8_head.cu", "qkv_gemm_mxf8_stats.cu", "qkv_gemm_mxf8_fused.cu", "qk_norm_rope.cu", "row_quant.cu", "rope_permute.cu"]
+HEADERS = ["ptx.cuh", "internal.h", "qkv_gemm_mxf8.cuh", "qk_norm_rope.cuh", "fp32x2.cuh", "kernel_kinds.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "-Xcompiler", "-Wformat", "-Xcompiler", "-Werror=format",

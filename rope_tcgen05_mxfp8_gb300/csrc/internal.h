@@ -38,13 +38,15 @@ enum : uint32_t {
 //                            chunk k < k_end/16, idx = (t/128 * k_end/16 + k) * 128
 //                            + t%128; the 16 fp16 sit at qk_val[idx*16 ..] (32 bytes)
 //                            and the exponent at qk_exp[idx]
+//   [.., + stats_bytes)      only for a per-head norm finished by the norm/RoPE pass: the
+//                            per-(row, head) statistics (see GemmArgs::stats_kind)
 //   [.., + T*H), [.., + 4T)  only for a packed or bf16 input: the e4m3 codes [T, H] and
 //                            fp32 row scales [T] the producer step writes for the GEMM
 constexpr size_t kStampOffset = 64;
 constexpr size_t kTaskCounterOffset = 128;  // uint32: next norm/RoPE task the GEMM's epilogue warps claim
 
 struct WorkspaceLayout {
-  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, qk_exp_off, act_off, act_scale_off, total;
+  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, qk_exp_off, stats_off, act_off, act_scale_off, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -134,6 +136,14 @@ struct GemmArgs {
   const uint16_t* gamma_k;   // [d_head] bf16, or null without a K segment
   const float* cos_t;        // [T, d_head] fp32 (rope)
   const float* sin_t;
+  // Per-head norm finished by the norm/RoPE pass: the epilogue writes per-(row, head)
+  // statistics of the un-normalised Q/K. stats_kind 2 (RMS): sum(o^2) per (row, head),
+  // accumulated with atomics (zeroed by prep). stats_kind 3 (LayerNorm): for each of
+  // the stat_parts tiles a head's columns can span, the part's (mean, M2) as a float2
+  // at ((row * heads + head) * stat_parts + part).
+  int stats_kind;
+  float* head_stats;
+  int stat_parts;
 };
 
 // Element (row t, column c) of O in either layout (c and the 16 columns after it
@@ -165,6 +175,12 @@ struct NormRopeArgs {
   unsigned long long* stamps;  // [0] first block start (min), [1] last block end (max)
   uint32_t* status;
   uint32_t* task_next;       // next unclaimed task (the GEMM's epilogue warps claim them)
+  // per-head norm (norm 2 RMS / 3 LayerNorm) from the GEMM's per-(row, head)
+  // statistics (see GemmArgs); 0: the across-heads norm or none
+  int head_kind;
+  const float* head_stats;
+  int stat_parts;
+  int tile_n;
 };
 
 // Supported N tiles (compile-time instantiations of K1).
@@ -175,7 +191,8 @@ size_t gemm_smem_bytes(int tile_n);
 // Launchers. Each returns cudaSuccess or the launch error.
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
                         size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
-                        uint32_t* task_next, cudaStream_t s, int num_sms);
+                        uint32_t* task_next, float* zero_extra, size_t zero_extra_count, cudaStream_t s,
+                        int num_sms);
 // K1. tmSF: the repacked scales as a uint32 [n_tiles * k_stages, sf_chunks * 128] map
 // with one-row boxes (used by the CTA-pair kernel). With `fused` (CTA-pair form only)
 // the epilogue warps also run the norm/RoPE tasks of `*fused` between tiles, and no
@@ -183,8 +200,8 @@ cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_pac
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                         const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms,
                         const NormRopeArgs* fused);
-// K1 with the per-head qk-norm epilogue (qkv_gemm_mxf8_head.cu); launch_gemm calls it
-// when a.head_norm != 0.
+// K1 with the per-head qk-norm epilogue, or with the per-head statistics epilogue
+// (qkv_gemm_mxf8_head.cu); launch_gemm calls it when a.head_norm or a.stats_kind is set.
 cudaError_t launch_gemm_head(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                              const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms);
 // K1 (CTA-pair form) with the norm/RoPE tasks run by its epilogue warps

@@ -16,6 +16,7 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kHeadGroup = 20;  // heads per warp task: small tasks keep the warps evenly loaded to the end
 
+template <bool kHeadStats>
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_constant__ NormRopeArgs p) {
   if (threadIdx.x == 0) atomicMin(&p.stamps[0], nrp::now_ns());
   const int lane = threadIdx.x & 31;
@@ -34,7 +35,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       if (lane == 0) atomicOr(p.status, kErrNormReadyWait);
       break;
     }
-    nrp::run_task(p, task, kHeadGroup, once);
+    nrp::run_task<kHeadStats>(p, task, kHeadGroup, once);
   }
   if (threadIdx.x == 0) atomicMax(&p.stamps[1], nrp::now_ns());
 }
@@ -50,11 +51,11 @@ cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms,
   // (registers are the limit) so every block finds its tasks as their panels
   // complete. That sizing only affects speed: the GEMM never waits for this kernel.
   // Alone, the pass takes every SM it can hold.
+  const auto kernel = a.head_kind != 0 ? qk_norm_rope_kernel<true> : qk_norm_rope_kernel<false>;
   int per_sm = 1;
   if (!overlap) {
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, qk_norm_rope_kernel, kThreads, 0) == cudaSuccess &&
-        occ > per_sm)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) == cudaSuccess && occ > per_sm)
       per_sm = occ;
   }
   long long blocks = (tasks + kThreads / 32 - 1) / (kThreads / 32);
@@ -69,7 +70,7 @@ cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, qk_norm_rope_kernel, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace qkvcte

@@ -139,7 +139,48 @@ __device__ __forceinline__ bool wait_panel_ready(const uint32_t* flag, uint32_t 
   }
 }
 
-// One task, called by a whole warp once its panel is known to be complete.
+// The per-head norm factors of head `hg` for row `t` from the GEMM's statistics. RMS:
+// from the head's sum of squares. LayerNorm: the (mean, M2) of each tile part of the
+// head's columns, combined with Chan, Golub and LeVeque's pairwise update (no large
+// sums subtracted); the hand-off holds each part's values centred on the part's mean,
+// so `shift_lo` / `shift_hi` (mean_part - mean_head of the parts holding this lane's
+// low and high chunk) turn them into deviations from the head's mean. Read through L2:
+// the GEMM writes them while this runs.
+__device__ __forceinline__ void head_factors(const NormRopeArgs& p, int t, int hg, int col_lo, int col_hi,
+                                             float& inv, float& shift_lo, float& shift_hi) {
+  const int d = p.d_head;
+  const int heads = p.n_q + p.n_kv;
+  if (p.head_kind == 2) {
+    const float s2 = __ldcg(p.head_stats + static_cast<size_t>(t) * heads + hg);
+    inv = 1.0f / sqrtf(s2 / static_cast<float>(d) + p.eps);
+    shift_lo = shift_hi = 0.0f;
+    return;
+  }
+  const int hs = hg * d;
+  const int t0 = hs / p.tile_n;
+  const float2* st = reinterpret_cast<const float2*>(p.head_stats) + (static_cast<size_t>(t) * heads + hg) * p.stat_parts;
+  float n = 0.0f, m = 0.0f, m2 = 0.0f;
+  for (int i = 0; i < p.stat_parts; ++i) {
+    const int lo = max(hs, (t0 + i) * p.tile_n);
+    const int hi = min(hs + d, (t0 + i + 1) * p.tile_n);
+    if (lo >= hi) break;
+    const float ni = static_cast<float>(hi - lo);
+    const float2 part = __ldcg(st + i);
+    const float nn = n + ni;
+    const float delta = part.x - m;
+    m += delta * (ni / nn);
+    m2 += part.y + delta * delta * (n * ni / nn);
+    n = nn;
+  }
+  inv = 1.0f / sqrtf(m2 / static_cast<float>(d) + p.eps);
+  shift_lo = __ldcg(st + (col_lo / p.tile_n - t0)).x - m;
+  shift_hi = __ldcg(st + (col_hi / p.tile_n - t0)).x - m;
+}
+
+// One task, called by a whole warp once its panel is known to be complete. kHeadStats:
+// the per-head norm from the GEMM's statistics (a separate instantiation, so the
+// across-heads form keeps its lower register count).
+template <bool kHeadStats>
 __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, int group_heads, uint64_t once) {
   const int lane = threadIdx.x & 31;
   const int d = p.d_head;
@@ -164,13 +205,12 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
   const int tr = t < p.T ? t : p.T - 1;
 
   float inv_q = 1.0f, inv_k = 1.0f;
-  if (p.norm) {
+  if (p.norm && !kHeadStats) {
     inv_q = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr)] / static_cast<float>(p.n_q * d) + p.eps);
     if (p.n_kv > 0)
       inv_k = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr) + 1] / static_cast<float>(p.n_kv * d) + p.eps);
   }
   float cl[16], ch[16], sl[16], sh[16];
-  float nsl[16];  // -sin of the low half: the rotation is one mul and one fma per lane pair
   if (p.rope) {
     const float* cr = p.cos_t + static_cast<size_t>(tr) * d + c * 16;
     const float* sr = p.sin_t + static_cast<size_t>(tr) * d + c * 16;
@@ -182,8 +222,6 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
     load8_nc(sr + 8, sl + 8);
     load8_nc(sr + half, sh);
     load8_nc(sr + half + 8, sh + 8);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) nsl[j] = -sl[j];
   }
   const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (t & 127);
   for (int hg0 = h_begin; hg0 < h_end; hg0 += kHeadBatch) {
@@ -209,7 +247,21 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
       float lo[16], hi[16];
       decode16(raw_lo[k], lo);
       decode16(raw_hi[k], hi);
-      if (p.norm) {
+      if constexpr (kHeadStats) {  // per-head norm: (y - mean) * inv * gamma[d_head]
+        float inv, shift_lo, shift_hi;
+        head_factors(p, tr, hg, col, col + half, inv, shift_lo, shift_hi);
+        const uint16_t* gamma = (seg ? p.gamma_k : p.gamma_q) + c * 16;
+        float g[8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          unpack8(__ldg(reinterpret_cast<const uint4*>(gamma) + q), g);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) lo[8 * q + j] = (lo[8 * q + j] + shift_lo) * (inv * g[j]);
+          unpack8(__ldg(reinterpret_cast<const uint4*>(gamma + half) + q), g);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) hi[8 * q + j] = (hi[8 * q + j] + shift_hi) * (inv * g[j]);
+        }
+      } else if (p.norm) {  // across heads
         const uint16_t* gamma = seg ? p.gamma_k : p.gamma_q;
         const float inv = seg ? inv_k : inv_q;
         const float2 inv2 = make_float2(inv, inv);
@@ -240,7 +292,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
         for (int j = 0; j < 8; ++j) {
           const float2 l2 = make_float2(lo[2 * j], lo[2 * j + 1]);
           const float2 h2 = make_float2(hi[2 * j], hi[2 * j + 1]);
-          const float2 a = ffma2(h2, make_float2(nsl[2 * j], nsl[2 * j + 1]),
+          const float2 a = ffma2(h2, make_float2(-sl[2 * j], -sl[2 * j + 1]),
                                  fmul2(l2, make_float2(cl[2 * j], cl[2 * j + 1])));
           const float2 b = ffma2(l2, make_float2(sh[2 * j], sh[2 * j + 1]),
                                  fmul2(h2, make_float2(ch[2 * j], ch[2 * j + 1])));
@@ -256,7 +308,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
       }
     }
   }
-  if (c == 0 && grp == 0 && row_ok && p.norm && p.inv_rms != nullptr) {
+  if (!kHeadStats && c == 0 && grp == 0 && row_ok && p.norm && p.inv_rms != nullptr) {
     p.inv_rms[2 * static_cast<size_t>(t)] = inv_q;
     p.inv_rms[2 * static_cast<size_t>(t) + 1] = p.n_kv > 0 ? inv_k : 0.0f;
   }

@@ -152,10 +152,19 @@ bool per_head_norm(const qkv_cte_desc& d) {
   return d.norm == QKV_CTE_NORM_HEAD_RMS || d.norm == QKV_CTE_NORM_HEAD_LAYER;
 }
 
+// Per-head norm finished in the GEMM's epilogue (tiles of whole heads, no second pass)
+// rather than from per-head statistics by the norm/RoPE pass (the default).
+bool head_norm_in_epilogue(const qkv_cte_desc& d) {
+  return per_head_norm(d) && (d.flags & QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE) != 0;
+}
+
+// Tiles a head's columns can touch: the statistics keep one part per tile.
+int stat_parts(int d_head, int tile_n) { return (d_head + tile_n - 2) / tile_n + 1; }
+
 int choose_tile_n(const qkv_cte_desc& d, int I) {
   if (d.tile_n != 0) return d.tile_n;
   (void)I;
-  if (per_head_norm(d)) {
+  if (head_norm_in_epilogue(d)) {
     // The per-head epilogue needs whole heads in every tile: the widest built tile
     // with two TMEM accumulator stages that d_head divides, else 256 (one stage).
     for (int t : {240, 192, 128})
@@ -201,7 +210,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
     return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
   const uint32_t known_flags = QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES |
                                QKV_CTE_FLAG_GEMM_CTA_PAIR | QKV_CTE_FLAG_GEMM_SINGLE_CTA |
-                               QKV_CTE_FLAG_NORM_IN_GEMM;
+                               QKV_CTE_FLAG_NORM_IN_GEMM | QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE;
   if ((d.flags & ~known_flags) != 0) return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
   if ((d.flags & QKV_CTE_FLAG_GEMM_CTA_PAIR) && (d.flags & QKV_CTE_FLAG_GEMM_SINGLE_CTA))
     return fail(QKV_CTE_ERR_INVALID, "QKV_CTE_FLAG_GEMM_CTA_PAIR and QKV_CTE_FLAG_GEMM_SINGLE_CTA exclude each other");
@@ -217,7 +226,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
     return fail(QKV_CTE_ERR_UNSUPPORTED, "a norm or RoPE needs d_head %% 32 == 0 (got %d)", d.d_head);
   const int tile_n = choose_tile_n(d, (int)I);
   if (!gemm_tile_supported(tile_n)) return fail(QKV_CTE_ERR_UNSUPPORTED, "tile_n %d not built", tile_n);
-  if (per_head_norm(d) && tile_n % d.d_head != 0)
+  if (head_norm_in_epilogue(d) && tile_n % d.d_head != 0)
     return fail(QKV_CTE_ERR_UNSUPPORTED, "per-head norm needs whole heads per tile: tile_n %d, d_head %d", tile_n,
                 d.d_head);
 
@@ -260,13 +269,19 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   w.qk_off = w.ready_off + align_up((size_t)g.blocks128 * sizeof(uint32_t), 256);
   // The norm/RoPE pass (and its hand-off) runs for the across-heads norm, or RoPE
   // without a norm; the per-head norms finish in the GEMM's epilogue.
-  const bool second_pass = !per_head_norm(d) && (d.norm == QKV_CTE_NORM_ACROSS_HEADS || d.rope);
+  const bool second_pass = !head_norm_in_epilogue(d) && (d.norm != QKV_CTE_NORM_NONE || d.rope);
   p->second_pass = second_pass;
-  p->fused_norm = second_pass && g.cta_pair && (d.flags & QKV_CTE_FLAG_NORM_IN_GEMM) &&
+  p->fused_norm = second_pass && g.cta_pair && !per_head_norm(d) && (d.flags & QKV_CTE_FLAG_NORM_IN_GEMM) &&
                   !(d.flags & QKV_CTE_FLAG_SERIAL_PASSES);
   const size_t hand_rows = second_pass ? (size_t)g.blocks128 * 128 : 0;
   w.qk_exp_off = w.qk_off + align_up(hand_rows * p->k_end * sizeof(uint16_t), 256);
-  w.act_off = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
+  w.stats_off = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
+  const size_t qk_heads = (size_t)(d.n_q_heads + d.n_kv_heads);
+  size_t stats_bytes = 0;
+  if (per_head_norm(d) && !head_norm_in_epilogue(d))
+    stats_bytes = hand_rows * qk_heads *
+                  (d.norm == QKV_CTE_NORM_HEAD_RMS ? sizeof(float) : 2 * sizeof(float) * stat_parts(d.d_head, tile_n));
+  w.act_off = w.stats_off + align_up(stats_bytes, 256);
   const bool produced = d.input_layout != QKV_CTE_INPUT_ROW_FP8;
   w.act_scale_off = w.act_off + (produced ? align_up((size_t)g.T * g.H, 256) : 0);
   w.total = w.act_scale_off + (produced ? align_up((size_t)g.T * sizeof(float), 256) : 0);
@@ -410,8 +425,13 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   uint32_t* ready = reinterpret_cast<uint32_t*>(ws + plan->ws.ready_off);
   unsigned long long* stamps = reinterpret_cast<unsigned long long*>(ws + kStampOffset);
   uint32_t* task_next = reinterpret_cast<uint32_t*>(ws + kTaskCounterOffset);
+  const bool head_stats = per_head_norm(d) && !head_norm_in_epilogue(d);
+  float* stats = head_stats ? reinterpret_cast<float*>(ws + plan->ws.stats_off) : nullptr;
+  // the RMS statistics are sums accumulated with atomics: they start at zero
+  const size_t zero_stats =
+      head_stats && d.norm == QKV_CTE_NORM_HEAD_RMS ? (size_t)g.blocks128 * 128 * (d.n_q_heads + d.n_kv_heads) : 0;
   e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0, ready, status,
-                  stamps, task_next, s, dev.sms);
+                  stamps, task_next, stats, zero_stats, s, dev.sms);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
   if (prof) cudaEventRecord(plan->ev[1], s);
 
@@ -434,8 +454,11 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.flags = d.flags;
   ga.d_head = d.d_head;
   ga.nbsd = d.output_layout == QKV_CTE_LAYOUT_NBSD ? 1 : 0;
-  ga.head_norm = per_head_norm(d) ? d.norm : 0;
-  ga.rope = per_head_norm(d) ? d.rope : 0;
+  ga.head_norm = head_norm_in_epilogue(d) ? d.norm : 0;
+  ga.rope = head_norm_in_epilogue(d) ? d.rope : 0;
+  ga.stats_kind = head_stats ? d.norm : 0;
+  ga.head_stats = stats;
+  ga.stat_parts = stat_parts(d.d_head, g.tile_n);
   ga.eps = d.eps;
   ga.gamma_q = gamma_q;
   ga.gamma_k = gamma_k;
@@ -465,6 +488,10 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.status = status;
   na.stamps = stamps + 2;
   na.task_next = task_next;
+  na.head_kind = head_stats ? d.norm : 0;
+  na.head_stats = stats;
+  na.stat_parts = stat_parts(d.d_head, g.tile_n);
+  na.tile_n = g.tile_n;
   CUtensorMap tmSF;
   if ((rc = encode_scales(&tmSF, sf_packed, g)) != QKV_CTE_OK) return rc;
   // On request the norm/RoPE tasks run inside the CTA-pair GEMM's epilogue warps;

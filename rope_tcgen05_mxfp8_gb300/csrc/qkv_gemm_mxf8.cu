@@ -18,7 +18,7 @@ __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __re
                                 int k_blocks, int tile_n, int n_tiles, int k_stages, int sf_chunks,
                                 float* __restrict__ sumsq, size_t sumsq_count, uint32_t* __restrict__ ready,
                                 int m_tiles, uint32_t* status, unsigned long long* stamps,
-                                uint32_t* task_next) {
+                                uint32_t* task_next, float* __restrict__ zero_extra, size_t zero_extra_count) {
   const size_t words = static_cast<size_t>(n_tiles) * k_stages * sf_chunks * 128;
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   const size_t first = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -39,6 +39,7 @@ __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __re
     packed[w] = v;
   }
   for (size_t i = first; i < sumsq_count; i += stride) sumsq[i] = 0.0f;
+  for (size_t i = first; i < zero_extra_count; i += stride) zero_extra[i] = 0.0f;
   for (size_t i = first; i < static_cast<size_t>(m_tiles); i += stride) ready[i] = 0u;
   if (first == 0) {
     status[0] = 0u;
@@ -78,23 +79,25 @@ size_t gemm_smem_bytes(int tile_n) {
 
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
                         size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
-                        uint32_t* task_next, cudaStream_t s, int num_sms) {
+                        uint32_t* task_next, float* zero_extra, size_t zero_extra_count, cudaStream_t s,
+                        int num_sms) {
   const size_t words = static_cast<size_t>(g.n_tiles) * g.k_stages * g.sf_chunks * 128;
-  const size_t work = words > sumsq_count ? words : sumsq_count;
+  size_t work = words > sumsq_count ? words : sumsq_count;
+  if (zero_extra_count > work) work = zero_extra_count;
   size_t blocks = (work + 255) / 256;
   const size_t cap = static_cast<size_t>(num_sms) * 4;
   if (blocks > cap) blocks = cap;
   if (blocks == 0) blocks = 1;
   qkv_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
       w_sf, reinterpret_cast<uint32_t*>(sf_packed), g.I, g.H / 32, g.tile_n, g.n_tiles, g.k_stages,
-      g.sf_chunks, sumsq, sumsq_count, ready, g.blocks128, status, stamps, task_next);
+      g.sf_chunks, sumsq, sumsq_count, ready, g.blocks128, status, stamps, task_next, zero_extra, zero_extra_count);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                         const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms,
                         const NormRopeArgs* fused) {
-  if (a.head_norm != 0) return launch_gemm_head(g, tmA, tmW, tmSF, a, s, num_sms);
+  if (a.head_norm != 0 || a.stats_kind != 0) return launch_gemm_head(g, tmA, tmW, tmSF, a, s, num_sms);
   if (fused != nullptr) {
     if (!g.cta_pair) return cudaErrorInvalidValue;
     return launch_gemm_fused(g, tmA, tmW, tmSF, a, *fused, s, num_sms);
@@ -102,18 +105,18 @@ cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtens
   const NormRopeArgs none{};
   if (g.cta_pair) {
     switch (g.tile_n) {
-      case 128: return launch_gemm_pair_t<128, false, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
-      case 192: return launch_gemm_pair_t<192, false, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
-      case 240: return launch_gemm_pair_t<240, false, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
-      case 256: return launch_gemm_pair_t<256, false, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
+      case 128: return launch_gemm_pair_t<128, kEpiPlain, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
+      case 192: return launch_gemm_pair_t<192, kEpiPlain, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
+      case 240: return launch_gemm_pair_t<240, kEpiPlain, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
+      case 256: return launch_gemm_pair_t<256, kEpiPlain, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (g.tile_n) {
-    case 128: return launch_gemm_t<128, false>(g, tmA, tmW, a, s, num_sms);
-    case 192: return launch_gemm_t<192, false>(g, tmA, tmW, a, s, num_sms);
-    case 240: return launch_gemm_t<240, false>(g, tmA, tmW, a, s, num_sms);
-    case 256: return launch_gemm_t<256, false>(g, tmA, tmW, a, s, num_sms);
+    case 128: return launch_gemm_t<128, kEpiPlain>(g, tmA, tmW, a, s, num_sms);
+    case 192: return launch_gemm_t<192, kEpiPlain>(g, tmA, tmW, a, s, num_sms);
+    case 240: return launch_gemm_t<240, kEpiPlain>(g, tmA, tmW, a, s, num_sms);
+    case 256: return launch_gemm_t<256, kEpiPlain>(g, tmA, tmW, a, s, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }

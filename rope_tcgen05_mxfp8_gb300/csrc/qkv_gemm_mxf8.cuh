@@ -275,7 +275,65 @@ __device__ __forceinline__ void epilogue_drain_head(const GemmShape& g, const Ge
   }
 }
 
+// Block-float hand-off of 16 values: the chunk's exponent E = floor(log2 max|v|)
+// (clamped; 0 for zero or non-finite maxima) and v * 2^-E in fp16, so every value
+// keeps 11 significant bits relative to the chunk maximum whatever its range.
+__device__ __forceinline__ void store_handoff16(const GemmArgs& a, size_t idx, const float* v) {
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+  const int field = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu);
+  int e = (field == 0 || field == 255) ? 0 : field - 127;
+  e = e < -126 ? -126 : (e > 126 ? 126 : e);
+  const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
+  uint32_t hv[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 x = fmul2(make_float2(v[2 * j], v[2 * j + 1]), make_float2(down, down));
+    hv[j] = pack_f16x2(x.x, x.y);
+  }
+  st_global_v8_b32(a.qk_val + idx * 16, hv);
+  a.qk_exp[idx] = static_cast<uint8_t>(e + 127);
+}
+
+// Close one part of a Q/K head (its columns c0..c1 in this tile) for the per-head
+// statistics. RMS adds the part's sum of squares to the (row, head) total. LayerNorm
+// stores the part's mean and its centred sum of squares M2, taken in a second pass over
+// the part's accumulator columns, and hands the part's values over centred on that
+// mean (o - mean_part): a large common offset would otherwise leave the deviations
+// LayerNorm amplifies below the hand-off's resolution. The norm/RoPE pass adds
+// mean_part - mean_head back, and combines the parts with Chan et al.'s pairwise
+// update, so no large sums are subtracted anywhere.
 template <int BN>
+__device__ __forceinline__ void stats_flush(const GemmShape& g, const GemmArgs& a, uint32_t t_acc, int col_base,
+                                            int row, bool row_ok, float ascale, size_t qk_row_idx, int head, int c0,
+                                            int c1, float s1, float s2) {
+  const int heads = a.k_end / a.d_head;
+  if (a.stats_kind == 2) {
+    if (row_ok) atomicAdd(&a.head_stats[static_cast<size_t>(row) * heads + head], s2);
+    return;
+  }
+  const float mean = s1 / static_cast<float>(c1 - c0);
+  float m2 = 0.0f;
+  for (int c = c0; c < c1; c += 16) {
+    float v[16];
+    projected16(a, t_acc + static_cast<uint32_t>(c - col_base), ascale, c, v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      v[j] -= mean;
+      m2 = fmaf(v[j], v[j], m2);
+    }
+    store_handoff16(a, qk_row_idx + static_cast<size_t>(c >> 4) * 128, v);
+  }
+  if (row_ok) {
+    const int part = col_base / BN - (head * a.d_head) / BN;
+    reinterpret_cast<float2*>(a.head_stats)[(static_cast<size_t>(row) * heads + head) * a.stat_parts + part] =
+        make_float2(mean, m2);
+  }
+}
+
+// kStats: 0 none, 2 per-head RMS statistics, 3 per-head LayerNorm statistics.
+template <int BN, int kStats>
 __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const GemmArgs& a, uint32_t t_acc,
                                                      int block128, int row_in_block, int col_base, uint64_t pol_out,
                                                      float& ss_q, float& ss_k) {
@@ -286,6 +344,8 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
   const size_t qk_row_idx = static_cast<size_t>(block128) * qk_chunks * 128 + row_in_block;
   ss_q = 0.0f;
   ss_k = 0.0f;
+  int st_head = -1, st_c0 = 0, st_c1 = 0;  // the open head part (kStats)
+  float st_s1 = 0.0f, st_s2 = 0.0f;
 #pragma unroll
   for (int c0 = 0; c0 < BN; c0 += 32) {
     uint32_t r[32];
@@ -341,27 +401,31 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
       }
       const float sq = sq2.x + sq2.y;
       if (col0 < a.q_end) ss_q += sq; else if (col0 < a.k_end) ss_k += sq;
-      if (a.qk_val != nullptr && col0 < a.k_end) {
-        // Q/K columns that the norm/RoPE pass will finish: the chunk's exponent
-        // E = floor(log2 max|v|) (clamped; 0 for zero or non-finite maxima) and
-        // v * 2^-E in fp16, so every value keeps 11 significant bits relative to
-        // the chunk maximum whatever its range.
-        float m = 0.0f;
+      if constexpr (kStats != 0) {
+        if (col0 < a.k_end) {
+          const int hh = col0 / a.d_head;  // uniform across the warp
+          if (hh != st_head) {
+            if (st_head >= 0)
+              stats_flush<BN>(g, a, t_acc, col_base, row, row_ok, ascale, qk_row_idx, st_head, st_c0, st_c1, st_s1,
+                              st_s2);
+            st_head = hh;
+            st_c0 = col0;
+            st_s1 = st_s2 = 0.0f;
+          }
+          if constexpr (kStats == 3) {  // LayerNorm also needs the part's sum
+            float s1 = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
-        const int field = static_cast<int>((__float_as_uint(m) >> 23) & 0xFFu);
-        int e = (field == 0 || field == 255) ? 0 : field - 127;
-        e = e < -126 ? -126 : (e > 126 ? 126 : e);
-        const float down = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);  // 2^-e
-        uint32_t hv[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2 x = fmul2(make_float2(v[2 * j], v[2 * j + 1]), make_float2(down, down));
-          hv[j] = pack_f16x2(x.x, x.y);
+            for (int j = 0; j < 16; ++j) s1 += v[j];
+            st_s1 += s1;
+          }
+          st_s2 += sq;
+          st_c1 = col0 + 16;
         }
-        const size_t idx = qk_row_idx + static_cast<size_t>(col0 >> 4) * 128;
-        st_global_v8_b32(a.qk_val + idx * 16, hv);
-        a.qk_exp[idx] = static_cast<uint8_t>(e + 127);
+      }
+      if (a.qk_val != nullptr && col0 < a.k_end) {
+        // Q/K columns the norm/RoPE pass will finish (LayerNorm statistics hand them
+        // over centred, from stats_flush)
+        if (kStats != 3) store_handoff16(a, qk_row_idx + static_cast<size_t>(col0 >> 4) * 128, v);
       } else if (row_ok) {
         uint32_t packed[8];
 #pragma unroll
@@ -371,19 +435,31 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
       }
     }
   }
+  if constexpr (kStats != 0) {
+    if (st_head >= 0)
+      stats_flush<BN>(g, a, t_acc, col_base, row, row_ok, ascale, qk_row_idx, st_head, st_c0, st_c1, st_s1, st_s2);
+  }
 }
 
-// The per-head variant is a separate instantiation of the kernels: its epilogue needs
-// about 50 more registers per thread, which would otherwise leave no room on an SM
-// sub-partition for a norm/RoPE warp beside the GEMM's two warps there.
-template <int BN, bool kHead>
+// Epilogue kinds, each a separate instantiation of the kernels (the per-head ones need
+// more registers per thread, which would otherwise leave no room on an SM
+// sub-partition for a norm/RoPE warp beside the GEMM's two warps there):
+//   kEpiPlain : Q/K to the norm/RoPE hand-off (or as projected), V to O
+//   kEpiHead  : the per-head norm and RoPE finished here (tiles hold whole heads)
+//   kEpiStatsRms / kEpiStatsLayer : as plain, plus the per-head statistics (RMS: sums of
+//               squares; LayerNorm: each part's mean and centred M2, values handed over
+//               centred) the norm/RoPE pass finishes from
+constexpr int kEpiPlain = 0, kEpiHead = 1, kEpiStatsRms = 2, kEpiStatsLayer = 3;
+
+template <int BN, int kEpi>
 __device__ __forceinline__ void epilogue_drain(const GemmShape& g, const GemmArgs& a, uint32_t t_acc, int block128,
                                                int row_in_block, int col_base, uint64_t pol_out, float& ss_q,
                                                float& ss_k) {
-  if constexpr (kHead)
+  if constexpr (kEpi == kEpiHead)
     epilogue_drain_head<BN>(g, a, t_acc, block128, row_in_block, col_base, pol_out, ss_q, ss_k);
   else
-    epilogue_drain_plain<BN>(g, a, t_acc, block128, row_in_block, col_base, pol_out, ss_q, ss_k);
+    epilogue_drain_plain<BN, kEpi == kEpiStatsRms ? 2 : (kEpi == kEpiStatsLayer ? 3 : 0)>(
+        g, a, t_acc, block128, row_in_block, col_base, pol_out, ss_q, ss_k);
 }
 
 // After the accumulator is released: add this warp's rows' sums of squares and, for
@@ -405,7 +481,7 @@ __device__ __forceinline__ void epilogue_publish(const GemmShape& g, const GemmA
   }
 }
 
-template <int BN, bool kHead>
+template <int BN, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                          const GemmShape g, const GemmArgs a) {
@@ -592,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       float ss_q, ss_k;
-      epilogue_drain<BN, kHead>(g, a, t_lane + static_cast<uint32_t>(acc * BN), m_blk, row_in_block, n_blk * BN, pol_out,
+      epilogue_drain<BN, kEpi>(g, a, t_lane + static_cast<uint32_t>(acc * BN), m_blk, row_in_block, n_blk * BN, pol_out,
                          ss_q, ss_k);
       tc_fence_before();
       __syncwarp();
@@ -694,7 +770,7 @@ __device__ __forceinline__ bool fused_try(const NormRopeArgs& nr, FusedWork& w, 
     w.started = true;
     if ((threadIdx.x & 31) == 0) atomicMin(&nr.stamps[0], globaltimer_ns());
   }
-  nrp::run_task(nr, w.pending, kFusedHeadGroup, once);
+  nrp::run_task<false>(nr, w.pending, kFusedHeadGroup, once);
   w.pending = -1;
   return true;
 }
@@ -744,7 +820,7 @@ __device__ __forceinline__ void fused_finish(const NormRopeArgs& nr, long long n
   if (w.started && (threadIdx.x & 31) == 0) atomicMax(&nr.stamps[1], globaltimer_ns());
 }
 
-template <int BN, bool kHead, bool kFused>
+template <int BN, int kEpi, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                               const __grid_constant__ CUtensorMap tmSF, const GemmShape g, const GemmArgs a,
@@ -947,7 +1023,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = block128 * kBM < g.T;
       float ss_q = 0.0f, ss_k = 0.0f;
       if (live)
-        epilogue_drain<BN, kHead>(g, a, t_lane + static_cast<uint32_t>(acc * BN), block128, row_in_block, n_blk * BN,
+        epilogue_drain<BN, kEpi>(g, a, t_lane + static_cast<uint32_t>(acc * BN), block128, row_in_block, n_blk * BN,
                            pol_out, ss_q, ss_k);
       tc_fence_before();
       __syncwarp();
@@ -974,11 +1050,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) atomicMax(&a.stamps[1], globaltimer_ns());
 }
 
-template <int BN, bool kHead>
+template <int BN, int kEpi>
 cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                           const GemmArgs& a, cudaStream_t s, int num_sms) {
   using C = K1Cfg<BN>;
-  auto kern = qkv_gemm_mxf8_kernel<BN, kHead>;
+  auto kern = qkv_gemm_mxf8_kernel<BN, kEpi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
@@ -988,12 +1064,12 @@ cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUte
   return cudaGetLastError();
 }
 
-template <int BN, bool kHead, bool kFused>
+template <int BN, int kEpi, bool kFused>
 cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                                const CUtensorMap& tmSF, const GemmArgs& a, const NormRopeArgs& nr, cudaStream_t s,
                                int num_sms) {
   using C = K1PairCfg<BN>;
-  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kHead, kFused>;
+  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, kFused>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;

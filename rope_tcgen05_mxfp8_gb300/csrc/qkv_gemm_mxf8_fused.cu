@@ -10,10 +10,10 @@ cudaError_t launch_gemm_fused(const GemmShape& g, const CUtensorMap& tmA, const 
                               const CUtensorMap& tmSF, const GemmArgs& a, const NormRopeArgs& nr, cudaStream_t s,
                               int num_sms) {
   switch (g.tile_n) {
-    case 128: return launch_gemm_pair_t<128, false, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
-    case 192: return launch_gemm_pair_t<192, false, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
-    case 240: return launch_gemm_pair_t<240, false, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
-    case 256: return launch_gemm_pair_t<256, false, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
+    case 128: return launch_gemm_pair_t<128, kEpiPlain, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
+    case 192: return launch_gemm_pair_t<192, kEpiPlain, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
+    case 240: return launch_gemm_pair_t<240, kEpiPlain, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
+    case 256: return launch_gemm_pair_t<256, kEpiPlain, true>(g, tmA, tmW, tmSF, a, nr, s, num_sms);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -38,6 +38,7 @@ QKV_CTE_FLAG_SERIAL_PASSES = 0x4
 QKV_CTE_FLAG_GEMM_CTA_PAIR = 0x8
 QKV_CTE_FLAG_GEMM_SINGLE_CTA = 0x10
 QKV_CTE_FLAG_NORM_IN_GEMM = 0x20
+QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE = 0x40
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
             "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",

@@ -80,7 +80,8 @@ def _plan_code(**kw):
     (dict(d_head=48, norm=0, rope=0), 0),        # plain projection: d % 16 is enough
     (dict(norm=2), 0),
     (dict(norm=3), 0),
-    (dict(norm=2, tile_n=240), -2),     # per-head norm: 128-wide heads do not divide a 240 tile
+    (dict(norm=2, tile_n=240), 0),      # per-head norm from statistics: any tile
+    (dict(norm=2, tile_n=240, flags=0x40), -2),  # ... in the epilogue: 128-wide heads do not divide 240
     (dict(norm=3, tile_n=256), 0),
     (dict(rope=-1), -1),
     (dict(eps=-1.0), -1),
@@ -102,7 +103,8 @@ def test_plan_validation(kw, code):
 
 def test_per_head_norm_chooses_a_tile_of_whole_heads():
     for d, tile in ((128, 128), (64, 192), (256, 256), (32, 192), (96, 192)):
-        plan, ws = q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, d, norm=2))
+        plan, ws = q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, d, norm=2,
+                                        flags=q.QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE))
         try:
             info = q.qkv_cte_get_plan_info(plan)
             assert info.tile_n == tile and info.tile_n % d == 0
@@ -112,7 +114,7 @@ def test_per_head_norm_chooses_a_tile_of_whole_heads():
 
 def test_per_head_norm_rejects_heads_no_tile_holds():
     with pytest.raises(q.QkvCteError) as ei:
-        q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, 160, norm=2))
+        q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, 160, norm=2, flags=q.QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE))
     assert ei.value.code == q.QKV_CTE_ERR_UNSUPPORTED and "whole heads" in str(ei.value)
 
 
@@ -138,16 +140,25 @@ def test_norm_runs_in_the_gemm_only_on_request():
             q.qkv_cte_destroy(plan)
 
 
-def test_per_head_norm_has_no_hand_off():
-    """The per-head kinds finish in the GEMM epilogue: no Q/K hand-off in the workspace."""
+def test_per_head_norm_workspace():
+    """In the epilogue the per-head kinds need no Q/K hand-off; from statistics they need
+    the hand-off plus per-(row, head) statistics: one float (RMS) or, per tile part of a
+    head, a (mean, M2) pair (LayerNorm)."""
     T = 1000
-    plan_a, ws_a = q.qkv_cte_plan(q.make_desc(T, 512, 4, 4, 128, norm=1, tile_n=128))
-    plan_h, ws_h = q.qkv_cte_plan(q.make_desc(T, 512, 4, 4, 128, norm=2, tile_n=128))
-    q.qkv_cte_destroy(plan_a)
-    q.qkv_cte_destroy(plan_h)
+    align = lambda x: -(-x // 256) * 256
     rows = -(-T // 128) * 128
     kq = 8 * 128
-    assert ws_a - ws_h == -(-(rows * kq * 2) // 256) * 256 + -(-(rows * kq // 16) // 256) * 256
+    hand_off = align(rows * kq * 2) + align(rows * kq // 16)
+    F = q.QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE
+    sizes = {}
+    for key, norm, flags in (("across", 1, 0), ("epi", 2, F), ("rms", 2, 0), ("ln", 3, 0)):
+        plan, ws = q.qkv_cte_plan(q.make_desc(T, 512, 4, 4, 128, norm=norm, tile_n=128, flags=flags))
+        q.qkv_cte_destroy(plan)
+        sizes[key] = ws
+    assert sizes["across"] - sizes["epi"] == hand_off
+    assert sizes["rms"] - sizes["across"] == align(rows * 8 * 4)
+    parts = (128 + 128 - 2) // 128 + 1          # tiles a 128-column head can touch at tile 128
+    assert sizes["ln"] - sizes["across"] == align(rows * 8 * parts * 8)
 
 
 def test_plan_info_reports_the_choices():

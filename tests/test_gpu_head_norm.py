@@ -8,7 +8,7 @@ import torch
 import workloads as wl
 from oracle import qkv_cte_oracle as O
 from rope_tcgen05_mxfp8_gb300 import (QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA,
-                                      qkv_cte_interleaved_to_rotate_half)
+                                      QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE, qkv_cte_interleaved_to_rotate_half)
 
 from gpu_harness import check_outputs, run_path, sampled_rows, to_device
 
@@ -18,54 +18,81 @@ DEV = torch.device("cuda", 0)
 RMS, LAYER = O.NORM_HEAD_RMS, O.NORM_HEAD_LAYER
 
 
-def _case(call, flags=0, tile_n=0, rows=None, nbsd=False, name=None):
-    inp = wl.make_inputs(call)
+FORMS = {"stats": 0, "epilogue": QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE}
+
+
+def _case(call, flags=0, tile_n=0, rows=None, nbsd=False, name=None, form="stats", inp=None):
+    inp = inp if inp is not None else wl.make_inputs(call)
     g = to_device(inp, DEV)
-    op, out, ss, inv = run_path(call, g, tile_n=tile_n, flags=flags, nbsd=nbsd)
+    op, out, ss, inv = run_path(call, g, tile_n=tile_n, flags=flags | FORMS[form], nbsd=nbsd)
     op.status()
-    assert op.info.tile_n % call.d_head == 0
-    return check_outputs(call, inp, out, ss, inv, rows=rows, name=name or call.name)
+    if form == "epilogue":
+        assert op.info.tile_n % call.d_head == 0
+    return check_outputs(call, inp, out, ss, inv, rows=rows, name=name or f"{call.name}_{form}")
 
 
+@pytest.mark.parametrize("form", ["stats", "epilogue"])
 @pytest.mark.parametrize("norm", [RMS, LAYER])
-@pytest.mark.parametrize("form", ["auto", "single", "pair"])
-def test_head_norm_tiny(norm, form):
-    flags = {"auto": 0, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR}[form]
-    call = wl.custom_call(name=f"head{norm}_{form}", tokens=256, hidden=512, n_q_heads=4, n_kv_heads=4, d_head=128,
-                          norm=norm, rope=1, seed=norm * 10 + len(form), has_w_col_scale=True)
-    _case(call, flags=flags)
+@pytest.mark.parametrize("gemm", ["auto", "single", "pair"])
+def test_head_norm_tiny(norm, gemm, form):
+    flags = {"auto": 0, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR}[gemm]
+    call = wl.custom_call(name=f"head{norm}_{gemm}", tokens=256, hidden=512, n_q_heads=4, n_kv_heads=4, d_head=128,
+                          norm=norm, rope=1, seed=norm * 10 + len(gemm), has_w_col_scale=True)
+    _case(call, flags=flags, form=form)
 
 
+@pytest.mark.parametrize("form", ["stats", "epilogue"])
 @pytest.mark.parametrize("T", [1, 129, 300])
 @pytest.mark.parametrize("norm,rope", [(RMS, 1), (LAYER, 1), (RMS, 0), (LAYER, 0)])
-def test_head_norm_ragged(T, norm, rope):
+def test_head_norm_ragged(T, norm, rope, form):
     call = wl.custom_call(name=f"headT{T}", tokens=T, hidden=256, n_q_heads=3, n_kv_heads=1, d_head=128,
                           norm=norm, rope=rope, seed=T + norm, has_w_col_scale=True)
-    _case(call, name=f"head_T{T}_n{norm}_r{rope}")
+    _case(call, name=f"head_T{T}_n{norm}_r{rope}_{form}", form=form)
 
 
-@pytest.mark.parametrize("norm,tile_n", [(RMS, 0), (LAYER, 0), (RMS, 128), (LAYER, 256)])
-def test_head_norm_d64_tiles(norm, tile_n):
-    # d = 64: the automatic tile is 192 (three heads); 128 and 256 hold two and four
+@pytest.mark.parametrize("norm,tile_n,form", [(RMS, 0, "epilogue"), (LAYER, 0, "epilogue"), (RMS, 128, "epilogue"),
+                                             (LAYER, 256, "epilogue"), (RMS, 0, "stats"), (LAYER, 0, "stats"),
+                                             (LAYER, 192, "stats"), (RMS, 128, "stats")])
+def test_head_norm_d64_tiles(norm, tile_n, form):
+    # d = 64: in the epilogue the automatic tile is 192 (three heads); 128 and 256 hold two
+    # and four. From statistics any tile works (240 puts heads across tile edges).
     call = wl.custom_call(name="head_d64", tokens=200, hidden=384, n_q_heads=5, n_kv_heads=2, d_head=64,
                           norm=norm, rope=1, seed=41 + norm, has_w_col_scale=True)
-    _case(call, tile_n=tile_n, name=f"head_d64_n{norm}_t{tile_n}")
+    _case(call, tile_n=tile_n, name=f"head_d64_n{norm}_t{tile_n}_{form}", form=form)
 
 
+@pytest.mark.parametrize("tile_n", [192, 240, 256])
+def test_head_layernorm_parts_and_offset(tile_n):
+    """LayerNorm statistics combined across tile parts: 128-wide heads over 192/240-wide
+    tiles straddle tile edges, d = 256 over 240 spans up to three parts. A common offset
+    of 1000 on every column (the bias) with deviations of ~0.3 loses everything in a
+    one-pass variance (sum of squares ~1e6 in fp32) and in an uncentred fp16 hand-off
+    (resolution ~0.5 at 1000); the centred parts and their pairwise combination must
+    not."""
+    for d, nq in ((128, 5), (256, 3)):
+        call = wl.custom_call(name=f"ln_parts_d{d}_t{tile_n}", tokens=300, hidden=256, n_q_heads=nq,
+                              n_kv_heads=1, d_head=d, norm=LAYER, rope=1, seed=tile_n + d, has_w_col_scale=True)
+        inp = dict(wl.make_inputs(call))
+        inp["bias"] = torch.full_like(inp["bias"], 1000.0)   # exact in bf16
+        _case(call, tile_n=tile_n, inp=inp, name=call.name)
+
+
+@pytest.mark.parametrize("form", ["stats", "epilogue"])
 @pytest.mark.parametrize("norm", [RMS, LAYER])
-def test_head_norm_separate_and_nbsd(norm):
+def test_head_norm_separate_and_nbsd(norm, form):
     call = wl.custom_call(name="head_sep", tokens=333, hidden=512, n_q_heads=6, n_kv_heads=0, d_head=128,
                           norm=norm, rope=0, seed=51 + norm)
-    _case(call, nbsd=True, name=f"head_sep_nbsd_n{norm}")
+    _case(call, nbsd=True, name=f"head_sep_nbsd_n{norm}_{form}", form=form)
 
 
+@pytest.mark.parametrize("form", ["stats", "epilogue"])
 @pytest.mark.parametrize("norm", [RMS, LAYER])
-def test_head_norm_wan480p_sampled(norm):
+def test_head_norm_wan480p_sampled(norm, form):
     base = wl.workload("wan480p")[0]
     call = wl.custom_call(name=f"wan480p_head{norm}", tokens=base.tokens, hidden=base.hidden,
                           n_q_heads=base.n_q_heads, n_kv_heads=base.n_kv_heads, d_head=base.d_head, norm=norm,
                           rope=1, rope_grid=base.rope_grid, outlier_frac=base.outlier_frac, seed=base.seed)
-    _case(call, rows=sampled_rows(call))
+    _case(call, rows=sampled_rows(call), form=form)
 
 
 # --- interleaved -> rotate-half ----------------------------------------------------
