@@ -440,3 +440,62 @@ def test_large_token_count_sampled():
     op.status()
     rows = np.unique(np.concatenate([sampled_rows(call, 2048), [0, call.tokens - 1]]))
     check_outputs(call, inp, out, ss, inv, rows=rows, name=call.name)
+
+
+# --- streams and graphs ---------------------------------------------------------------
+
+def test_cuda_graph_capture_and_replay():
+    """The launch sequence (prep, the GEMM, the norm/RoPE pass as a programmatic
+    dependent) captures into a CUDA graph; every replay recomputes O correctly."""
+    call = wl.custom_call(name="graph", tokens=1000, hidden=1024, n_q_heads=3, n_kv_heads=2, d_head=128, seed=111,
+                          has_w_col_scale=True)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    from rope_tcgen05_mxfp8_gb300 import QkvCte
+
+    op = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, device=DEV)
+    out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=DEV)
+    ss = torch.empty(call.tokens, 2, dtype=torch.float32, device=DEV)
+    inv = torch.empty(call.tokens, 2, dtype=torch.float32, device=DEV)
+    args = (g["A"], g["a_scale"], g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"])
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        op(*args, out=out, w_col_scale=g["w_col_scale"], sumsq=ss, inv_rms=inv)   # warm-up outside the capture
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        op(*args, out=out, w_col_scale=g["w_col_scale"], sumsq=ss, inv_rms=inv)
+    for i in range(3):
+        out.fill_(float("nan"))
+        ss.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        op.status()
+        check_outputs(call, inp, out, ss, inv, name=f"graph_replay_{i}")
+
+
+def test_independent_calls_on_two_streams():
+    """Two plans, each with its own workspace, run at the same time on two streams."""
+    from rope_tcgen05_mxfp8_gb300 import QkvCte
+
+    calls = [wl.custom_call(name="stream_a", tokens=1500, hidden=1024, n_q_heads=4, n_kv_heads=2, d_head=128, seed=121),
+             wl.custom_call(name="stream_b", tokens=900, hidden=512, n_q_heads=6, n_kv_heads=0, d_head=64, norm=1,
+                            rope=0, seed=122)]
+    inps = [wl.make_inputs(c) for c in calls]
+    gs = [to_device(i, DEV) for i in inps]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    ops, outs, sss = [], [], []
+    for c, g in zip(calls, gs):
+        ops.append(QkvCte(c.tokens, c.hidden, c.n_q_heads, c.n_kv_heads, c.d_head, norm=c.norm, rope=c.rope,
+                          device=DEV))
+        outs.append(torch.full((c.tokens, c.width), float("nan"), dtype=torch.bfloat16, device=DEV))
+        sss.append(torch.empty(c.tokens, 2, dtype=torch.float32, device=DEV))
+    for _ in range(3):
+        for c, g, op, out, ss, s in zip(calls, gs, ops, outs, sss, streams):
+            with torch.cuda.stream(s):
+                op(g["A"], g["a_scale"], g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"],
+                   out=out, sumsq=ss, stream=s)
+    torch.cuda.synchronize()
+    for c, inp, op, out, ss, s in zip(calls, inps, ops, outs, sss, streams):
+        op.status(s)
+        check_outputs(c, inp, out, ss, None, name=c.name)
