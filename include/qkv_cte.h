@@ -97,8 +97,9 @@ enum { QKV_CTE_INPUT_ROW_FP8 = 0, QKV_CTE_INPUT_PACKED = 1, QKV_CTE_INPUT_BF16 =
 /* Test hook: the GEMM's load warp issues nothing, so every bounded wait downstream
  * runs out and the kernel exits through its error path (status word set). */
 #define QKV_CTE_FLAG_TEST_STALL 0x1u
-/* Record CUDA events between the launches of each run so qkv_cte_pass_times() can
- * report per-pass device times. */
+/* Record a CUDA event before and after each run so qkv_cte_pass_times() can report
+ * per-pass device times (nothing is recorded between the run's launches, which
+ * overlap). */
 #define QKV_CTE_FLAG_PROFILE 0x2u
 /* Launch the norm/RoPE pass as its own kernel after the GEMM has finished instead of
  * overlapping the two (same results; used to time each pass on its own). */
@@ -208,8 +209,9 @@ int qkv_cte_status(void* workspace, void* stream);
 
 /* Device times in milliseconds of the most recent run of `plan`, which must have been
  * created with QKV_CTE_FLAG_PROFILE. ms must hold 4 floats:
- *   ms[0] prep (the input's unpack or quantise step when it is packed or bf16, the
- *         scale repack and clears), from CUDA events around those launches;
+ *   ms[0] the rest of the run: the input's unpack or quantise step when it is packed
+ *         or bf16, the scale repack and clears, and launch gaps (ms[3] less the span
+ *         from the GEMM's start to the last end of the GEMM or the norm/RoPE work);
  *   ms[1] GEMM with its fused epilogue (including the norm/RoPE work when it runs in
  *         the GEMM's epilogue warps), and ms[2] norm + RoPE (0 when the call has
  *         neither): first start to last end of that work, from %globaltimer stamps the

@@ -192,7 +192,7 @@ size_t gemm_smem_bytes(int tile_n);
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
                         size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
                         uint32_t* task_next, float* zero_extra, size_t zero_extra_count, cudaStream_t s,
-                        int num_sms);
+                        int num_sms, bool after_producer);
 // K1. tmSF: the repacked scales as a uint32 [n_tiles * k_stages, sf_chunks * 128] map
 // with one-row boxes (used by the CTA-pair kernel). With `fused` (CTA-pair form only)
 // the epilogue warps also run the norm/RoPE tasks of `*fused` between tiles, and no

@@ -23,7 +23,7 @@ struct qkv_cte_plan_s {
   int q_end, k_end;
   // QKV_CTE_FLAG_PROFILE: events before the prep kernel, after it, and after the last
   // kernel of the latest run (no event between K1 and K2: it would serialise them)
-  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  cudaEvent_t ev[2] = {nullptr, nullptr};
   int ev_device = -1;
   bool ran = false;
   bool has_norm_pass = false;
@@ -320,9 +320,8 @@ int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms) {
   if (plan == nullptr || ms == nullptr) return fail(QKV_CTE_ERR_INVALID, "null argument");
   if (!(plan->d.flags & QKV_CTE_FLAG_PROFILE)) return fail(QKV_CTE_ERR_INVALID, "plan made without QKV_CTE_FLAG_PROFILE");
   if (!plan->ran) return fail(QKV_CTE_ERR_INVALID, "plan has not run");
-  cudaError_t e = cudaEventSynchronize(plan->ev[2]);
-  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[0], plan->ev[0], plan->ev[1]);
-  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[3], plan->ev[0], plan->ev[2]);
+  cudaError_t e = cudaEventSynchronize(plan->ev[1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms[3], plan->ev[0], plan->ev[1]);
   unsigned long long st[4] = {0, 0, 0, 0};
   if (e == cudaSuccess)
     e = cudaMemcpy(st, static_cast<const uint8_t*>(plan->last_workspace) + kStampOffset, sizeof(st),
@@ -330,6 +329,11 @@ int qkv_cte_pass_times(qkv_cte_plan_t plan, float* ms) {
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "pass times: %s", cudaGetErrorString(e));
   ms[1] = st[1] > st[0] ? (float)((st[1] - st[0]) * 1e-6) : 0.0f;
   ms[2] = (plan->has_norm_pass && st[3] > st[2]) ? (float)((st[3] - st[2]) * 1e-6) : 0.0f;
+  // The rest of the run: the producer step, the scale repack and clears, launch gaps.
+  // The GEMM starts its timed span once that work is complete (it waits for it).
+  const unsigned long long last = plan->has_norm_pass && st[3] > st[1] ? st[3] : st[1];
+  const float spans = last > st[0] ? (float)((last - st[0]) * 1e-6) : 0.0f;
+  ms[0] = ms[3] > spans ? ms[3] - spans : 0.0f;
   return ok();
 }
 
@@ -406,7 +410,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
     cudaGetDevice(&cur);
     if (plan->ev[0] != nullptr && plan->ev_device != cur)
       return fail(QKV_CTE_ERR_INVALID, "a profiled plan must stay on one device");
-    for (int i = 0; i < 3 && plan->ev[i] == nullptr; ++i)
+    for (int i = 0; i < 2 && plan->ev[i] == nullptr; ++i)
       if ((e = cudaEventCreate(&plan->ev[i])) != cudaSuccess)
         return fail(QKV_CTE_ERR_CUDA, "cudaEventCreate: %s", cudaGetErrorString(e));
     plan->ev_device = cur;
@@ -431,9 +435,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   const size_t zero_stats =
       head_stats && d.norm == QKV_CTE_NORM_HEAD_RMS ? (size_t)g.blocks128 * 128 * (d.n_q_heads + d.n_kv_heads) : 0;
   e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0, ready, status,
-                  stamps, task_next, stats, zero_stats, s, dev.sms);
+                  stamps, task_next, stats, zero_stats, s, dev.sms, produced);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
-  if (prof) cudaEventRecord(plan->ev[1], s);
 
   GemmArgs ga;
   ga.a_scale = A_scale;
@@ -505,7 +508,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
     if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "norm/rope launch: %s", cudaGetErrorString(e));
   }
   if (prof) {
-    cudaEventRecord(plan->ev[2], s);
+    cudaEventRecord(plan->ev[1], s);
     plan->ran = true;
     plan->has_norm_pass = plan->second_pass;
     plan->last_workspace = workspace;

@@ -12,34 +12,57 @@ namespace {
 // n = tile*tile_n + 128*chunk + 32*c + r for K block 4*stage + kb. That is the
 // 32-row x 16-byte shared-memory image tcgen05.cp 32x128b.warpx4 turns into the
 // TMEM scale-factor layout of an M=128 block-scaled MMA. Columns past I (or past
-// the tile) get 127. Also clears the status word, the panel counters, the timing
-// stamps and the sum-of-squares buffer.
-__global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __restrict__ packed, int I,
-                                int k_blocks, int tile_n, int n_tiles, int k_stages, int sf_chunks,
-                                float* __restrict__ sumsq, size_t sumsq_count, uint32_t* __restrict__ ready,
-                                int m_tiles, uint32_t* status, unsigned long long* stamps,
-                                uint32_t* task_next, float* __restrict__ zero_extra, size_t zero_extra_count) {
-  const size_t words = static_cast<size_t>(n_tiles) * k_stages * sf_chunks * 128;
+// the tile) get 127.
+//
+// The first n_tiles * stage_groups blocks each repack one N tile for up to
+// kPrepStages K stages: they read the tile's rows of w_sf (consecutive threads,
+// consecutive rows: 4 * kPrepStages contiguous bytes each) into shared memory and
+// write the blocks from there, so both sides are coalesced. Every block then takes a
+// share of the clears: the sum-of-squares buffer, the extra statistics, the panel
+// counters, the status word, the task counter and the timing stamps. Launched as a
+// programmatic dependent of a producer kernel (bf16 or packed activations), this
+// kernel does its own work beside it and waits for it before it ends, so the GEMM,
+// which waits for this kernel, also finds the producer's output complete.
+constexpr int kPrepThreads = 256;
+constexpr int kPrepStages = 8;
+
+__global__ void __launch_bounds__(kPrepThreads) qkv_prep_kernel(
+    const uint8_t* __restrict__ w_sf, uint32_t* __restrict__ packed, int I, int k_blocks, int tile_n, int n_tiles,
+    int k_stages, int sf_chunks, float* __restrict__ sumsq, size_t sumsq_count, uint32_t* __restrict__ ready,
+    int m_tiles, uint32_t* status, unsigned long long* stamps, uint32_t* task_next, float* __restrict__ zero_extra,
+    size_t zero_extra_count) {
+  __shared__ uint32_t rows[256][kPrepStages + 1];  // +1: the column reads below hit 32 banks
+  const int groups = (k_stages + kPrepStages - 1) / kPrepStages;
+  if (static_cast<int>(blockIdx.x) < n_tiles * groups) {
+    const int nt = static_cast<int>(blockIdx.x) / groups;
+    const int kst0 = (static_cast<int>(blockIdx.x) - nt * groups) * kPrepStages;
+    const int n_st = min(kPrepStages, k_stages - kst0);
+    const int i = threadIdx.x;  // tile_n <= 256 = kPrepThreads
+    const int n = nt * tile_n + i;
+    const bool live = i < tile_n && n < I;
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(w_sf + static_cast<size_t>(live ? n : 0) * k_blocks) + kst0;
+#pragma unroll
+    for (int k = 0; k < kPrepStages; ++k) rows[i][k] = (live && k < n_st) ? __ldg(src + k) : 0x7F7F7F7Fu;
+    __syncthreads();
+    const int per_stage = sf_chunks * 128;
+    uint32_t* dst = packed + (static_cast<size_t>(nt) * k_stages + kst0) * per_stage;
+    for (int w = threadIdx.x; w < n_st * per_stage; w += kPrepThreads) {
+      const int ks = w / per_stage;
+      const int rem = w - ks * per_stage;
+      const int within = rem & 127;
+      const int n_local = (rem >> 7) * 128 + (within & 3) * 32 + (within >> 2);
+      dst[w] = n_local < 256 ? rows[n_local][ks] : 0x7F7F7F7Fu;
+    }
+  }
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
   const size_t first = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  for (size_t w = first; w < words; w += stride) {
-    const int within = static_cast<int>(w & 127);
-    const int r = within >> 2;
-    const int c = within & 3;
-    size_t rest = w >> 7;
-    const int chunk = static_cast<int>(rest % sf_chunks);
-    rest /= sf_chunks;
-    const int kst = static_cast<int>(rest % k_stages);
-    const int nt = static_cast<int>(rest / k_stages);
-    const int n_local = chunk * 128 + c * 32 + r;
-    const int n = nt * tile_n + n_local;
-    uint32_t v = 0x7F7F7F7Fu;
-    if (n_local < tile_n && n < I)
-      v = __ldg(reinterpret_cast<const uint32_t*>(w_sf + static_cast<size_t>(n) * k_blocks + kst * 4));
-    packed[w] = v;
-  }
   for (size_t i = first; i < sumsq_count; i += stride) sumsq[i] = 0.0f;
-  for (size_t i = first; i < zero_extra_count; i += stride) zero_extra[i] = 0.0f;
+  if ((zero_extra_count & 3) == 0 && (reinterpret_cast<uintptr_t>(zero_extra) & 15) == 0) {
+    float4* z4 = reinterpret_cast<float4*>(zero_extra);
+    for (size_t i = first; i < zero_extra_count / 4; i += stride) z4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  } else {
+    for (size_t i = first; i < zero_extra_count; i += stride) zero_extra[i] = 0.0f;
+  }
   for (size_t i = first; i < static_cast<size_t>(m_tiles); i += stride) ready[i] = 0u;
   if (first == 0) {
     status[0] = 0u;
@@ -47,6 +70,8 @@ __global__ void qkv_prep_kernel(const uint8_t* __restrict__ w_sf, uint32_t* __re
     stamps[0] = stamps[2] = ~0ull;
     stamps[1] = stamps[3] = 0ull;
   }
+  // With a programmatic predecessor (the producer step), end only after it has.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // dst |= src: one chunk's status word into the status word of a run made of chunks.
@@ -80,18 +105,29 @@ size_t gemm_smem_bytes(int tile_n) {
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
                         size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
                         uint32_t* task_next, float* zero_extra, size_t zero_extra_count, cudaStream_t s,
-                        int num_sms) {
-  const size_t words = static_cast<size_t>(g.n_tiles) * g.k_stages * g.sf_chunks * 128;
-  size_t work = words > sumsq_count ? words : sumsq_count;
-  if (zero_extra_count > work) work = zero_extra_count;
-  size_t blocks = (work + 255) / 256;
+                        int num_sms, bool after_producer) {
+  if (g.tile_n > kPrepThreads) return cudaErrorInvalidValue;
+  const size_t repack = static_cast<size_t>(g.n_tiles) * ((g.k_stages + kPrepStages - 1) / kPrepStages);
+  size_t clear = sumsq_count > zero_extra_count / 4 ? sumsq_count : zero_extra_count / 4;
+  if (clear < static_cast<size_t>(g.blocks128)) clear = static_cast<size_t>(g.blocks128);
+  size_t blocks = (clear + kPrepThreads - 1) / kPrepThreads;
   const size_t cap = static_cast<size_t>(num_sms) * 4;
   if (blocks > cap) blocks = cap;
+  if (blocks < repack) blocks = repack;
   if (blocks == 0) blocks = 1;
-  qkv_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      w_sf, reinterpret_cast<uint32_t*>(sf_packed), g.I, g.H / 32, g.tile_n, g.n_tiles, g.k_stages,
-      g.sf_chunks, sumsq, sumsq_count, ready, g.blocks128, status, stamps, task_next, zero_extra, zero_extra_count);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(kPrepThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_producer ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, qkv_prep_kernel, w_sf, reinterpret_cast<uint32_t*>(sf_packed), g.I, g.H / 32,
+                            g.tile_n, g.n_tiles, g.k_stages, g.sf_chunks, sumsq, sumsq_count, ready, g.blocks128,
+                            status, stamps, task_next, zero_extra, zero_extra_count);
 }
 
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,

@@ -532,6 +532,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // The set-up above overlaps the prep kernel (a programmatic dependency): everything
+  // below reads its scale image or its cleared sums, counters and stamps.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // Every CTA of this persistent grid is resident: let the norm/RoPE pass launch now.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) atomicMin(&a.stamps[0], globaltimer_ns());
@@ -877,6 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers, TMEM and A-side scales of both CTAs are ready
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // prep complete (as above)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) atomicMin(&a.stamps[0], globaltimer_ns());
 
@@ -1060,8 +1064,18 @@ cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUte
   if (e != cudaSuccess) return e;
   const int tiles = g.m_tiles * g.n_tiles;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, kThreads, C::SMEM, s>>>(tmA, tmW, g, a);
-  return cudaGetLastError();
+  // a programmatic dependent of the prep kernel: the prologue overlaps it
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, g, a);
 }
 
 template <int BN, int kEpi, bool kFused>
@@ -1081,13 +1095,15 @@ cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the prep kernel
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, tmSF, g, a, nr);
 }
 

@@ -103,6 +103,9 @@ __global__ void __launch_bounds__(kQuantThreads, 10) row_quantize_kernel(const u
                                                                          float* __restrict__ scale,
                                                                          uint8_t* __restrict__ packed) {
   __shared__ uint32_t warp_max[2][kQuantThreads / 32];
+  // Inside a run the next kernel (the scale repack and clears) does not read what this
+  // one writes before it waits for it: it may start now.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
@@ -164,6 +167,7 @@ __global__ void __launch_bounds__(kQuantThreads, 10) row_quantize_kernel(const u
 __global__ void __launch_bounds__(kThreads) unpack_rows_kernel(const uint8_t* __restrict__ packed, int T, int H,
                                                                uint8_t* __restrict__ codes,
                                                                float* __restrict__ scale) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");  // as in row_quantize_kernel
   const int lane = threadIdx.x & 31;
   const int warp = static_cast<int>((blockIdx.x * static_cast<unsigned>(kThreads) + threadIdx.x) >> 5);
   const int n_warps = static_cast<int>((gridDim.x * static_cast<unsigned>(kThreads)) >> 5);
