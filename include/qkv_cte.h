@@ -119,7 +119,7 @@ enum { QKV_CTE_INPUT_ROW_FP8 = 0, QKV_CTE_INPUT_PACKED = 1, QKV_CTE_INPUT_BF16 =
 /* Per-head norms (QKV_CTE_NORM_HEAD_RMS / _LAYER): finish the norm and RoPE in the GEMM's
  * epilogue while each tile is in TMEM (tiles of whole heads, no second pass) instead
  * of the default: the GEMM writes per-(row, head) statistics (RMS: sum of squares;
- * LayerNorm: each tile part's mean and centred sum of squares) and the norm/RoPE pass
+ * LayerNorm: each tile part's shift, mean and centred sum of squares) and the norm/RoPE pass
  * finishes from them, which keeps the GEMM's wide tiles. Same results to rounding. */
 #define QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE 0x40u
 

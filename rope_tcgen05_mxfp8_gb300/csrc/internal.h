@@ -139,8 +139,9 @@ struct GemmArgs {
   // Per-head norm finished by the norm/RoPE pass: the epilogue writes per-(row, head)
   // statistics of the un-normalised Q/K. stats_kind 2 (RMS): sum(o^2) per (row, head),
   // accumulated with atomics (zeroed by prep). stats_kind 3 (LayerNorm): for each of
-  // the stat_parts tiles a head's columns can span, the part's (mean, M2) as a float2
-  // at ((row * heads + head) * stat_parts + part).
+  // the stat_parts tiles a head's columns can span, the part's (shift, mean, M2, 0) as
+  // a float4 at ((row * heads + head) * stat_parts + part); the part's Q/K values are
+  // handed over as o - shift (shift: the part's first value in the row).
   int stats_kind;
   float* head_stats;
   int stat_parts;

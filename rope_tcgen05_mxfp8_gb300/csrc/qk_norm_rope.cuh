@@ -139,42 +139,68 @@ __device__ __forceinline__ bool wait_panel_ready(const uint32_t* flag, uint32_t 
   }
 }
 
-// The per-head norm factors of head `hg` for row `t` from the GEMM's statistics. RMS:
-// from the head's sum of squares. LayerNorm: the (mean, M2) of each tile part of the
-// head's columns, combined with Chan, Golub and LeVeque's pairwise update (no large
-// sums subtracted); the hand-off holds each part's values centred on the part's mean,
-// so `shift_lo` / `shift_hi` (mean_part - mean_head of the parts holding this lane's
-// low and high chunk) turn them into deviations from the head's mean. Read through L2:
-// the GEMM writes them while this runs.
-__device__ __forceinline__ void head_factors(const NormRopeArgs& p, int t, int hg, int col_lo, int col_hi,
-                                             float& inv, float& shift_lo, float& shift_hi) {
-  const int d = p.d_head;
+// This lane's share of the GEMM's statistics for head `hg` of row `t`, loaded with the
+// head's hand-off chunks so the loads are in flight together. RMS: the head's sum of
+// squares in .x. LayerNorm: the (shift, mean, M2, -) of the head's tile part c (the
+// lane's chunk index), when the head has that part; the lanes of a row share them in
+// head_factors. Read through L2: the GEMM writes them while this runs.
+__device__ __forceinline__ float4 head_stats_share(const NormRopeArgs& p, int t, int hg, int c) {
   const int heads = p.n_q + p.n_kv;
+  if (p.head_kind == 2) return make_float4(__ldcg(p.head_stats + static_cast<size_t>(t) * heads + hg), 0.f, 0.f, 0.f);
+  const float4* st = reinterpret_cast<const float4*>(p.head_stats) + (static_cast<size_t>(t) * heads + hg) * p.stat_parts;
+  return c < p.stat_parts ? __ldcg(st + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// The per-head norm factors of head `hg` for row `t`. RMS: from the head's sum of
+// squares. LayerNorm: the parts' (mean, M2) are combined in part order with Chan,
+// Golub and LeVeque's pairwise update (no large sums subtracted); part i comes from
+// lane row_base + i of the row (its head_stats_share), or is loaded here when the row
+// has fewer lanes than parts. The hand-off holds each part's values centred on the
+// part's shift, so `shift_lo` / `shift_hi` (shift_part - mean_head of the parts holding
+// this lane's low and high chunk) turn them into deviations from the head's mean.
+// Called by the whole warp (the shuffles; the head is the same for every lane). Every
+// lane of a row repeats this per head, so it uses the fast reciprocal square root and
+// quotient (a few ulp, far below the bf16 rounding of the result).
+__device__ __forceinline__ void head_factors(const NormRopeArgs& p, int t, int hg, int col_lo, int col_hi, float4 share,
+                                             int row_base, int per_row, float inv_d, float& inv, float& shift_lo,
+                                             float& shift_hi) {
+  const int d = p.d_head;
   if (p.head_kind == 2) {
-    const float s2 = __ldcg(p.head_stats + static_cast<size_t>(t) * heads + hg);
-    inv = 1.0f / sqrtf(s2 / static_cast<float>(d) + p.eps);
+    inv = rsqrtf(fmaf(share.x, inv_d, p.eps));
     shift_lo = shift_hi = 0.0f;
     return;
   }
+  const int heads = p.n_q + p.n_kv;
   const int hs = hg * d;
   const int t0 = hs / p.tile_n;
-  const float2* st = reinterpret_cast<const float2*>(p.head_stats) + (static_cast<size_t>(t) * heads + hg) * p.stat_parts;
-  float n = 0.0f, m = 0.0f, m2 = 0.0f;
+  const int part_lo = col_lo / p.tile_n - t0, part_hi = col_hi / p.tile_n - t0;
+  const float4* st = reinterpret_cast<const float4*>(p.head_stats) + (static_cast<size_t>(t) * heads + hg) * p.stat_parts;
+  float n = 0.0f, m = 0.0f, m2 = 0.0f, c_lo = 0.0f, c_hi = 0.0f;
   for (int i = 0; i < p.stat_parts; ++i) {
     const int lo = max(hs, (t0 + i) * p.tile_n);
     const int hi = min(hs + d, (t0 + i + 1) * p.tile_n);
-    if (lo >= hi) break;
+    if (lo >= hi) break;  // the same for the whole warp
+    float4 part;
+    if (i < per_row) {
+      part.x = __shfl_sync(0xffffffffu, share.x, row_base + i);
+      part.y = __shfl_sync(0xffffffffu, share.y, row_base + i);
+      part.z = __shfl_sync(0xffffffffu, share.z, row_base + i);
+    } else {
+      part = __ldcg(st + i);
+    }
     const float ni = static_cast<float>(hi - lo);
-    const float2 part = __ldcg(st + i);
     const float nn = n + ni;
-    const float delta = part.x - m;
-    m += delta * (ni / nn);
-    m2 += part.y + delta * delta * (n * ni / nn);
+    const float w = __fdividef(ni, nn);
+    const float delta = part.y - m;
+    m = fmaf(delta, w, m);
+    m2 += part.z + delta * delta * (n * w);
     n = nn;
+    if (i == part_lo) c_lo = part.x;
+    if (i == part_hi) c_hi = part.x;
   }
-  inv = 1.0f / sqrtf(m2 / static_cast<float>(d) + p.eps);
-  shift_lo = __ldcg(st + (col_lo / p.tile_n - t0)).x - m;
-  shift_hi = __ldcg(st + (col_hi / p.tile_n - t0)).x - m;
+  inv = rsqrtf(fmaf(m2, inv_d, p.eps));
+  shift_lo = c_lo - m;
+  shift_hi = c_hi - m;
 }
 
 // One task, called by a whole warp once its panel is known to be complete. kHeadStats:
@@ -204,6 +230,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
   (void)ld_acquire(p.ready + panel);  // each lane acquires the panel's publication
   const int tr = t < p.T ? t : p.T - 1;
 
+  const float inv_d = 1.0f / static_cast<float>(d);  // per-head norms
   float inv_q = 1.0f, inv_k = 1.0f;
   if (p.norm && !kHeadStats) {
     inv_q = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr)] / static_cast<float>(p.n_q * d) + p.eps);
@@ -226,6 +253,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
   const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (t & 127);
   for (int hg0 = h_begin; hg0 < h_end; hg0 += kHeadBatch) {
     RawChunk raw_lo[kHeadBatch], raw_hi[kHeadBatch];
+    float4 share[kHeadBatch];  // per-head norms: this lane's share of the statistics
 #pragma unroll
     for (int k = 0; k < kHeadBatch; ++k) {
       const int hg = hg0 + k;
@@ -236,6 +264,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
       const size_t i_hi = idx0 + static_cast<size_t>((col + half) >> 4) * 128;
       load_raw(p.qk_val + i_lo * 16, p.qk_exp + i_lo, raw_lo[k], once);
       load_raw(p.qk_val + i_hi * 16, p.qk_exp + i_hi, raw_hi[k], once);
+      if constexpr (kHeadStats) share[k] = head_stats_share(p, tr, hg, c);
     }
 #pragma unroll
     for (int k = 0; k < kHeadBatch; ++k) {
@@ -249,7 +278,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
       decode16(raw_hi[k], hi);
       if constexpr (kHeadStats) {  // per-head norm: (y - mean) * inv * gamma[d_head]
         float inv, shift_lo, shift_hi;
-        head_factors(p, tr, hg, col, col + half, inv, shift_lo, shift_hi);
+        head_factors(p, tr, hg, col, col + half, share[k], lane - c, per_row, inv_d, inv, shift_lo, shift_hi);
         const uint16_t* gamma = (seg ? p.gamma_k : p.gamma_q) + c * 16;
         float g[8];
 #pragma unroll

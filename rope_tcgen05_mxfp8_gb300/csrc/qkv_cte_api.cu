@@ -280,7 +280,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   size_t stats_bytes = 0;
   if (per_head_norm(d) && !head_norm_in_epilogue(d))
     stats_bytes = hand_rows * qk_heads *
-                  (d.norm == QKV_CTE_NORM_HEAD_RMS ? sizeof(float) : 2 * sizeof(float) * stat_parts(d.d_head, tile_n));
+                  (d.norm == QKV_CTE_NORM_HEAD_RMS ? sizeof(float) : 4 * sizeof(float) * stat_parts(d.d_head, tile_n));
   w.act_off = w.stats_off + align_up(stats_bytes, 256);
   const bool produced = d.input_layout != QKV_CTE_INPUT_ROW_FP8;
   w.act_scale_off = w.act_off + (produced ? align_up((size_t)g.T * g.H, 256) : 0);

@@ -297,39 +297,27 @@ __device__ __forceinline__ void store_handoff16(const GemmArgs& a, size_t idx, c
 }
 
 // Close one part of a Q/K head (its columns c0..c1 in this tile) for the per-head
-// statistics. RMS adds the part's sum of squares to the (row, head) total. LayerNorm
-// stores the part's mean and its centred sum of squares M2, taken in a second pass over
-// the part's accumulator columns, and hands the part's values over centred on that
-// mean (o - mean_part): a large common offset would otherwise leave the deviations
-// LayerNorm amplifies below the hand-off's resolution. The norm/RoPE pass adds
-// mean_part - mean_head back, and combines the parts with Chan et al.'s pairwise
-// update, so no large sums are subtracted anywhere.
-template <int BN>
-__device__ __forceinline__ void stats_flush(const GemmShape& g, const GemmArgs& a, uint32_t t_acc, int col_base,
-                                            int row, bool row_ok, float ascale, size_t qk_row_idx, int head, int c0,
-                                            int c1, float s1, float s2) {
+// statistics. RMS adds the part's sum of squares to the (row, head) total. LayerNorm:
+// the drain has taken the part in one pass, centred on the part's first value `shift`
+// (s1 = sum(o - shift), s2 = sum((o - shift)^2)) and has handed the values over
+// centred the same way, so a large common offset cannot push the deviations LayerNorm
+// amplifies below the hand-off's resolution, and the part's M2 = s2 - s1^2/n loses
+// only the bits of (mean - shift)^2 / variance. The part's (shift, mean, M2) go to the
+// statistics; the norm/RoPE pass combines the parts with Chan et al.'s pairwise update
+// (no large sums subtracted) and adds shift - mean_head back.
+__device__ __forceinline__ void stats_flush(const GemmArgs& a, int row, bool row_ok, int head, int part, int c0,
+                                            int c1, float s1, float s2, float shift) {
+  if (!row_ok) return;
   const int heads = a.k_end / a.d_head;
   if (a.stats_kind == 2) {
-    if (row_ok) atomicAdd(&a.head_stats[static_cast<size_t>(row) * heads + head], s2);
+    atomicAdd(&a.head_stats[static_cast<size_t>(row) * heads + head], s2);
     return;
   }
-  const float mean = s1 / static_cast<float>(c1 - c0);
-  float m2 = 0.0f;
-  for (int c = c0; c < c1; c += 16) {
-    float v[16];
-    projected16(a, t_acc + static_cast<uint32_t>(c - col_base), ascale, c, v);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      v[j] -= mean;
-      m2 = fmaf(v[j], v[j], m2);
-    }
-    store_handoff16(a, qk_row_idx + static_cast<size_t>(c >> 4) * 128, v);
-  }
-  if (row_ok) {
-    const int part = col_base / BN - (head * a.d_head) / BN;
-    reinterpret_cast<float2*>(a.head_stats)[(static_cast<size_t>(row) * heads + head) * a.stat_parts + part] =
-        make_float2(mean, m2);
-  }
+  const float n = static_cast<float>(c1 - c0);
+  const float dm = s1 / n;  // mean - shift
+  const float m2 = fmaxf(fmaf(-s1, dm, s2), 0.0f);
+  reinterpret_cast<float4*>(a.head_stats)[(static_cast<size_t>(row) * heads + head) * a.stat_parts + part] =
+      make_float4(shift, shift + dm, m2, 0.0f);
 }
 
 // kStats: 0 none, 2 per-head RMS statistics, 3 per-head LayerNorm statistics.
@@ -345,7 +333,7 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
   ss_q = 0.0f;
   ss_k = 0.0f;
   int st_head = -1, st_c0 = 0, st_c1 = 0;  // the open head part (kStats)
-  float st_s1 = 0.0f, st_s2 = 0.0f;
+  float st_s1 = 0.0f, st_s2 = 0.0f, st_shift = 0.0f;
 #pragma unroll
   for (int c0 = 0; c0 < BN; c0 += 32) {
     uint32_t r[32];
@@ -406,26 +394,34 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
           const int hh = col0 / a.d_head;  // uniform across the warp
           if (hh != st_head) {
             if (st_head >= 0)
-              stats_flush<BN>(g, a, t_acc, col_base, row, row_ok, ascale, qk_row_idx, st_head, st_c0, st_c1, st_s1,
-                              st_s2);
+              stats_flush(a, row, row_ok, st_head, col_base / BN - (st_head * a.d_head) / BN, st_c0, st_c1, st_s1,
+                          st_s2, st_shift);
             st_head = hh;
             st_c0 = col0;
             st_s1 = st_s2 = 0.0f;
+            if constexpr (kStats == 3) st_shift = v[0];
           }
-          if constexpr (kStats == 3) {  // LayerNorm also needs the part's sum
-            float s1 = 0.0f;
+          if constexpr (kStats == 3) {  // LayerNorm: centred on the part's first value
+            float2 s1 = make_float2(0.0f, 0.0f), s2 = make_float2(0.0f, 0.0f);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) s1 += v[j];
-            st_s1 += s1;
+            for (int j = 0; j < 8; ++j) {
+              const float2 dv = make_float2(v[2 * j] - st_shift, v[2 * j + 1] - st_shift);
+              v[2 * j] = dv.x;
+              v[2 * j + 1] = dv.y;
+              s1 = make_float2(s1.x + dv.x, s1.y + dv.y);
+              s2 = ffma2(dv, dv, s2);
+            }
+            st_s1 += s1.x + s1.y;
+            st_s2 += s2.x + s2.y;
+          } else {
+            st_s2 += sq;
           }
-          st_s2 += sq;
           st_c1 = col0 + 16;
         }
       }
       if (a.qk_val != nullptr && col0 < a.k_end) {
-        // Q/K columns the norm/RoPE pass will finish (LayerNorm statistics hand them
-        // over centred, from stats_flush)
-        if (kStats != 3) store_handoff16(a, qk_row_idx + static_cast<size_t>(col0 >> 4) * 128, v);
+        // Q/K columns the norm/RoPE pass will finish (centred for the LayerNorm statistics)
+        store_handoff16(a, qk_row_idx + static_cast<size_t>(col0 >> 4) * 128, v);
       } else if (row_ok) {
         uint32_t packed[8];
 #pragma unroll
@@ -437,7 +433,8 @@ __device__ __forceinline__ void epilogue_drain_plain(const GemmShape& g, const G
   }
   if constexpr (kStats != 0) {
     if (st_head >= 0)
-      stats_flush<BN>(g, a, t_acc, col_base, row, row_ok, ascale, qk_row_idx, st_head, st_c0, st_c1, st_s1, st_s2);
+      stats_flush(a, row, row_ok, st_head, col_base / BN - (st_head * a.d_head) / BN, st_c0, st_c1, st_s1, st_s2,
+                  st_shift);
   }
 }
 

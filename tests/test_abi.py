@@ -158,7 +158,7 @@ def test_per_head_norm_workspace():
     assert sizes["across"] - sizes["epi"] == hand_off
     assert sizes["rms"] - sizes["across"] == align(rows * 8 * 4)
     parts = (128 + 128 - 2) // 128 + 1          # tiles a 128-column head can touch at tile 128
-    assert sizes["ln"] - sizes["across"] == align(rows * 8 * parts * 8)
+    assert sizes["ln"] - sizes["across"] == align(rows * 8 * parts * 16)
 
 
 def test_plan_info_reports_the_choices():
