@@ -23,13 +23,17 @@ enum : uint32_t {
 //   [0, 256)                 status word (offset 0); at kStampOffset four uint64
 //                            %globaltimer stamps: K1 first start, K1 last end, norm/RoPE
 //                            first start, norm/RoPE last end; at kTaskCounterOffset the
-//                            norm/RoPE task counter of the fused GEMM
+//                            counter the norm/RoPE tasks are claimed from
 //   [256, 256 + ss_bytes)    fp32 [T, 2] sum-of-squares accumulator (used when the
 //                            caller passes no sumsq buffer)
 //   [.., + sf_bytes)         W's UE8M0 scales repacked per (N tile, K stage) in the
 //                            order the MMA's scale-factor copy consumes them
 //   [.., + ready_bytes)      uint32 [blocks128]: per 128-row block, how many epilogue
 //                            warp-tiles of K1's Q/K tiles have finished (4 per tile)
+//   [.., + 4 * kSmTable)     uint32 per SM (%smid): the mask of SM sub-partitions
+//                            (%warpid & 3) K1's TMA-load and MMA-issue warps occupy while
+//                            K1's CTA there runs, 0 otherwise (a scheduling hint for
+//                            the norm/RoPE pass)
 //   [.., + qk_bytes)         the un-normalised Q and K columns handed from K1 to K2
 //                            (only when a norm/RoPE pass runs) in block floating
 //                            point: per row and 16-column chunk, one power-of-two
@@ -43,10 +47,12 @@ enum : uint32_t {
 //   [.., + T*H), [.., + 4T)  only for a packed or bf16 input: the e4m3 codes [T, H] and
 //                            fp32 row scales [T] the producer step writes for the GEMM
 constexpr size_t kStampOffset = 64;
-constexpr size_t kTaskCounterOffset = 128;  // uint32: next norm/RoPE task the GEMM's epilogue warps claim
+constexpr size_t kTaskCounterOffset = 128;  // uint32: the next unclaimed norm/RoPE task
+constexpr int kSmTable = 1024;              // entries of the per-SM sub-partition table
 
 struct WorkspaceLayout {
-  size_t status_off, sumsq_off, sf_off, ready_off, qk_off, qk_exp_off, stats_off, act_off, act_scale_off, total;
+  size_t status_off, sumsq_off, sf_off, ready_off, sm_busy_off, qk_off, qk_exp_off, stats_off, act_off, act_scale_off,
+      total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -121,6 +127,7 @@ struct GemmArgs {
   uint8_t* qk_exp;           // Q/K hand-off exponent bytes
   float* sumsq;              // may be null: then no sum of squares is accumulated
   uint32_t* ready;           // per-panel completion counters (K2 overlaps K1 on them)
+  uint32_t* sm_busy;         // [kSmTable] sub-partitions of this kernel's load and MMA warps, per SM
   unsigned long long* stamps;  // [0] first CTA start (min), [1] last CTA end (max)
   uint32_t* status;
   int q_end, k_end;          // Q = [0, q_end), K = [q_end, k_end), V = [k_end, I)
@@ -172,10 +179,11 @@ struct NormRopeArgs {
   float* inv_rms;            // may be null
   int nbsd;                  // O layout (see GemmArgs)
   const uint32_t* ready;     // per 128-row panel: K1 epilogue warp-tiles finished
+  const uint32_t* sm_busy;   // [kSmTable] K1's load/MMA sub-partitions per SM (0: no K1 CTA there)
   uint32_t ready_target;     // 4 * K1's Q/K tiles: the panel's Q and K are final
   unsigned long long* stamps;  // [0] first block start (min), [1] last block end (max)
   uint32_t* status;
-  uint32_t* task_next;       // next unclaimed task (the GEMM's epilogue warps claim them)
+  uint32_t* task_next;       // next unclaimed task (claimed by K2's warps, or by the fused GEMM's epilogue warps)
   // per-head norm (norm 2 RMS / 3 LayerNorm) from the GEMM's per-(row, head)
   // statistics (see GemmArgs); 0: the across-heads norm or none
   int head_kind;
@@ -191,7 +199,8 @@ size_t gemm_smem_bytes(int tile_n);
 
 // Launchers. Each returns cudaSuccess or the launch error.
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
-                        size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
+                        size_t sumsq_count, uint32_t* ready, uint32_t* sm_busy, uint32_t* status,
+                        unsigned long long* stamps,
                         uint32_t* task_next, float* zero_extra, size_t zero_extra_count, cudaStream_t s,
                         int num_sms, bool after_producer);
 // K1. tmSF: the repacked scales as a uint32 [n_tiles * k_stages, sf_chunks * 128] map

@@ -7,6 +7,12 @@
 // CTAs and take each task once K1's counter says the task's 128-row panel is complete
 // (a bounded acquire wait), so it mostly hides under the GEMM. Alone (serial flag) it
 // is an HBM-bound pass over the hand-off.
+//
+// Warps claim tasks in order from a counter. A warp that shares its SM sub-partition
+// with the TMA-load or MMA-issue warp of the K1 CTA on its SM (K1 publishes them per
+// SM) holds back until that CTA has finished, then joins for the tasks left: sharing
+// those schedulers slows the GEMM about twice as much per unit of this work as running
+// on the other two sub-partitions.
 #include "qk_norm_rope.cuh"
 
 namespace qkvcte {
@@ -16,20 +22,41 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kHeadGroup = 20;  // heads per warp task: small tasks keep the warps evenly loaded to the end
 
+// Lane 0: hold back (bounded) while the K1 CTA on this SM occupies this warp's
+// sub-partition with its load or MMA warp and tasks remain.
+__device__ __forceinline__ void defer_while_busy(const NormRopeArgs& p, long long tasks) {
+  if (p.sm_busy == nullptr) return;
+  const uint32_t* busy = p.sm_busy + (nrp::sm_id() & (kSmTable - 1));
+  const uint32_t bit = 1u << (nrp::warp_slot() & 3);
+  if (!(nrp::ld_relaxed(busy) & bit)) return;
+  const unsigned long long t0 = nrp::now_ns();
+  while (true) {
+    __nanosleep(2000);
+    if (!(nrp::ld_relaxed(busy) & bit)) return;
+    if (static_cast<long long>(nrp::ld_relaxed(p.task_next)) >= tasks) return;
+    if (nrp::now_ns() - t0 > nrp::kWaitLimitNs) return;  // a hint only: go ahead
+  }
+}
+
 template <bool kHeadStats>
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_constant__ NormRopeArgs p) {
   if (threadIdx.x == 0) atomicMin(&p.stamps[0], nrp::now_ns());
   const int lane = threadIdx.x & 31;
   const long long tasks = nrp::task_count(p, kHeadGroup);
-  const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
+  if (lane == 0) defer_while_busy(p, tasks);
+  __syncwarp();
   // Read-once hand-off and write-once output: first out of L2, so the GEMM's
   // L2-resident weight band running beside this pass keeps its place.
   const uint64_t once = nrp::evict_first_policy();
-  for (long long task = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5); task < tasks;
-       task += warps) {
-    const int panel = nrp::task_panel(p, task, kHeadGroup);
+  while (true) {
+    long long task = 0;
     int ok = 1;
-    if (lane == 0) ok = nrp::wait_panel_ready(p.ready + panel, p.ready_target) ? 1 : 0;
+    if (lane == 0) {
+      task = atomicAdd(p.task_next, 1u);
+      if (task < tasks) ok = nrp::wait_panel_ready(p.ready + nrp::task_panel(p, task, kHeadGroup), p.ready_target);
+    }
+    task = __shfl_sync(0xffffffffu, task, 0);
+    if (task >= tasks) break;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (!ok) {
       if (lane == 0) atomicOr(p.status, kErrNormReadyWait);

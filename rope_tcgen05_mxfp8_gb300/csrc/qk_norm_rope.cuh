@@ -41,6 +41,27 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The SM this thread runs on, and its warp's hardware slot there: the slot's low two
+// bits name the SM sub-partition (the warp scheduler) the warp issues from. Both are
+// where the warp is now; they serve as scheduling hints only.
+__device__ __forceinline__ uint32_t sm_id() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(v));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t warp_slot() {
+  uint32_t v;
+  asm volatile("mov.u32 %0, %%warpid;" : "=r"(v));
+  return v;
+}
+
 __device__ __forceinline__ unsigned long long now_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

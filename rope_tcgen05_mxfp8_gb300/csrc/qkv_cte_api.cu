@@ -266,7 +266,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   w.sumsq_off = 256;
   w.sf_off = w.sumsq_off + align_up((size_t)g.T * 2 * sizeof(float), 256);
   w.ready_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
-  w.qk_off = w.ready_off + align_up((size_t)g.blocks128 * sizeof(uint32_t), 256);
+  w.sm_busy_off = w.ready_off + align_up((size_t)g.blocks128 * sizeof(uint32_t), 256);
+  w.qk_off = w.sm_busy_off + align_up((size_t)kSmTable * sizeof(uint32_t), 256);
   // The norm/RoPE pass (and its hand-off) runs for the across-heads norm, or RoPE
   // without a norm; the per-head norms finish in the GEMM's epilogue.
   const bool second_pass = !head_norm_in_epilogue(d) && (d.norm != QKV_CTE_NORM_NONE || d.rope);
@@ -427,6 +428,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "producer launch: %s", cudaGetErrorString(e));
 
   uint32_t* ready = reinterpret_cast<uint32_t*>(ws + plan->ws.ready_off);
+  uint32_t* sm_busy = reinterpret_cast<uint32_t*>(ws + plan->ws.sm_busy_off);
   unsigned long long* stamps = reinterpret_cast<unsigned long long*>(ws + kStampOffset);
   uint32_t* task_next = reinterpret_cast<uint32_t*>(ws + kTaskCounterOffset);
   const bool head_stats = per_head_norm(d) && !head_norm_in_epilogue(d);
@@ -434,7 +436,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   // the RMS statistics are sums accumulated with atomics: they start at zero
   const size_t zero_stats =
       head_stats && d.norm == QKV_CTE_NORM_HEAD_RMS ? (size_t)g.blocks128 * 128 * (d.n_q_heads + d.n_kv_heads) : 0;
-  e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0, ready, status,
+  e = launch_prep(g, w_sf, sf_packed, need_ss ? ss : nullptr, need_ss ? (size_t)g.T * 2 : 0, ready, sm_busy, status,
                   stamps, task_next, stats, zero_stats, s, dev.sms, produced);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "prep launch: %s", cudaGetErrorString(e));
 
@@ -450,6 +452,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.qk_exp = qk_exp;
   ga.sumsq = need_ss ? ss : nullptr;
   ga.ready = ready;
+  ga.sm_busy = sm_busy;
   ga.stamps = stamps;
   ga.status = status;
   ga.q_end = plan->q_end;
@@ -487,6 +490,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.inv_rms = inv_rms;
   na.nbsd = d.output_layout == QKV_CTE_LAYOUT_NBSD ? 1 : 0;
   na.ready = ready;
+  na.sm_busy = sm_busy;
   na.ready_target = 4u * (uint32_t)g.n_qk_tiles;
   na.status = status;
   na.stamps = stamps + 2;

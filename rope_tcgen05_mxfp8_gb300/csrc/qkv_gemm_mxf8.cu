@@ -19,7 +19,8 @@ namespace {
 // consecutive rows: 4 * kPrepStages contiguous bytes each) into shared memory and
 // write the blocks from there, so both sides are coalesced. Every block then takes a
 // share of the clears: the sum-of-squares buffer, the extra statistics, the panel
-// counters, the status word, the task counter and the timing stamps. Launched as a
+// counters, the per-SM sub-partition table, the status word, the task counter and the
+// timing stamps. Launched as a
 // programmatic dependent of a producer kernel (bf16 or packed activations), this
 // kernel does its own work beside it and waits for it before it ends, so the GEMM,
 // which waits for this kernel, also finds the producer's output complete.
@@ -29,8 +30,8 @@ constexpr int kPrepStages = 8;
 __global__ void __launch_bounds__(kPrepThreads) qkv_prep_kernel(
     const uint8_t* __restrict__ w_sf, uint32_t* __restrict__ packed, int I, int k_blocks, int tile_n, int n_tiles,
     int k_stages, int sf_chunks, float* __restrict__ sumsq, size_t sumsq_count, uint32_t* __restrict__ ready,
-    int m_tiles, uint32_t* status, unsigned long long* stamps, uint32_t* task_next, float* __restrict__ zero_extra,
-    size_t zero_extra_count) {
+    int m_tiles, uint32_t* __restrict__ sm_busy, uint32_t* status, unsigned long long* stamps, uint32_t* task_next,
+    float* __restrict__ zero_extra, size_t zero_extra_count) {
   __shared__ uint32_t rows[256][kPrepStages + 1];  // +1: the column reads below hit 32 banks
   const int groups = (k_stages + kPrepStages - 1) / kPrepStages;
   if (static_cast<int>(blockIdx.x) < n_tiles * groups) {
@@ -64,6 +65,7 @@ __global__ void __launch_bounds__(kPrepThreads) qkv_prep_kernel(
     for (size_t i = first; i < zero_extra_count; i += stride) zero_extra[i] = 0.0f;
   }
   for (size_t i = first; i < static_cast<size_t>(m_tiles); i += stride) ready[i] = 0u;
+  for (size_t i = first; i < static_cast<size_t>(kSmTable); i += stride) sm_busy[i] = 0u;
   if (first == 0) {
     status[0] = 0u;
     *task_next = 0u;
@@ -103,13 +105,14 @@ size_t gemm_smem_bytes(int tile_n) {
 }
 
 cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_packed, float* sumsq,
-                        size_t sumsq_count, uint32_t* ready, uint32_t* status, unsigned long long* stamps,
-                        uint32_t* task_next, float* zero_extra, size_t zero_extra_count, cudaStream_t s,
-                        int num_sms, bool after_producer) {
+                        size_t sumsq_count, uint32_t* ready, uint32_t* sm_busy, uint32_t* status,
+                        unsigned long long* stamps, uint32_t* task_next, float* zero_extra, size_t zero_extra_count,
+                        cudaStream_t s, int num_sms, bool after_producer) {
   if (g.tile_n > kPrepThreads) return cudaErrorInvalidValue;
   const size_t repack = static_cast<size_t>(g.n_tiles) * ((g.k_stages + kPrepStages - 1) / kPrepStages);
   size_t clear = sumsq_count > zero_extra_count / 4 ? sumsq_count : zero_extra_count / 4;
   if (clear < static_cast<size_t>(g.blocks128)) clear = static_cast<size_t>(g.blocks128);
+  if (clear < static_cast<size_t>(kSmTable)) clear = static_cast<size_t>(kSmTable);
   size_t blocks = (clear + kPrepThreads - 1) / kPrepThreads;
   const size_t cap = static_cast<size_t>(num_sms) * 4;
   if (blocks > cap) blocks = cap;
@@ -127,7 +130,7 @@ cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_pac
   cfg.numAttrs = after_producer ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, qkv_prep_kernel, w_sf, reinterpret_cast<uint32_t*>(sf_packed), g.I, g.H / 32,
                             g.tile_n, g.n_tiles, g.k_stages, g.sf_chunks, sumsq, sumsq_count, ready, g.blocks128,
-                            status, stamps, task_next, zero_extra, zero_extra_count);
+                            sm_busy, status, stamps, task_next, zero_extra, zero_extra_count);
 }
 
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,

@@ -478,6 +478,17 @@ __device__ __forceinline__ void epilogue_publish(const GemmShape& g, const GemmA
   }
 }
 
+// Record in the per-SM table which sub-partitions this CTA's TMA-load and MMA-issue
+// warps occupy (0 when the CTA is done). The norm/RoPE pass, running beside the GEMM,
+// keeps its warps off those two while the CTA runs: sharing a scheduler with them slows
+// the GEMM three times as much as running on the other two. Only a hint: nothing waits
+// for it to be exact. Called by thread 0 after prep (which clears the table).
+__device__ __forceinline__ void publish_busy(const GemmArgs& a, uint32_t mask) {
+  if (threadIdx.x != 0 || a.sm_busy == nullptr) return;
+  a.sm_busy[nrp::sm_id() & (kSmTable - 1)] = mask;
+  __threadfence();
+}
+
 template <int BN, int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_mxf8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
@@ -496,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* busy_slot = tmem_slot + 2;  // [2]: sub-partition bits of the load and MMA warps
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -524,6 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     reinterpret_cast<uint32_t*>(sSFA)[threadIdx.x - 64] = 0x7F7F7F7Fu;
     fence_proxy_async_smem();
   }
+  if (warp <= 1 && lane == 0) busy_slot[warp] = 1u << (nrp::warp_slot() & 3);
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -532,6 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The set-up above overlaps the prep kernel (a programmatic dependency): everything
   // below reads its scale image or its cleared sums, counters and stamps.
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  publish_busy(a, busy_slot[0] | busy_slot[1]);
   // Every CTA of this persistent grid is resident: let the norm/RoPE pass launch now.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) atomicMin(&a.stamps[0], globaltimer_ns());
@@ -689,7 +703,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) atomicMax(&a.stamps[1], globaltimer_ns());
+  if (threadIdx.x == 0) {
+    atomicMax(&a.stamps[1], globaltimer_ns());
+    publish_busy(a, 0u);  // this SM's sub-partitions are free for the norm/RoPE pass
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -839,6 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = tempty + 2;                               // leader
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint32_t* busy_slot = tmem_slot + 2;  // [2]: sub-partition bits of the load and MMA warps
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -871,6 +889,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     reinterpret_cast<uint32_t*>(sSFA)[threadIdx.x - 64] = 0x7F7F7F7Fu;  // A-side scales: 2^0
     fence_proxy_async_smem();
   }
+  // the load warp's sub-partition, and the MMA issuer's (the leader's MMA warp only)
+  if (warp <= 1 && lane == 0) busy_slot[warp] = (warp == 0 || leader) ? 1u << (nrp::warp_slot() & 3) : 0u;
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -878,6 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   asm volatile("griddepcontrol.wait;" ::: "memory");  // prep complete (as above)
+  publish_busy(a, busy_slot[0] | busy_slot[1]);
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) atomicMin(&a.stamps[0], globaltimer_ns());
 
@@ -1048,7 +1069,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) atomicMax(&a.stamps[1], globaltimer_ns());
+  if (threadIdx.x == 0) {
+    atomicMax(&a.stamps[1], globaltimer_ns());
+    publish_busy(a, 0u);  // this SM's sub-partitions are free for the norm/RoPE pass
+  }
 }
 
 template <int BN, int kEpi>

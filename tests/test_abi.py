@@ -210,6 +210,7 @@ def test_workspace_size_formula(input_layout):
         kq = (nq + nkv) * 128
         qk = -(-(rows * kq * 2) // 256) * 256 + -(-(rows * kq // 16) // 256) * 256  # hand-off
         ready = -(-(-(-T // 128) * 4) // 256) * 256        # per-panel counters
+        ready += 1024 * 4                                   # per-SM sub-partition table
         # a packed or bf16 input: the producer's codes [T, H] and row scales [T]
         act = (-(-(T * 5120) // 256) * 256 + -(-(T * 4) // 256) * 256) if input_layout else 0
         assert ws == 256 + ss + -(-sf // 256) * 256 + ready + qk + act
