@@ -180,6 +180,7 @@ struct NormRopeArgs {
   int nbsd;                  // O layout (see GemmArgs)
   const uint32_t* ready;     // per 128-row panel: K1 epilogue warp-tiles finished
   const uint32_t* sm_busy;   // [kSmTable] K1's load/MMA sub-partitions per SM (0: no K1 CTA there)
+  int claim;                 // 1: claim tasks from task_next, off K1's load/MMA sub-partitions; 0: stride
   uint32_t ready_target;     // 4 * K1's Q/K tiles: the panel's Q and K are final
   unsigned long long* stamps;  // [0] first block start (min), [1] last block end (max)
   uint32_t* status;

@@ -8,11 +8,14 @@
 // (a bounded acquire wait), so it mostly hides under the GEMM. Alone (serial flag) it
 // is an HBM-bound pass over the hand-off.
 //
-// Warps claim tasks in order from a counter. A warp that shares its SM sub-partition
-// with the TMA-load or MMA-issue warp of the K1 CTA on its SM (K1 publishes them per
-// SM) holds back until that CTA has finished, then joins for the tasks left: sharing
-// those schedulers slows the GEMM about twice as much per unit of this work as running
-// on the other two sub-partitions.
+// Beside K1, warps claim tasks in order from a counter. A warp that shares its SM
+// sub-partition with the TMA-load or MMA-issue warp of the K1 CTA on its SM (K1
+// publishes them per SM) holds back until that CTA has finished, then joins for the
+// tasks left: sharing those schedulers slows the GEMM about twice as much per unit of
+// this work as running on the other two sub-partitions. The per-head norms' tasks are
+// heavier (the statistics of every head): with fewer warps they would fall behind the
+// GEMM, so there, as when the pass runs alone, every warp takes every gridDim-th task
+// (no counter on the critical path).
 #include "qk_norm_rope.cuh"
 
 namespace qkvcte {
@@ -43,16 +46,17 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
   if (threadIdx.x == 0) atomicMin(&p.stamps[0], nrp::now_ns());
   const int lane = threadIdx.x & 31;
   const long long tasks = nrp::task_count(p, kHeadGroup);
-  if (lane == 0) defer_while_busy(p, tasks);
+  if (p.claim && lane == 0) defer_while_busy(p, tasks);
   __syncwarp();
   // Read-once hand-off and write-once output: first out of L2, so the GEMM's
   // L2-resident weight band running beside this pass keeps its place.
   const uint64_t once = nrp::evict_first_policy();
+  const long long warps = static_cast<long long>(gridDim.x) * (kThreads / 32);
+  long long task = static_cast<long long>(blockIdx.x) * (kThreads / 32) + (threadIdx.x >> 5) - warps;
   while (true) {
-    long long task = 0;
     int ok = 1;
     if (lane == 0) {
-      task = atomicAdd(p.task_next, 1u);
+      task = p.claim ? static_cast<long long>(atomicAdd(p.task_next, 1u)) : task + warps;
       if (task < tasks) ok = nrp::wait_panel_ready(p.ready + nrp::task_panel(p, task, kHeadGroup), p.ready_target);
     }
     task = __shfl_sync(0xffffffffu, task, 0);
@@ -97,7 +101,9 @@ cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
+  NormRopeArgs args = a;
+  args.claim = overlap && a.head_kind == 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args);
 }
 
 }  // namespace qkvcte

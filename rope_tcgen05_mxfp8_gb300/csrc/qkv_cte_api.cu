@@ -470,7 +470,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.gamma_k = gamma_k;
   ga.cos_t = cos_table;
   ga.sin_t = sin_table;
-  NormRopeArgs na;
+  NormRopeArgs na{};
   na.T = g.T;
   na.I = g.I;
   na.n_q = d.n_q_heads;
