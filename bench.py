@@ -44,7 +44,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--steps", type=int, default=100)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="wan480p")
@@ -63,7 +63,7 @@ def _args():
     p.add_argument("--e2e-chunk", type=int, default=0, help="row chunk of the host-streaming e2e leg (0: the library's 2048)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
-    p.add_argument("--cpu-rows", type=int, default=4096, help="oracle row sample for cpu_baseline")
+    p.add_argument("--cpu-rows", type=int, default=12288, help="oracle row sample for cpu_baseline")
     p.add_argument("--ref-rows", type=int, default=256, help="oracle row sample per reference step")
     return p.parse_args()
 
@@ -94,16 +94,19 @@ def _blas_threads():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 200 ms during the timed region."""
+    """nvidia-smi clock / throttle-reason samples every 20 ms, kept only when their
+    timestamp falls inside the timed region (mark_start / mark_end)."""
 
-    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+    FIELDS = ["timestamp", "index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+    PERIOD_MS = 20
 
     def __init__(self, gpu_id: str):
         self.gpu_id = gpu_id
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -112,9 +115,27 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)], stdout=self.out,
+                stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _epoch(stamp):
+        import datetime
+
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()  # nvidia-smi prints local time
+            except ValueError:
+                pass
+        return None
 
     def stop(self):
         if self.proc is None:
@@ -132,18 +153,33 @@ class ClockSampler:
                 if len(parts) == len(self.FIELDS):
                     rows.append(parts)
         os.unlink(self.path)
+        return self.summarise(rows, self.t0, self.t1)
+
+    @classmethod
+    def summarise(cls, rows, t0=None, t1=None):
+        """Median SM clock, max clock and the throttle reasons seen, over the samples
+        taken between t0 and t1 (epoch seconds); all samples if none fall inside."""
         if not rows:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        inside = rows
+        if t0 is not None and t1 is not None:
+            stamped = [(cls._epoch(r[0]), r) for r in rows]
+            inside = [r for t, r in stamped if t is not None and t0 <= t <= t1]
+        used = inside if inside else rows
+        sm = [float(r[2]) for r in used if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in used if r[3].replace(".", "").isdigit()]
         reasons = set()
-        for r in rows:
+        for r in used:
             for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
-                                 r[5:9]):
+                                 r[6:10]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": sorted(reasons), "samples": len(used),
+               "window": "timed region" if inside else "no sample fell inside the timed region: all samples"}
+        if t0 is not None and t1 is not None:
+            out["timed_region_s"] = round(t1 - t0, 3)
+        return out
 
 
 def _k1_traffic(workload, tile_n, pair):
@@ -333,7 +369,8 @@ def run_ours(args):
     passes = []
     barrier()
     sampler.start()
-    time.sleep(0.3)
+    time.sleep(0.3)  # nvidia-smi's first sample
+    sampler.mark_start()
     for i in range(args.steps):
         if not args.no_flush:
             flush.zero_()
@@ -341,6 +378,8 @@ def run_ours(args):
         step()
         ev[i][1].record(stream)
         passes.append(op.pass_times())
+    torch.cuda.synchronize(dev)
+    sampler.mark_end()
     barrier()
     clocks = sampler.stop()
     op.status(stream)

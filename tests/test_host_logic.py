@@ -35,3 +35,28 @@ def test_banded_tile_order_covers_every_tile_once(bands_bin, T, H, I, tile_n, k_
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("ok")
+
+
+def test_clock_samples_are_kept_only_inside_the_timed_region():
+    """bench.py reports clocks from the nvidia-smi samples taken while the timed steps
+    ran; idle samples before or after them must not enter the median."""
+    import datetime
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def row(t, mhz, cap="Not Active"):
+        stamp = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return [stamp, "0", str(mhz), "2070", "900.0", "0x0", "Not Active", "Not Active", "Not Active", cap]
+
+    t0 = 1_800_000_000.0
+    rows = [row(t0 - 0.2, 345), row(t0 + 0.01, 2070), row(t0 + 0.03, 2055, "Active"), row(t0 + 0.05, 2070),
+            row(t0 + 0.4, 345)]
+    out = bench.ClockSampler.summarise(rows, t0, t0 + 0.1)
+    assert out["samples"] == 3 and out["window"] == "timed region"
+    assert out["sm_mhz"] == 2070 and out["sm_max_mhz"] == 2070
+    assert out["reasons"] == ["sw_power_cap"]
+    # nothing inside the window: every sample, and the line says so
+    out = bench.ClockSampler.summarise(rows, t0 + 0.06, t0 + 0.07)
+    assert out["samples"] == 5 and out["window"].startswith("no sample")
