@@ -174,8 +174,15 @@ class ClockSampler:
                                  r[6:10]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
-        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-               "reasons": sorted(reasons), "samples": len(used),
+        pw = []
+        for r in used:
+            try:
+                pw.append(float(r[4]))
+            except ValueError:
+                pass
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_min_mhz": min(sm) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "power_w_median": statistics.median(pw) if pw else None,
+               "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(used),
                "window": "timed region" if inside else "no sample fell inside the timed region: all samples"}
         if t0 is not None and t1 is not None:
             out["timed_region_s"] = round(t1 - t0, 3)
