@@ -719,7 +719,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // leader's barrier. Per SM this halves the W bytes staged and read from shared
 // memory and the scale-factor copies per FLOP.
 // ---------------------------------------------------------------------------
-template <int BN>
+// Ring depth. Shared memory and the L1 cache are one array per SM, so every ring stage
+// is taken from the L1 that the loads of the norm/RoPE work running beside the GEMM
+// (gamma, cos/sin, the statistics) and the epilogue's bias and column scales go
+// through. Where that work runs beside the GEMM and a stage is large (tile_n >= 192),
+// the ring is kept to 4 stages (128 KB at tile_n 240, leaving ~124 KB of L1 instead
+// of ~28 KB with the 7 stages that fit). Measured at the Wan 480p shape: the GEMM
+// alone takes the same time with 4 to 7 stages (1.662-1.672 ms), while the step with
+// the norm/RoPE pass overlapped took 1.741-1.748 ms with 4 stages against 1.752-1.762
+// with 5 on one box, and 1.733-1.739 with 5 against 1.751-1.759 with 7 on another.
+// The per-head-epilogue form runs nothing beside it and keeps the deepest ring.
+template <int BN, bool kShallow>
 struct K1PairCfg {
   static constexpr int HALF_N = BN / 2;
   static constexpr int SF_CHUNKS = (BN + 127) / 128;
@@ -734,7 +744,8 @@ struct K1PairCfg {
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int FIXED = 1024 + 512 + 256;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int STAGES_CAP = (kShallow && BN >= 192) ? 4 : 8;
+  static constexpr int STAGES = STAGES_FIT > STAGES_CAP ? STAGES_CAP : STAGES_FIT;
   static constexpr size_t SMEM = FIXED + static_cast<size_t>(STAGES) * STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "pair MMA N");
@@ -842,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                               const __grid_constant__ CUtensorMap tmSF, const GemmShape g, const GemmArgs a,
                               const __grid_constant__ NormRopeArgs nr) {
-  using C = K1PairCfg<BN>;
+  using C = K1PairCfg<BN, kEpi != kEpiHead>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -1103,7 +1114,7 @@ template <int BN, int kEpi, bool kFused>
 cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                                const CUtensorMap& tmSF, const GemmArgs& a, const NormRopeArgs& nr, cudaStream_t s,
                                int num_sms) {
-  using C = K1PairCfg<BN>;
+  using C = K1PairCfg<BN, kEpi != kEpiHead>;
   auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, kFused>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
