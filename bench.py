@@ -51,6 +51,8 @@ def _args():
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--gemm", choices=["auto", "pair", "single"], default="auto",
                    help="GEMM form: 256-row tiles on SM pairs, 128-row tiles on one SM, or the library's choice")
+    p.add_argument("--a-multicast", action="store_true",
+                   help="run the CTA-pair GEMM in clusters of two pairs sharing each A tile")
     p.add_argument("--norm-in-gemm", action="store_true",
                    help="run the norm/RoPE work inside the GEMM's epilogue warps instead of its own kernel")
     p.add_argument("--layout", choices=["bsd", "nbsd"], default="bsd",
@@ -199,11 +201,11 @@ def _spread(step_ms):
             "first_quarter_mean": statistics.mean(step_ms[:q]), "last_quarter_mean": statistics.mean(step_ms[-q:])}
 
 
-def _k1_traffic(workload, tile_n, pair):
+def _k1_traffic(workload, tile_n, pair, quad=False):
     """DRAM bytes per GEMM launch from the committed ncu summary of that GEMM form
-    (profiles/qkv_gemm_mxf8[_pair]_<workload>.md), if it was taken on the current
+    (profiles/qkv_gemm_mxf8{,_pair,_quad}_<workload>.md), if it was taken on the current
     kernel source and this workload/tile; else None."""
-    name = "qkv_gemm_mxf8_pair" if pair else "qkv_gemm_mxf8"
+    name = "qkv_gemm_mxf8_quad" if quad else ("qkv_gemm_mxf8_pair" if pair else "qkv_gemm_mxf8")
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (name, workload))
     if not os.path.exists(path):
         return None
@@ -295,7 +297,7 @@ _INPUT_NOTE = {
 }
 
 
-def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8", op_norm_in_gemm=False):
+def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8", op_norm_in_gemm=False, gemm_form=None):
     return {
         "workload": (f"{call.name}: Wan2.2-style fused QKV self-attention projection, T={call.tokens} "
                      f"H={call.hidden} n_q={call.n_q_heads} n_kv={call.n_kv_heads} d_head={call.d_head} "
@@ -303,6 +305,7 @@ def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8", op_norm_
         "tokens": call.tokens, "hidden": call.hidden, "width": call.width,
         "n_q_heads": call.n_q_heads, "n_kv_heads": call.n_kv_heads, "d_head": call.d_head,
         "tile_n": tile_n,
+        "gemm_form": gemm_form,
         "output_layout": "NBSd [heads, T, d_head]" if layout == "nbsd" else "BSD [T, I]",
         "norm_rope_work": "inside the GEMM's epilogue warps" if op_norm_in_gemm else "its own kernel, overlapped with the GEMM",
         "qk_norm": {0: "none", 1: "across heads (RMS)", 2: "per head RMS, in the GEMM epilogue",
@@ -350,6 +353,10 @@ def run_ours(args):
         from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_NORM_IN_GEMM
 
         gemm_flag |= QKV_CTE_FLAG_NORM_IN_GEMM
+    if args.a_multicast:
+        from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_A_MULTICAST
+
+        gemm_flag |= QKV_CTE_FLAG_GEMM_A_MULTICAST
     layout = QKV_CTE_LAYOUT_NBSD if args.layout == "nbsd" else QKV_CTE_LAYOUT_BSD
     input_layout = {"fp8": QKV_CTE_INPUT_ROW_FP8, "packed": QKV_CTE_INPUT_PACKED, "bf16": QKV_CTE_INPUT_BF16}[args.input]
     # The step's activation input, resident on the device (and its host copy for e2e).
@@ -492,7 +499,10 @@ def run_ours(args):
                "sample": (f"{len(rows)} seeded rows of the {call.tokens}-token workload in one oracle call "
                           f"({dt:.2f} s; float64 numpy, BLAS threads via {how})")}
 
-    traffic = _k1_traffic(args.workload, tile_n, bool(op.info.cta_pair))
+    quad = bool(op.info.a_multicast)
+    gemm_form = ("CTA pairs (M = 256 MMAs), clusters of two pairs sharing each A tile by TMA multicast" if quad
+                 else "CTA pairs (M = 256 MMAs)" if op.info.cta_pair else "single CTAs (M = 128 MMAs)")
+    traffic = _k1_traffic(args.workload, tile_n, bool(op.info.cta_pair), quad)
     producer = None
     if args.input != "fp8":
         # bytes the producer step must move: read the input rows, write e4m3 codes + scales
@@ -509,7 +519,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; Wan2.2 480p shapes and distributions)",
         "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout, input_kind=args.input,
-                          op_norm_in_gemm=bool(op.info.norm_in_gemm)),
+                          op_norm_in_gemm=bool(op.info.norm_in_gemm), gemm_form=gemm_form),
         "pct_nominal_dense_fp8_peak": 100.0 * value / (world * NOMINAL_FP8_TFLOPS),
         "pct_measured_fp8_peak": 100.0 * value / (world * fp8_peak),
         "passes_ms": {"prep": prep_ms, "gemm_epilogue": gemm_ms, "norm_rope_span": norm_span_ms,
@@ -522,7 +532,8 @@ def run_ours(args):
         "norm_rope": {"GB/s": k2_gbs, "bytes": k2_bytes, "measured_on": "serial side run",
                       "frac_of_hbm": (k2_gbs / hbm_gbs) if k2_gbs else None, "peak_GB/s": hbm_gbs},
         "roofline": {"bound": "tensor",
-                     "kernel": ("qkv_gemm_mxf8_pair_kernel<%d>" if op.info.cta_pair else "qkv_gemm_mxf8_kernel<%d>")
+                     "kernel": ("qkv_gemm_mxf8_pair_kernel<%d> (A-sharing clusters)" if quad else
+                                "qkv_gemm_mxf8_pair_kernel<%d>" if op.info.cta_pair else "qkv_gemm_mxf8_kernel<%d>")
                      % tile_n, "achieved": k1_achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": k1_achieved / fp8_peak,
                      "traffic": traffic,

@@ -63,6 +63,9 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 struct DeviceInfo {
   bool init = false;
   int major = 0, minor = 0, sms = 0;
+  // clusters of two CTA pairs of the plain-epilogue GEMM the device holds at once, per
+  // tile width (128, 192, 240, 256); -1 until first asked
+  int quad_clusters[4] = {-1, -1, -1, -1};
 };
 
 constexpr int kMaxDevices = 64;
@@ -85,6 +88,20 @@ int device_info(DeviceInfo* out) {
   }
   *out = d;
   return QKV_CTE_OK;
+}
+
+// Clusters for the A-sharing GEMM form on the current device: the number the device
+// holds at once if that covers every SM (a persistent grid on fewer SMs would lose
+// more than sharing A saves), else 0 (use the pair form). Asked once per device and
+// tile width.
+int quad_clusters_for(int tile_n, int sms) {
+  const int slot = tile_n == 128 ? 0 : tile_n == 192 ? 1 : tile_n == 240 ? 2 : tile_n == 256 ? 3 : -1;
+  int dev = 0;
+  if (slot < 0 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  int& n = g_dev[dev].quad_clusters[slot];
+  if (n < 0) n = gemm_quad_clusters(tile_n, sms);
+  return n >= sms / 4 ? sms / 4 : 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -210,7 +227,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
     return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
   const uint32_t known_flags = QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES |
                                QKV_CTE_FLAG_GEMM_CTA_PAIR | QKV_CTE_FLAG_GEMM_SINGLE_CTA |
-                               QKV_CTE_FLAG_NORM_IN_GEMM | QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE;
+                               QKV_CTE_FLAG_NORM_IN_GEMM | QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE |
+                               QKV_CTE_FLAG_GEMM_A_MULTICAST;
   if ((d.flags & ~known_flags) != 0) return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
   if ((d.flags & QKV_CTE_FLAG_GEMM_CTA_PAIR) && (d.flags & QKV_CTE_FLAG_GEMM_SINGLE_CTA))
     return fail(QKV_CTE_ERR_INVALID, "QKV_CTE_FLAG_GEMM_CTA_PAIR and QKV_CTE_FLAG_GEMM_SINGLE_CTA exclude each other");
@@ -260,6 +278,17 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   p->k_end = p->q_end + d.n_kv_heads * d.d_head;
   g.n_qk_tiles = (p->k_end + tile_n - 1) / tile_n;
   if (g.n_qk_tiles > g.n_tiles) g.n_qk_tiles = g.n_tiles;
+  // The norm/RoPE pass (and its hand-off) runs for the across-heads norm, or RoPE
+  // without a norm; the per-head norms finish in the GEMM's epilogue.
+  const bool second_pass = !head_norm_in_epilogue(d) && (d.norm != QKV_CTE_NORM_NONE || d.rope);
+  p->second_pass = second_pass;
+  p->fused_norm = second_pass && g.cta_pair && !per_head_norm(d) && (d.flags & QKV_CTE_FLAG_NORM_IN_GEMM) &&
+                  !(d.flags & QKV_CTE_FLAG_SERIAL_PASSES);
+  // On request two CTA pairs share each A tile (TMA multicast in clusters of four) when
+  // the tiles pair up: an even number of N tiles, the plain epilogue, the pass not in
+  // the GEMM.
+  g.quad = (d.flags & QKV_CTE_FLAG_GEMM_A_MULTICAST) && g.cta_pair && g.n_tiles % 2 == 0 && !per_head_norm(d) &&
+           !p->fused_norm;
   make_bands(g, band_tiles(g));
   WorkspaceLayout& w = p->ws;
   w.status_off = 0;
@@ -268,12 +297,6 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   w.ready_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
   w.sm_busy_off = w.ready_off + align_up((size_t)g.blocks128 * sizeof(uint32_t), 256);
   w.qk_off = w.sm_busy_off + align_up((size_t)kSmTable * sizeof(uint32_t), 256);
-  // The norm/RoPE pass (and its hand-off) runs for the across-heads norm, or RoPE
-  // without a norm; the per-head norms finish in the GEMM's epilogue.
-  const bool second_pass = !head_norm_in_epilogue(d) && (d.norm != QKV_CTE_NORM_NONE || d.rope);
-  p->second_pass = second_pass;
-  p->fused_norm = second_pass && g.cta_pair && !per_head_norm(d) && (d.flags & QKV_CTE_FLAG_NORM_IN_GEMM) &&
-                  !(d.flags & QKV_CTE_FLAG_SERIAL_PASSES);
   const size_t hand_rows = second_pass ? (size_t)g.blocks128 * 128 : 0;
   w.qk_exp_off = w.qk_off + align_up(hand_rows * p->k_end * sizeof(uint16_t), 256);
   w.stats_off = w.qk_exp_off + align_up(hand_rows * (p->k_end / 16), 256);
@@ -300,6 +323,7 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info) {
   info->cta_pair = plan->g.cta_pair;
   info->norm_in_gemm = plan->fused_norm ? 1 : 0;
   info->workspace_bytes = (int64_t)plan->ws.total;
+  info->a_multicast = plan->g.quad;
   return ok();
 }
 
@@ -394,8 +418,12 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   // step writes into the workspace.
   const uint8_t* A_codes = produced ? ws + plan->ws.act_off : A;
   const float* A_scale = produced ? reinterpret_cast<const float*>(ws + plan->ws.act_scale_off) : a_scale;
+  // The A-sharing form loads A in 64-row halves (one per pair of the cluster).
+  const int quad_clusters = g.quad ? quad_clusters_for(g.tile_n, dev.sms) : 0;
   CUtensorMap tmA, tmW;
-  if ((rc = encode_operand(&tmA, A_codes, (uint64_t)g.T, (uint64_t)g.H, 128u, "A")) != QKV_CTE_OK) return rc;
+  if ((rc = encode_operand(&tmA, A_codes, (uint64_t)g.T, (uint64_t)g.H, quad_clusters > 0 ? 64u : 128u, "A")) !=
+      QKV_CTE_OK)
+    return rc;
   const uint32_t w_box_rows = g.cta_pair ? (uint32_t)g.tile_n / 2 : (uint32_t)g.tile_n;
   if ((rc = encode_operand(&tmW, W, (uint64_t)g.I, (uint64_t)g.H, w_box_rows, "W")) != QKV_CTE_OK) return rc;
 
@@ -504,7 +532,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   // On request the norm/RoPE tasks run inside the CTA-pair GEMM's epilogue warps;
   // otherwise as their own kernel, overlapped with the GEMM (or after it, serialised).
   const bool fused = plan->second_pass && plan->fused_norm;
-  e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms, fused ? &na : nullptr);
+  e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms, fused ? &na : nullptr, quad_clusters);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
 
   if (plan->second_pass && !fused) {

@@ -848,11 +848,20 @@ __device__ __forceinline__ void fused_finish(const NormRopeArgs& nr, long long n
   if (w.started && (threadIdx.x & 31) == 0) atomicMax(&nr.stamps[1], globaltimer_ns());
 }
 
-template <int BN, int kEpi, bool kFused>
+// kQuad: clusters of two pairs. Both pairs of a cluster compute the same 256-row panel
+// at the same time, on neighbouring N tiles (the tile order pairs them: tiles 2u and
+// 2u+1 share their rows), so they need the same A tile. Each CTA loads half of its
+// 128 rows of it (64 rows) and multicasts them to the CTA of the same pair rank in
+// both pairs: A is read from L2 once per cluster instead of once per pair. Every
+// landing is counted on the destination pair's full barrier (which still expects both
+// CTAs' whole stage), and a stage is free again once both pairs' MMAs have read it
+// (each CTA's empty barrier takes one commit from each pair).
+template <int BN, int kEpi, bool kFused, bool kQuad>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                               const __grid_constant__ CUtensorMap tmSF, const GemmShape g, const GemmArgs a,
                               const __grid_constant__ NormRopeArgs nr) {
+  static_assert(!(kQuad && kFused), "the in-GEMM norm form runs on pairs only");
   using C = K1PairCfg<BN, kEpi != kEpiHead>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -871,15 +880,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_ctarank();
+  const uint32_t crank = cluster_ctarank();       // rank in the cluster
+  const uint32_t rank = crank & 1u;               // rank in the pair
+  const uint32_t lead = crank & ~1u;              // cluster rank of this pair's leader
+  const uint32_t qpair = kQuad ? (crank >> 1) : 0u;  // which pair of the cluster
   const bool leader = rank == 0;
-  const int pair = blockIdx.x >> 1;
-  const int n_pairs = gridDim.x >> 1;
+  // Tiles of this pair: tile_first, tile_first + tile_step, ...
+  const int tile_first = kQuad ? 2 * static_cast<int>(blockIdx.x >> 2) + static_cast<int>(qpair)
+                               : static_cast<int>(blockIdx.x >> 1);
+  const int tile_step = kQuad ? 2 * static_cast<int>(gridDim.x >> 2) : static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kQuad ? 2 : 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&tfull[s]), 1);
@@ -927,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = (a.flags & kFlagTestStall) == 0;
-      for (int tile = pair; ok && tile < num_tiles; tile += n_pairs) {
+      for (int tile = tile_first; ok && tile < num_tiles; tile += tile_step) {
         int m_blk, n_blk;
         tile_coords(g, tile, m_blk, n_blk);
         for (int kb = 0; kb < g.k_stages; ++kb) {
@@ -938,9 +952,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb_local = smem_u32(&full[stage]);
           if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::STAGE_BYTES);
-          const uint32_t fb = mapa_shared(fb_local, 0);
-          tma_load_2d_pair(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * kBK,
-                           m_blk * 2 * kBM + static_cast<int>(rank) * kBM, fb, pol_stream);
+          const uint32_t fb = mapa_shared(fb_local, lead);
+          if constexpr (kQuad) {
+            // rows [64 * qpair, 64 * qpair + 64) of this CTA's 128: to this rank in both pairs
+            tma_load_2d_pair_multicast(smem_u32(sA + stage * C::A_BYTES + qpair * (C::A_BYTES / 2)), &tmA, kb * kBK,
+                                       m_blk * 2 * kBM + static_cast<int>(rank) * kBM + static_cast<int>(qpair) * (kBM / 2),
+                                       fb, static_cast<uint16_t>((1u << rank) | (1u << (2u + rank))), pol_stream);
+          } else {
+            tma_load_2d_pair(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * kBK,
+                             m_blk * 2 * kBM + static_cast<int>(rank) * kBM, fb, pol_stream);
+          }
           tma_load_2d_pair(smem_u32(sB + stage * C::B_BYTES), &tmW, kb * kBK,
                            n_blk * BN + static_cast<int>(rank) * C::HALF_N, fb, pol_keep);
           tma_load_2d_pair(smem_u32(sSFB + stage * C::SFB_BYTES), &tmSF, 0, n_blk * g.k_stages + kb, fb, pol_keep);
@@ -984,7 +1005,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = pair; ok && tile < num_tiles; tile += n_pairs) {
+      for (int tile = tile_first; ok && tile < num_tiles; tile += tile_step) {
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
           record_failure(a.status, abort_flag, kErrMmaTmemEmptyWait);
           break;
@@ -1008,14 +1029,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBK / 32; ++k)
             mma_mxf8_pair(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t,
                           (kb | k) != 0 ? 1u : 0u);
-          tc_commit_pair_multicast(smem_u32(&empty[stage]), 0x3);
+          // the stage is free once every CTA that wrote into it sees this pair done
+          tc_commit_pair_multicast(smem_u32(&empty[stage]), kQuad ? 0xF : static_cast<uint16_t>(0x3u << lead));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit_pair_multicast(smem_u32(&tfull[acc]), 0x3);
+        tc_commit_pair_multicast(smem_u32(&tfull[acc]), static_cast<uint16_t>(0x3u << lead));
         if (++acc == C::ACC_STAGES) {
           acc = 0;
           acc_phase ^= 1u;
@@ -1037,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     FusedWork fw;
     const long long n_tasks = kFused ? nrp::task_count(nr, kFusedHeadGroup) : 0;
     const uint64_t once = kFused ? nrp::evict_first_policy() : 0;
-    for (int tile = pair; tile < num_tiles; tile += n_pairs) {
+    for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
       int m_blk, n_blk;
       tile_coords(g, tile, m_blk, n_blk);
       bool ok;
@@ -1060,7 +1082,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            pol_out, ss_q, ss_k);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), 0));
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty[acc]), lead));
       if (live)
         epilogue_publish<BN>(g, a, block128, row_in_block, n_blk * BN, n_blk < g.n_qk_tiles, ss_q, ss_k, lane);
       if (++acc == C::ACC_STAGES) {
@@ -1110,18 +1132,28 @@ cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUte
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, g, a);
 }
 
-template <int BN, int kEpi, bool kFused>
+// The launch of the CTA-pair GEMM: clusters of one pair, or of two pairs sharing
+// their A tiles (kQuad; the tile count must be even and `clusters` at most what the
+// device holds at once, from gemm_quad_clusters).
+template <int BN, int kEpi, bool kFused, bool kQuad = false>
 cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                                const CUtensorMap& tmSF, const GemmArgs& a, const NormRopeArgs& nr, cudaStream_t s,
-                               int num_sms) {
+                               int num_sms, int quad_clusters = 0) {
   using C = K1PairCfg<BN, kEpi != kEpiHead>;
-  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, kFused>;
+  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, kFused, kQuad>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   const int tiles = g.m_tiles * g.n_tiles;
-  const int pairs = num_sms / 2;
-  const int grid = 2 * (tiles < pairs ? tiles : pairs);
+  int grid;
+  if constexpr (kQuad) {
+    if (tiles % 2 != 0 || quad_clusters < 1) return cudaErrorInvalidValue;
+    const int units = tiles / 2;
+    grid = 4 * (units < quad_clusters ? units : quad_clusters);
+  } else {
+    const int pairs = num_sms / 2;
+    grid = 2 * (tiles < pairs ? tiles : pairs);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -1129,7 +1161,7 @@ cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kQuad ? 4 : 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the prep kernel
@@ -1137,6 +1169,33 @@ cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, tmSF, g, a, nr);
+}
+
+// How many clusters of two pairs of this GEMM the device holds at once (0 on error).
+template <int BN, int kEpi>
+int quad_clusters_t(int num_sms) {
+  using C = K1PairCfg<BN, kEpi != kEpiHead>;
+  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, false, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM)) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(4 * (num_sms / 4)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 4;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace
