@@ -65,7 +65,7 @@ def _args():
     p.add_argument("--e2e-chunk", type=int, default=0, help="row chunk of the host-streaming e2e leg (0: the library's 2048)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
-    p.add_argument("--cpu-rows", type=int, default=12288, help="oracle row sample for cpu_baseline")
+    p.add_argument("--cpu-rows", type=int, default=20480, help="oracle row sample for cpu_baseline")
     p.add_argument("--ref-rows", type=int, default=256, help="oracle row sample per reference step")
     return p.parse_args()
 

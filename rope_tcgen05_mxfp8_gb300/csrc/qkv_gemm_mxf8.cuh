@@ -881,8 +881,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t crank = cluster_ctarank();       // rank in the cluster
-  const uint32_t rank = crank & 1u;               // rank in the pair
-  const uint32_t lead = crank & ~1u;              // cluster rank of this pair's leader
+  const uint32_t rank = kQuad ? (crank & 1u) : crank;  // rank in the pair
+  // cluster rank of this pair's leader (a constant for plain pairs: the pair kernel's
+  // code stays as it was without the cluster form, which measured 1.8 % faster)
+  const uint32_t lead = kQuad ? (crank & ~1u) : 0u;
   const uint32_t qpair = kQuad ? (crank >> 1) : 0u;  // which pair of the cluster
   const bool leader = rank == 0;
   // Tiles of this pair: tile_first, tile_first + tile_step, ...
