@@ -257,8 +257,8 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   g.I = (int)I;
   g.tile_n = tile_n;
   // The pair form is the default once there is more than one 128-row block: it stages
-  // half of each W tile per SM, issues the MMAs for two SMs from one thread and keeps a
-  // deeper operand ring (7 stages instead of 4); measured ~1% faster at 480p.
+  // half of each W tile per SM and issues the MMAs for two SMs from one thread;
+  // measured ~1% faster at 480p.
   if (d.flags & QKV_CTE_FLAG_GEMM_CTA_PAIR)
     g.cta_pair = 1;
   else if (d.flags & QKV_CTE_FLAG_GEMM_SINGLE_CTA)
