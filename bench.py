@@ -499,7 +499,7 @@ def run_ours(args):
                "sample": (f"{len(rows)} seeded rows of the {call.tokens}-token workload in one oracle call "
                           f"({dt:.2f} s; float64 numpy, BLAS threads via {how})")}
 
-    quad = bool(op.info.a_multicast)
+    quad = op.plan_info().a_multicast_ran == 1  # the form the timed runs used
     gemm_form = ("CTA pairs (M = 256 MMAs), clusters of two pairs sharing each A tile by TMA multicast" if quad
                  else "CTA pairs (M = 256 MMAs)" if op.info.cta_pair else "single CTAs (M = 128 MMAs)")
     traffic = _k1_traffic(args.workload, tile_n, bool(op.info.cta_pair), quad)

@@ -29,6 +29,7 @@ struct qkv_cte_plan_s {
   bool has_norm_pass = false;
   bool second_pass = false;  // the norm/RoPE work runs (across-heads norm, or RoPE alone)
   bool fused_norm = false;   // ... inside the CTA-pair GEMM's epilogue warps
+  int last_a_multicast = -1; // the GEMM form of the latest run: 1 A-sharing clusters, 0 not, -1 no run yet
   const void* last_workspace = nullptr;
   // qkv_cte_run_host: plans for one chunk and for the shorter last chunk, the copy
   // streams and the events that order staging buffers (created on first use)
@@ -91,9 +92,9 @@ int device_info(DeviceInfo* out) {
 }
 
 // Clusters for the A-sharing GEMM form on the current device: the number the device
-// holds at once if that covers every SM (a persistent grid on fewer SMs would lose
-// more than sharing A saves), else 0 (use the pair form). Asked once per device and
-// tile width.
+// holds at once (0: none fit, use the pair form). Clusters of four must sit in one
+// GPC, so this can cover fewer SMs than pairs do: on GB300, 36 clusters (144 of the
+// 152 SMs) against 76 pairs. Asked once per device and tile width.
 int quad_clusters_for(int tile_n, int sms) {
   const int slot = tile_n == 128 ? 0 : tile_n == 192 ? 1 : tile_n == 240 ? 2 : tile_n == 256 ? 3 : -1;
   int dev = 0;
@@ -101,7 +102,7 @@ int quad_clusters_for(int tile_n, int sms) {
   std::lock_guard<std::mutex> lk(g_dev_mu);
   int& n = g_dev[dev].quad_clusters[slot];
   if (n < 0) n = gemm_quad_clusters(tile_n, sms);
-  return n >= sms / 4 ? sms / 4 : 0;
+  return n < sms / 4 ? n : sms / 4;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -324,6 +325,7 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info) {
   info->norm_in_gemm = plan->fused_norm ? 1 : 0;
   info->workspace_bytes = (int64_t)plan->ws.total;
   info->a_multicast = plan->g.quad;
+  info->a_multicast_ran = plan->last_a_multicast;
   return ok();
 }
 
@@ -534,6 +536,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   const bool fused = plan->second_pass && plan->fused_norm;
   e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms, fused ? &na : nullptr, quad_clusters);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+  plan->last_a_multicast = quad_clusters > 0 && !fused ? 1 : 0;
 
   if (plan->second_pass && !fused) {
     e = launch_norm_rope(na, s, dev.sms, (d.flags & QKV_CTE_FLAG_SERIAL_PASSES) == 0);

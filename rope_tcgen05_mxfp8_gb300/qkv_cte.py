@@ -76,6 +76,7 @@ class qkv_cte_plan_info(ctypes.Structure):
         ("norm_in_gemm", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
         ("a_multicast", ctypes.c_int32),
+        ("a_multicast_ran", ctypes.c_int32),
     ]
 
 
@@ -342,6 +343,10 @@ class QkvCte:
         self.width = (n_q_heads + 2 * n_kv_heads) * d_head
         dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.workspace = torch.zeros(max(self.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+
+    def plan_info(self) -> qkv_cte_plan_info:
+        """The plan's choices now (a_multicast_ran reflects the latest run)."""
+        return qkv_cte_get_plan_info(self.plan)
 
     def __call__(self, A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, out=None,
                  w_col_scale=None, sumsq=None, inv_rms=None, stream=None):

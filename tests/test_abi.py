@@ -205,7 +205,9 @@ def test_plan_info_reports_when_two_pairs_share_a():
     for kw, expect in cases:
         plan, _ = q.qkv_cte_plan(q.make_desc(**kw))
         try:
-            assert q.qkv_cte_get_plan_info(plan).a_multicast == expect, kw
+            info = q.qkv_cte_get_plan_info(plan)
+            assert info.a_multicast == expect, kw
+            assert info.a_multicast_ran == -1, kw  # no run yet
         finally:
             q.qkv_cte_destroy(plan)
 

@@ -534,6 +534,8 @@ def test_a_sharing_clusters_match_oracle_and_plain_pairs(name, nbsd):
     op_s, out_s, ss_s, inv_s = run_path(call, g, nbsd=nbsd, flags=QKV_CTE_FLAG_GEMM_A_MULTICAST)
     op_p, out_p, ss_p, inv_p = run_path(call, g, nbsd=nbsd)
     assert op_s.info.a_multicast == 1 and op_p.info.a_multicast == 0
+    # the cluster form really ran (not the pair form the run falls back to without room for it)
+    assert op_s.plan_info().a_multicast_ran == 1 and op_p.plan_info().a_multicast_ran == 0
     op_s.status()
     op_p.status()
     check_outputs(call, inp, out_s, ss_s, inv_s, name=f"{call.name}_shared_a")
@@ -550,7 +552,7 @@ def test_a_sharing_wan480p_sampled_and_repeatable():
     inp = wl.make_inputs(call)
     g = to_device(inp, DEV)
     op1, out1, ss1, inv1 = run_path(call, g, flags=QKV_CTE_FLAG_GEMM_A_MULTICAST)
-    assert op1.info.a_multicast == 1
+    assert op1.info.a_multicast == 1 and op1.plan_info().a_multicast_ran == 1
     op1.status()
     check_outputs(call, inp, out1, ss1, inv1, rows=sampled_rows(call), name="wan480p_shared_a")
     op2, out2, _, _ = run_path(call, g, flags=QKV_CTE_FLAG_GEMM_A_MULTICAST)
