@@ -497,7 +497,12 @@ def run_ours(args):
         cpu = {"value": 2.0 * len(rows) * call.hidden * call.width / dt / 1e12, "unit": "TFLOP/s",
                "cores": cores, "kind": "oracle",
                "sample": (f"{len(rows)} seeded rows of the {call.tokens}-token workload in one oracle call "
-                          f"({dt:.2f} s; float64 numpy, BLAS threads via {how})")}
+                          f"({dt:.2f} s; float64 numpy, BLAS threads via {how})"),
+               "rows_per_s": len(rows) / dt,
+               # rows are independent: a whole step is the sample's time scaled by the row count
+               # (an extrapolation unless the sample is every row)
+               "full_step_s": dt * call.tokens / len(rows),
+               "full_step_s_is": "measured" if len(rows) == call.tokens else "extrapolated linearly in rows"}
 
     quad = op.plan_info().a_multicast_ran == 1  # the form the timed runs used
     gemm_form = ("CTA pairs (M = 256 MMAs), clusters of two pairs sharing each A tile by TMA multicast" if quad
