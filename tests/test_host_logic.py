@@ -77,3 +77,44 @@ def test_clock_samples_are_kept_only_inside_the_timed_region():
     # nothing inside the window: every sample, and the line says so
     out = bench.ClockSampler.summarise(rows, t0 + 0.06, t0 + 0.07)
     assert out["samples"] == 5 and out["window"].startswith("no sample")
+
+
+def test_bench_traffic_only_from_a_profile_of_the_current_kernel(tmp_path, monkeypatch):
+    """bench.py reports the GEMM's DRAM traffic from the committed ncu summary only while
+    that summary's source hash matches the kernel sources; otherwise traffic is null."""
+    import shutil
+    import sys
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    name = "qkv_gemm_mxf8_pair_wan480p.md"
+    src = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(src):
+        pytest.skip("no committed GEMM profile")
+    fake_root = tmp_path / "repo"
+    (fake_root / "profiles").mkdir(parents=True)
+    shutil.copy(src, fake_root / "profiles" / name)
+    rec = {}
+    for line in open(src):
+        if ":" in line and not line.startswith(("|", " ", "#", "-")):
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    for rel in rec["sources"].split():
+        (fake_root / rel).parent.mkdir(parents=True, exist_ok=True)
+        shutil.copy(os.path.join(ROOT, rel), fake_root / rel)
+    monkeypatch.setattr(bench, "ROOT", str(fake_root))
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in rec["sources"].split():
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    current = h.hexdigest() == rec["source_sha256"]  # False while a kernel change awaits a new capture
+    expect = int(rec["dram_bytes_per_launch"]) if current else None
+    assert bench._k1_traffic("wan480p", 240, True) == expect
+    assert bench._k1_traffic("wan480p", 192, True) is None       # another tile width
+    assert bench._k1_traffic("short", 240, True) is None         # another workload
+    first = rec["sources"].split()[0]
+    with open(fake_root / first, "a") as f:                      # the kernel changed since the capture
+        f.write("\n// changed\n")
+    assert bench._k1_traffic("wan480p", 240, True) is None
