@@ -33,7 +33,7 @@ namespace qkvcte {
 namespace nrp {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kHeadBatch = 4;  // heads whose hand-off loads are in flight together
+constexpr int kHeadBatch = 4;  // default: heads whose hand-off loads are in flight together
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
@@ -226,8 +226,9 @@ __device__ __forceinline__ void head_factors(const NormRopeArgs& p, int t, int h
 
 // One task, called by a whole warp once its panel is known to be complete. kHeadStats:
 // the per-head norm from the GEMM's statistics (a separate instantiation, so the
-// across-heads form keeps its lower register count).
-template <bool kHeadStats>
+// across-heads form keeps its lower register count). kBatch: heads whose loads are in
+// flight together (more per warp, or fewer registers and so more warps per SM).
+template <bool kHeadStats, int kBatch = kHeadBatch>
 __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, int group_heads, uint64_t once) {
   const int lane = threadIdx.x & 31;
   const int d = p.d_head;
@@ -272,11 +273,11 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
     load8_nc(sr + half + 8, sh + 8);
   }
   const size_t idx0 = static_cast<size_t>(panel) * qk_chunks * 128 + (t & 127);
-  for (int hg0 = h_begin; hg0 < h_end; hg0 += kHeadBatch) {
-    RawChunk raw_lo[kHeadBatch], raw_hi[kHeadBatch];
-    float4 share[kHeadBatch];  // per-head norms: this lane's share of the statistics
+  for (int hg0 = h_begin; hg0 < h_end; hg0 += kBatch) {
+    RawChunk raw_lo[kBatch], raw_hi[kBatch];
+    float4 share[kBatch];  // per-head norms: this lane's share of the statistics
 #pragma unroll
-    for (int k = 0; k < kHeadBatch; ++k) {
+    for (int k = 0; k < kBatch; ++k) {
       const int hg = hg0 + k;
       if (hg >= h_end) break;
       const int seg = hg >= p.n_q ? 1 : 0;
@@ -288,7 +289,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
       if constexpr (kHeadStats) share[k] = head_stats_share(p, tr, hg, c);
     }
 #pragma unroll
-    for (int k = 0; k < kHeadBatch; ++k) {
+    for (int k = 0; k < kBatch; ++k) {
       const int hg = hg0 + k;
       if (hg >= h_end) break;
       const int seg = hg >= p.n_q ? 1 : 0;
