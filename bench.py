@@ -51,8 +51,6 @@ def _args():
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--gemm", choices=["auto", "pair", "single"], default="auto",
                    help="GEMM form: 256-row tiles on SM pairs, 128-row tiles on one SM, or the library's choice")
-    p.add_argument("--a-multicast", action="store_true",
-                   help="run the CTA-pair GEMM in clusters of two pairs sharing each A tile")
     p.add_argument("--norm-in-gemm", action="store_true",
                    help="run the norm/RoPE work inside the GEMM's epilogue warps instead of its own kernel")
     p.add_argument("--layout", choices=["bsd", "nbsd"], default="bsd",
@@ -201,11 +199,11 @@ def _spread(step_ms):
             "first_quarter_mean": statistics.mean(step_ms[:q]), "last_quarter_mean": statistics.mean(step_ms[-q:])}
 
 
-def _k1_traffic(workload, tile_n, pair, quad=False):
+def _k1_traffic(workload, tile_n, pair):
     """DRAM bytes per GEMM launch from the committed ncu summary of that GEMM form
-    (profiles/qkv_gemm_mxf8{,_pair,_quad}_<workload>.md), if it was taken on the current
+    (profiles/qkv_gemm_mxf8{,_pair}_<workload>.md), if it was taken on the current
     kernel source and this workload/tile; else None."""
-    name = "qkv_gemm_mxf8_quad" if quad else ("qkv_gemm_mxf8_pair" if pair else "qkv_gemm_mxf8")
+    name = "qkv_gemm_mxf8_pair" if pair else "qkv_gemm_mxf8"
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (name, workload))
     if not os.path.exists(path):
         return None
@@ -353,10 +351,6 @@ def run_ours(args):
         from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_NORM_IN_GEMM
 
         gemm_flag |= QKV_CTE_FLAG_NORM_IN_GEMM
-    if args.a_multicast:
-        from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_A_MULTICAST
-
-        gemm_flag |= QKV_CTE_FLAG_GEMM_A_MULTICAST
     layout = QKV_CTE_LAYOUT_NBSD if args.layout == "nbsd" else QKV_CTE_LAYOUT_BSD
     input_layout = {"fp8": QKV_CTE_INPUT_ROW_FP8, "packed": QKV_CTE_INPUT_PACKED, "bf16": QKV_CTE_INPUT_BF16}[args.input]
     # The step's activation input, resident on the device (and its host copy for e2e).
@@ -504,10 +498,8 @@ def run_ours(args):
                "full_step_s": dt * call.tokens / len(rows),
                "full_step_s_is": "measured" if len(rows) == call.tokens else "extrapolated linearly in rows"}
 
-    quad = op.plan_info().a_multicast_ran == 1  # the form the timed runs used
-    gemm_form = ("CTA pairs (M = 256 MMAs), clusters of two pairs sharing each A tile by TMA multicast" if quad
-                 else "CTA pairs (M = 256 MMAs)" if op.info.cta_pair else "single CTAs (M = 128 MMAs)")
-    traffic = _k1_traffic(args.workload, tile_n, bool(op.info.cta_pair), quad)
+    gemm_form = "CTA pairs (M = 256 MMAs)" if op.info.cta_pair else "single CTAs (M = 128 MMAs)"
+    traffic = _k1_traffic(args.workload, tile_n, bool(op.info.cta_pair))
     producer = None
     if args.input != "fp8":
         # bytes the producer step must move: read the input rows, write e4m3 codes + scales
@@ -537,8 +529,7 @@ def run_ours(args):
         "norm_rope": {"GB/s": k2_gbs, "bytes": k2_bytes, "measured_on": "serial side run",
                       "frac_of_hbm": (k2_gbs / hbm_gbs) if k2_gbs else None, "peak_GB/s": hbm_gbs},
         "roofline": {"bound": "tensor",
-                     "kernel": ("qkv_gemm_mxf8_pair_kernel<%d> (A-sharing clusters)" if quad else
-                                "qkv_gemm_mxf8_pair_kernel<%d>" if op.info.cta_pair else "qkv_gemm_mxf8_kernel<%d>")
+                     "kernel": ("qkv_gemm_mxf8_pair_kernel<%d>" if op.info.cta_pair else "qkv_gemm_mxf8_kernel<%d>")
                      % tile_n, "achieved": k1_achieved,
                      "peak": fp8_peak, "unit": "TFLOP/s", "frac": k1_achieved / fp8_peak,
                      "traffic": traffic,

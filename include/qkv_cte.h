@@ -56,7 +56,7 @@
 extern "C" {
 #endif
 
-#define QKV_CTE_ABI_VERSION 3
+#define QKV_CTE_ABI_VERSION 4
 
 #define QKV_CTE_OK 0
 #define QKV_CTE_ERR_INVALID (-1)        /* null / inconsistent argument, mode-segment mismatch */
@@ -122,15 +122,6 @@ enum { QKV_CTE_INPUT_ROW_FP8 = 0, QKV_CTE_INPUT_PACKED = 1, QKV_CTE_INPUT_BF16 =
  * LayerNorm: each tile part's shift, mean and centred sum of squares) and the norm/RoPE pass
  * finishes from them, which keeps the GEMM's wide tiles. Same results to rounding. */
 #define QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE 0x40u
-/* Run the CTA-pair GEMM (plain epilogue: no per-head norm, no in-GEMM norm; an even number
- * of N tiles) in clusters of two pairs that compute neighbouring N tiles of the same
- * 256-row panel and share its A tile: each CTA loads half of its A rows and multicasts
- * them to both pairs, so A is read from L2 once per two tiles. Runs on as many clusters
- * of four as the device holds at once (on GB300 36, i.e. 144 of the 152 SMs, as a cluster
- * must sit in one GPC); ignored where the conditions do not hold (plan info a_multicast).
- * Same results as the pair form (the same MMAs in the same order). Off by default. */
-#define QKV_CTE_FLAG_GEMM_A_MULTICAST 0x80u
-
 /* Problem description ([qkv_cte] "Interface" argument table, flattened to scalars). */
 typedef struct {
     int64_t tokens;        /* T = B*S rows; 0 is allowed (nothing is launched); <= INT32_MAX */
@@ -161,11 +152,6 @@ typedef struct {
     int32_t norm_in_gemm;    /* 1: the norm/RoPE work runs inside the GEMM's epilogue warps (one
                                 kernel); 0: as a kernel of its own, or there is none */
     int64_t workspace_bytes; /* as returned by qkv_cte_plan */
-    int32_t a_multicast;     /* 1: the plan tiles for the A-sharing cluster form
-                                (QKV_CTE_FLAG_GEMM_A_MULTICAST); it runs when the device
-                                holds enough clusters of four */
-    int32_t a_multicast_ran; /* the GEMM form of the plan's most recent qkv_cte_run: 1 the
-                                A-sharing clusters ran, 0 they did not, -1 no run yet */
 } qkv_cte_plan_info;
 
 /* Validate `desc` (host only, no CUDA call) and create a plan.

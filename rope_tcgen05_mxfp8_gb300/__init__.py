@@ -8,7 +8,7 @@ activations per row or unpacks packed [T, H + 4] rows). This package is the thin
 """
 from .qkv_cte import (  # noqa: F401
     EXPORTED, QKV_CTE_ERR_ARCH, QKV_CTE_ERR_CUDA, QKV_CTE_ERR_DEVICE_TIMEOUT, QKV_CTE_ERR_INVALID,
-    QKV_CTE_ERR_UNSUPPORTED, QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA, QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_NORM_IN_GEMM, QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE, QKV_CTE_FLAG_GEMM_A_MULTICAST, QKV_CTE_FLAG_SERIAL_PASSES, QKV_CTE_FLAG_TEST_STALL, QKV_CTE_LAYOUT_BSD, QKV_CTE_LAYOUT_NBSD,
+    QKV_CTE_ERR_UNSUPPORTED, QKV_CTE_FLAG_GEMM_CTA_PAIR, QKV_CTE_FLAG_GEMM_SINGLE_CTA, QKV_CTE_FLAG_PROFILE, QKV_CTE_FLAG_NORM_IN_GEMM, QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE, QKV_CTE_FLAG_SERIAL_PASSES, QKV_CTE_FLAG_TEST_STALL, QKV_CTE_LAYOUT_BSD, QKV_CTE_LAYOUT_NBSD,
     QKV_CTE_INPUT_BF16, QKV_CTE_INPUT_PACKED, QKV_CTE_INPUT_ROW_FP8,
     QKV_CTE_NORM_ACROSS_HEADS, QKV_CTE_NORM_HEAD_LAYER, QKV_CTE_NORM_HEAD_RMS, QKV_CTE_NORM_NONE,
     QKV_CTE_MODE_FUSED, QKV_CTE_MODE_SEPARATE, QKV_CTE_NOALLOC_SCRATCH_BYTES, QKV_CTE_OK, QkvCte, QkvCteError, library_path, load,

@@ -67,11 +67,6 @@ constexpr int kMaxBands = 16;
 // slab of W, which stays resident in L2 while A streams through. The bands of tiles
 // holding Q or K columns come first and the V-only bands last: the norm/RoPE pass
 // waits only for a panel's Q/K tiles, so it overlaps the V bands.
-//
-// With `quad` every band holds an even number of N tiles (the Q/K run is rounded up
-// to even, taking in the first V-only tile when needed), so linear tiles 2u and 2u+1
-// always share their row panel: two CTA pairs computing them together can share the
-// A tile (the multicast form of the CTA-pair kernel).
 struct GemmShape {
   int T, H, I;
   int tile_n;       // N tile (columns of O per tile)
@@ -80,7 +75,6 @@ struct GemmShape {
   int m_tiles, n_tiles, k_stages;
   int sf_chunks;    // 128-column scale-factor chunks per N tile
   int n_qk_tiles;   // N tiles holding at least one Q or K column: [0, n_qk_tiles)
-  int quad;         // 1: bands of an even number of N tiles (n_tiles even), for the A-sharing form
   int n_bands;
   int band_n0[kMaxBands];          // first N tile of each band
   int band_nc[kMaxBands];          // N tiles in each band
@@ -100,17 +94,12 @@ __host__ __device__ inline void tile_coords(const GemmShape& g, int tile, int& m
 // Cut [0, n_tiles) into bands of at most `band_tiles` N tiles, Q/K tiles first.
 inline void make_bands(GemmShape& g, int band_tiles) {
   if (band_tiles < 1) band_tiles = 1;
-  int qk_run = g.n_qk_tiles;
-  if (g.quad) {  // even runs and bands (n_tiles is even)
-    qk_run += qk_run & 1;
-    if (qk_run > g.n_tiles) qk_run = g.n_tiles;
-    band_tiles += band_tiles & 1;
-  }
+  const int qk_run = g.n_qk_tiles;
   const int runs[2][2] = {{0, qk_run}, {qk_run, g.n_tiles - qk_run}};
   int need = 0;
   for (const auto& r : runs) need += (r[1] + band_tiles - 1) / band_tiles;
   while (need > kMaxBands) {
-    band_tiles += g.quad ? 2 : 1;
+    ++band_tiles;
     need = 0;
     for (const auto& r : runs) need += (r[1] + band_tiles - 1) / band_tiles;
   }
@@ -220,14 +209,9 @@ cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_pac
 // with one-row boxes (used by the CTA-pair kernel). With `fused` (CTA-pair form only)
 // the epilogue warps also run the norm/RoPE tasks of `*fused` between tiles, and no
 // separate pass is launched.
-// quad_clusters > 0 (g.quad, the plain epilogue, no `fused`): the A-sharing form, with
-// tmA encoded in 64-row boxes, on at most quad_clusters clusters of two pairs.
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                         const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms,
-                        const NormRopeArgs* fused, int quad_clusters);
-// How many clusters of two CTA pairs of the plain-epilogue GEMM with this tile width
-// the current device holds at once (0 if none or on error).
-int gemm_quad_clusters(int tile_n, int num_sms);
+                        const NormRopeArgs* fused);
 // K1 with the per-head qk-norm epilogue, or with the per-head statistics epilogue
 // (qkv_gemm_mxf8_head.cu); launch_gemm calls it when a.head_norm or a.stats_kind is set.
 cudaError_t launch_gemm_head(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,

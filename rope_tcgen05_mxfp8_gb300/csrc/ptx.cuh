@@ -292,19 +292,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
-// The same, multicast: the tile lands at this shared-memory offset in every cluster CTA
-// of `cta_mask`, and each landing is counted on the mbarrier at `bar_cluster`'s offset
-// in the leader CTA of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_multicast(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                                           uint32_t bar_cluster, uint16_t cta_mask,
-                                                           uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar_cluster), "h"(cta_mask), "l"(policy)
-      : "memory");
-}
-
 // Both CTAs of the pair execute these together (one warp each).
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)

@@ -29,7 +29,6 @@ struct qkv_cte_plan_s {
   bool has_norm_pass = false;
   bool second_pass = false;  // the norm/RoPE work runs (across-heads norm, or RoPE alone)
   bool fused_norm = false;   // ... inside the CTA-pair GEMM's epilogue warps
-  int last_a_multicast = -1; // the GEMM form of the latest run: 1 A-sharing clusters, 0 not, -1 no run yet
   const void* last_workspace = nullptr;
   // qkv_cte_run_host: plans for one chunk and for the shorter last chunk, the copy
   // streams and the events that order staging buffers (created on first use)
@@ -64,9 +63,6 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 struct DeviceInfo {
   bool init = false;
   int major = 0, minor = 0, sms = 0;
-  // clusters of two CTA pairs of the plain-epilogue GEMM the device holds at once, per
-  // tile width (128, 192, 240, 256); -1 until first asked
-  int quad_clusters[4] = {-1, -1, -1, -1};
 };
 
 constexpr int kMaxDevices = 64;
@@ -89,20 +85,6 @@ int device_info(DeviceInfo* out) {
   }
   *out = d;
   return QKV_CTE_OK;
-}
-
-// Clusters for the A-sharing GEMM form on the current device: the number the device
-// holds at once (0: none fit, use the pair form). Clusters of four must sit in one
-// GPC, so this can cover fewer SMs than pairs do: on GB300, 36 clusters (144 of the
-// 152 SMs) against 76 pairs. Asked once per device and tile width.
-int quad_clusters_for(int tile_n, int sms) {
-  const int slot = tile_n == 128 ? 0 : tile_n == 192 ? 1 : tile_n == 240 ? 2 : tile_n == 256 ? 3 : -1;
-  int dev = 0;
-  if (slot < 0 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
-  std::lock_guard<std::mutex> lk(g_dev_mu);
-  int& n = g_dev[dev].quad_clusters[slot];
-  if (n < 0) n = gemm_quad_clusters(tile_n, sms);
-  return n < sms / 4 ? n : sms / 4;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -228,8 +210,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
     return fail(QKV_CTE_ERR_INVALID, "unknown output layout");
   const uint32_t known_flags = QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES |
                                QKV_CTE_FLAG_GEMM_CTA_PAIR | QKV_CTE_FLAG_GEMM_SINGLE_CTA |
-                               QKV_CTE_FLAG_NORM_IN_GEMM | QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE |
-                               QKV_CTE_FLAG_GEMM_A_MULTICAST;
+                               QKV_CTE_FLAG_NORM_IN_GEMM | QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE;
   if ((d.flags & ~known_flags) != 0) return fail(QKV_CTE_ERR_INVALID, "unknown flags 0x%x", d.flags);
   if ((d.flags & QKV_CTE_FLAG_GEMM_CTA_PAIR) && (d.flags & QKV_CTE_FLAG_GEMM_SINGLE_CTA))
     return fail(QKV_CTE_ERR_INVALID, "QKV_CTE_FLAG_GEMM_CTA_PAIR and QKV_CTE_FLAG_GEMM_SINGLE_CTA exclude each other");
@@ -285,11 +266,6 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   p->second_pass = second_pass;
   p->fused_norm = second_pass && g.cta_pair && !per_head_norm(d) && (d.flags & QKV_CTE_FLAG_NORM_IN_GEMM) &&
                   !(d.flags & QKV_CTE_FLAG_SERIAL_PASSES);
-  // On request two CTA pairs share each A tile (TMA multicast in clusters of four) when
-  // the tiles pair up: an even number of N tiles, the plain epilogue, the pass not in
-  // the GEMM.
-  g.quad = (d.flags & QKV_CTE_FLAG_GEMM_A_MULTICAST) && g.cta_pair && g.n_tiles % 2 == 0 && !per_head_norm(d) &&
-           !p->fused_norm;
   make_bands(g, band_tiles(g));
   WorkspaceLayout& w = p->ws;
   w.status_off = 0;
@@ -324,8 +300,6 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info) {
   info->cta_pair = plan->g.cta_pair;
   info->norm_in_gemm = plan->fused_norm ? 1 : 0;
   info->workspace_bytes = (int64_t)plan->ws.total;
-  info->a_multicast = plan->g.quad;
-  info->a_multicast_ran = plan->last_a_multicast;
   return ok();
 }
 
@@ -420,12 +394,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   // step writes into the workspace.
   const uint8_t* A_codes = produced ? ws + plan->ws.act_off : A;
   const float* A_scale = produced ? reinterpret_cast<const float*>(ws + plan->ws.act_scale_off) : a_scale;
-  // The A-sharing form loads A in 64-row halves (one per pair of the cluster).
-  const int quad_clusters = g.quad ? quad_clusters_for(g.tile_n, dev.sms) : 0;
   CUtensorMap tmA, tmW;
-  if ((rc = encode_operand(&tmA, A_codes, (uint64_t)g.T, (uint64_t)g.H, quad_clusters > 0 ? 64u : 128u, "A")) !=
-      QKV_CTE_OK)
-    return rc;
+  if ((rc = encode_operand(&tmA, A_codes, (uint64_t)g.T, (uint64_t)g.H, 128u, "A")) != QKV_CTE_OK) return rc;
   const uint32_t w_box_rows = g.cta_pair ? (uint32_t)g.tile_n / 2 : (uint32_t)g.tile_n;
   if ((rc = encode_operand(&tmW, W, (uint64_t)g.I, (uint64_t)g.H, w_box_rows, "W")) != QKV_CTE_OK) return rc;
 
@@ -534,9 +504,8 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   // On request the norm/RoPE tasks run inside the CTA-pair GEMM's epilogue warps;
   // otherwise as their own kernel, overlapped with the GEMM (or after it, serialised).
   const bool fused = plan->second_pass && plan->fused_norm;
-  e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms, fused ? &na : nullptr, quad_clusters);
+  e = launch_gemm(g, tmA, tmW, tmSF, ga, s, dev.sms, fused ? &na : nullptr);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
-  plan->last_a_multicast = quad_clusters > 0 && !fused ? 1 : 0;
 
   if (plan->second_pass && !fused) {
     e = launch_norm_rope(na, s, dev.sms, (d.flags & QKV_CTE_FLAG_SERIAL_PASSES) == 0);

@@ -133,34 +133,15 @@ cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_pac
                             sm_busy, status, stamps, task_next, zero_extra, zero_extra_count);
 }
 
-int gemm_quad_clusters(int tile_n, int num_sms) {
-  switch (tile_n) {
-    case 128: return quad_clusters_t<128, kEpiPlain>(num_sms);
-    case 192: return quad_clusters_t<192, kEpiPlain>(num_sms);
-    case 240: return quad_clusters_t<240, kEpiPlain>(num_sms);
-    case 256: return quad_clusters_t<256, kEpiPlain>(num_sms);
-    default: return 0;
-  }
-}
-
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                         const CUtensorMap& tmSF, const GemmArgs& a, cudaStream_t s, int num_sms,
-                        const NormRopeArgs* fused, int quad_clusters) {
+                        const NormRopeArgs* fused) {
   if (a.head_norm != 0 || a.stats_kind != 0) return launch_gemm_head(g, tmA, tmW, tmSF, a, s, num_sms);
   if (fused != nullptr) {
     if (!g.cta_pair) return cudaErrorInvalidValue;
     return launch_gemm_fused(g, tmA, tmW, tmSF, a, *fused, s, num_sms);
   }
   const NormRopeArgs none{};
-  if (g.cta_pair && g.quad && quad_clusters > 0) {
-    switch (g.tile_n) {
-      case 128: return launch_gemm_pair_t<128, kEpiPlain, false, true>(g, tmA, tmW, tmSF, a, none, s, num_sms, quad_clusters);
-      case 192: return launch_gemm_pair_t<192, kEpiPlain, false, true>(g, tmA, tmW, tmSF, a, none, s, num_sms, quad_clusters);
-      case 240: return launch_gemm_pair_t<240, kEpiPlain, false, true>(g, tmA, tmW, tmSF, a, none, s, num_sms, quad_clusters);
-      case 256: return launch_gemm_pair_t<256, kEpiPlain, false, true>(g, tmA, tmW, tmSF, a, none, s, num_sms, quad_clusters);
-      default: return cudaErrorInvalidValue;
-    }
-  }
   if (g.cta_pair) {
     switch (g.tile_n) {
       case 128: return launch_gemm_pair_t<128, kEpiPlain, false>(g, tmA, tmW, tmSF, a, none, s, num_sms);

@@ -719,24 +719,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 // leader's barrier. Per SM this halves the W bytes staged and read from shared
 // memory and the scale-factor copies per FLOP.
 // ---------------------------------------------------------------------------
-// Ring depth. Shared memory and the L1 cache are one array per SM, so every ring stage
-// is taken from the L1 that the loads of the norm/RoPE work running beside the GEMM
-// (gamma, cos/sin, the statistics) and the epilogue's bias and column scales go
-// through. Where that work runs beside the GEMM and a stage is large (tile_n >= 192),
-// the ring is kept to 4 stages (128 KB at tile_n 240, leaving ~124 KB of L1 instead
-// of ~28 KB with the 7 stages that fit). Measured at the Wan 480p shape: the GEMM
-// alone takes the same time with 4 to 7 stages (1.662-1.672 ms), while the step with
-// the norm/RoPE pass overlapped took 1.741-1.748 ms with 4 stages against 1.752-1.762
-// with 5 on one box, and 1.733-1.739 with 5 against 1.751-1.759 with 7 on another.
-// The per-head-epilogue form runs nothing beside it and keeps the deepest ring.
-template <int BN, bool kShallow>
+// Stage depth. A ring stage holds two 128-byte K blocks (K = 256 per stage: eight MMAs
+// and one scale-factor copy group per barrier wait). The tensor pipe runs the MMAs of
+// a continuously fed issue stream at the full rate, but every stage boundary (the
+// wait for the stage's operands and the copy of its block scales into TMEM, which is
+// ordered against the MMAs in flight) opens a bubble. Measured on GB300 with the
+// 480p tile stream and real TMA traffic, M = 256, N = 240: 1.50 ms per launch with
+// 128-byte stages against 1.20 ms with 256-byte stages (1.06 ms with no stage
+// boundaries at all), so the boundaries are made half as frequent. A K length that
+// is an odd number of 128-byte blocks ends on a half stage.
+//
+// Ring depth: as many stages as fit (three at tile_n 192 to 256: 192 KB). Measured at
+// the Wan 480p shape with the norm/RoPE pass overlapped: 1.616 ms per step with three
+// 256-byte stages against 2.094 ms with two (which left more L1 for the pass beside
+// the GEMM, but cannot cover the load latency).
+template <int BN>
 struct K1PairCfg {
   static constexpr int HALF_N = BN / 2;
   static constexpr int SF_CHUNKS = (BN + 127) / 128;
-  static constexpr int A_BYTES = kBM * kBK;
-  static constexpr int B_BYTES = HALF_N * kBK;
-  static constexpr int SFB_BYTES = SF_CHUNKS * 512;
-  static constexpr int SFB_COLS = SF_CHUNKS * 4;
+  static constexpr int KW = 2;                           // 128-byte K blocks per stage
+  static constexpr int A_HALF = kBM * kBK;               // one 128-byte K block of A
+  static constexpr int B_HALF = HALF_N * kBK;            // ... of this CTA's half of W
+  static constexpr int SF_HALF = SF_CHUNKS * 512;        // ... of the tile's scales
+  static constexpr int A_BYTES = KW * A_HALF;
+  static constexpr int B_BYTES = KW * B_HALF;
+  static constexpr int SFB_BYTES = KW * SF_HALF;
+  static constexpr int SFB_COLS = KW * SF_CHUNKS * 4;
   static constexpr int ACC_STAGES = (2 * BN + 4 + SFB_COLS <= 512) ? 2 : 1;
   static constexpr int SFA_COL = ACC_STAGES * BN;
   static constexpr int SFB_COL = SFA_COL + 4;
@@ -744,12 +752,12 @@ struct K1PairCfg {
   static constexpr int SMEM_LIMIT = 232448;
   static constexpr int FIXED = 1024 + 512 + 256;
   static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED) / STAGE_BYTES;
-  static constexpr int STAGES_CAP = (kShallow && BN >= 192) ? 4 : 8;
-  static constexpr int STAGES = STAGES_FIT > STAGES_CAP ? STAGES_CAP : STAGES_FIT;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
   static constexpr size_t SMEM = FIXED + static_cast<size_t>(STAGES) * STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;
   static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "pair MMA N");
   static_assert(HALF_N % 8 == 0, "W half tile in whole 8-row swizzle atoms");
+  static_assert(B_HALF % 1024 == 0 && A_HALF % 1024 == 0, "K blocks on swizzle-atom boundaries");
   static_assert(SFB_COL + SFB_COLS <= 512, "TMEM columns");
   static_assert(STAGES >= 2, "pipeline depth");
 };
@@ -848,21 +856,12 @@ __device__ __forceinline__ void fused_finish(const NormRopeArgs& nr, long long n
   if (w.started && (threadIdx.x & 31) == 0) atomicMax(&nr.stamps[1], globaltimer_ns());
 }
 
-// kQuad: clusters of two pairs. Both pairs of a cluster compute the same 256-row panel
-// at the same time, on neighbouring N tiles (the tile order pairs them: tiles 2u and
-// 2u+1 share their rows), so they need the same A tile. Each CTA loads half of its
-// 128 rows of it (64 rows) and multicasts them to the CTA of the same pair rank in
-// both pairs: A is read from L2 once per cluster instead of once per pair. Every
-// landing is counted on the destination pair's full barrier (which still expects both
-// CTAs' whole stage), and a stage is free again once both pairs' MMAs have read it
-// (each CTA's empty barrier takes one commit from each pair).
-template <int BN, int kEpi, bool kFused, bool kQuad>
+template <int BN, int kEpi, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
     qkv_gemm_mxf8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW,
                               const __grid_constant__ CUtensorMap tmSF, const GemmShape g, const GemmArgs a,
                               const __grid_constant__ NormRopeArgs nr) {
-  static_assert(!(kQuad && kFused), "the in-GEMM norm form runs on pairs only");
-  using C = K1PairCfg<BN, kEpi != kEpiHead>;
+  using C = K1PairCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -880,22 +879,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();       // rank in the cluster
-  const uint32_t rank = kQuad ? (crank & 1u) : crank;  // rank in the pair
-  // cluster rank of this pair's leader (a constant for plain pairs: the pair kernel's
-  // code stays as it was without the cluster form, which measured 1.8 % faster)
-  const uint32_t lead = kQuad ? (crank & ~1u) : 0u;
-  const uint32_t qpair = kQuad ? (crank >> 1) : 0u;  // which pair of the cluster
+  const uint32_t rank = cluster_ctarank();  // rank in the pair
+  constexpr uint32_t lead = 0u;             // cluster rank of the pair's leader
   const bool leader = rank == 0;
   // Tiles of this pair: tile_first, tile_first + tile_step, ...
-  const int tile_first = kQuad ? 2 * static_cast<int>(blockIdx.x >> 2) + static_cast<int>(qpair)
-                               : static_cast<int>(blockIdx.x >> 1);
-  const int tile_step = kQuad ? 2 * static_cast<int>(gridDim.x >> 2) : static_cast<int>(gridDim.x >> 1);
+  const int tile_first = static_cast<int>(blockIdx.x >> 1);
+  const int tile_step = static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), kQuad ? 2 : 1);
+      mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&tfull[s]), 1);
@@ -943,30 +937,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = (a.flags & kFlagTestStall) == 0;
+      const int n_stages = (g.k_stages + C::KW - 1) / C::KW;
       for (int tile = tile_first; ok && tile < num_tiles; tile += tile_step) {
         int m_blk, n_blk;
         tile_coords(g, tile, m_blk, n_blk);
-        for (int kb = 0; kb < g.k_stages; ++kb) {
+        for (int ks = 0; ks < n_stages; ++ks) {
           if (!mbar_wait_bounded(smem_u32(&empty[stage]), phase ^ 1u, abort_flag, kWaitLimitNs)) {
             record_failure(a.status, abort_flag, kErrProducerEmptyWait);
             ok = false;
             break;
           }
+          const int kb0 = ks * C::KW;  // first 128-byte K block of the stage
+          const int halves = g.k_stages - kb0 < C::KW ? g.k_stages - kb0 : C::KW;
           const uint32_t fb_local = smem_u32(&full[stage]);
-          if (leader) mbar_arrive_expect_tx(fb_local, 2 * C::STAGE_BYTES);
+          if (leader)
+            mbar_arrive_expect_tx(fb_local, 2u * static_cast<uint32_t>(halves) * (C::A_HALF + C::B_HALF + C::SF_HALF));
           const uint32_t fb = mapa_shared(fb_local, lead);
-          if constexpr (kQuad) {
-            // rows [64 * qpair, 64 * qpair + 64) of this CTA's 128: to this rank in both pairs
-            tma_load_2d_pair_multicast(smem_u32(sA + stage * C::A_BYTES + qpair * (C::A_BYTES / 2)), &tmA, kb * kBK,
-                                       m_blk * 2 * kBM + static_cast<int>(rank) * kBM + static_cast<int>(qpair) * (kBM / 2),
-                                       fb, static_cast<uint16_t>((1u << rank) | (1u << (2u + rank))), pol_stream);
-          } else {
-            tma_load_2d_pair(smem_u32(sA + stage * C::A_BYTES), &tmA, kb * kBK,
+          for (int h = 0; h < halves; ++h) {
+            const int kb = kb0 + h;
+            tma_load_2d_pair(smem_u32(sA + stage * C::A_BYTES + h * C::A_HALF), &tmA, kb * kBK,
                              m_blk * 2 * kBM + static_cast<int>(rank) * kBM, fb, pol_stream);
+            tma_load_2d_pair(smem_u32(sB + stage * C::B_BYTES + h * C::B_HALF), &tmW, kb * kBK,
+                             n_blk * BN + static_cast<int>(rank) * C::HALF_N, fb, pol_keep);
+            tma_load_2d_pair(smem_u32(sSFB + stage * C::SFB_BYTES + h * C::SF_HALF), &tmSF, 0,
+                             n_blk * g.k_stages + kb, fb, pol_keep);
           }
-          tma_load_2d_pair(smem_u32(sB + stage * C::B_BYTES), &tmW, kb * kBK,
-                           n_blk * BN + static_cast<int>(rank) * C::HALF_N, fb, pol_keep);
-          tma_load_2d_pair(smem_u32(sSFB + stage * C::SFB_BYTES), &tmSF, 0, n_blk * g.k_stages + kb, fb, pol_keep);
           ++issued;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -1001,6 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_mxf8_e4m3(2 * kBM, BN);
       const uint32_t sfa_t = tmem_base + C::SFA_COL;
       const uint32_t sfb_t = tmem_base + C::SFB_COL;
+      const int n_stages = (g.k_stages + C::KW - 1) / C::KW;
       tc_copy_32x128b_x4_pair(sfa_t, smem_desc_plain(smem_u32(sSFA)));
       int stage = 0;
       uint32_t phase = 0;
@@ -1014,25 +1010,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_t = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < g.k_stages; ++kb) {
+        for (int ks = 0; ks < n_stages; ++ks) {
           if (!mbar_wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs)) {
             record_failure(a.status, abort_flag, kErrMmaFullWait);
             ok = false;
             break;
           }
           tc_fence_after();
+          const int halves = g.k_stages - ks * C::KW < C::KW ? g.k_stages - ks * C::KW : C::KW;
           const uint32_t sf_smem = smem_u32(sSFB + stage * C::SFB_BYTES);
+          // the block scales of both K blocks first, then their eight MMAs back to back
+          for (int h = 0; h < halves; ++h) {
 #pragma unroll
-          for (int c = 0; c < C::SF_CHUNKS; ++c)
-            tc_copy_32x128b_x4_pair(sfb_t + 4 * c, smem_desc_plain(sf_smem + 512 * c));
-          const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
-          const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
+            for (int c = 0; c < C::SF_CHUNKS; ++c)
+              tc_copy_32x128b_x4_pair(sfb_t + 4 * (h * C::SF_CHUNKS + c),
+                                      smem_desc_plain(sf_smem + h * C::SF_HALF + 512 * c));
+          }
+          for (int h = 0; h < halves; ++h) {
+            const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES + h * C::A_HALF));
+            const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES + h * C::B_HALF));
+            const uint32_t sfb_h = sfb_t + static_cast<uint32_t>(4 * h * C::SF_CHUNKS);
 #pragma unroll
-          for (int k = 0; k < kBK / 32; ++k)
-            mma_mxf8_pair(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t,
-                          (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBK / 32; ++k)
+              mma_mxf8_pair(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_h,
+                            (ks | h | k) != 0 ? 1u : 0u);
+          }
           // the stage is free once every CTA that wrote into it sees this pair done
-          tc_commit_pair_multicast(smem_u32(&empty[stage]), kQuad ? 0xF : static_cast<uint16_t>(0x3u << lead));
+          tc_commit_pair_multicast(smem_u32(&empty[stage]), static_cast<uint16_t>(0x3u << lead));
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -1134,28 +1138,19 @@ cudaError_t launch_gemm_t(const GemmShape& g, const CUtensorMap& tmA, const CUte
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, g, a);
 }
 
-// The launch of the CTA-pair GEMM: clusters of one pair, or of two pairs sharing
-// their A tiles (kQuad; the tile count must be even and `clusters` at most what the
-// device holds at once, from gemm_quad_clusters).
-template <int BN, int kEpi, bool kFused, bool kQuad = false>
+// The launch of the CTA-pair GEMM: clusters of one pair, one pair per two SMs.
+template <int BN, int kEpi, bool kFused>
 cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,
                                const CUtensorMap& tmSF, const GemmArgs& a, const NormRopeArgs& nr, cudaStream_t s,
-                               int num_sms, int quad_clusters = 0) {
-  using C = K1PairCfg<BN, kEpi != kEpiHead>;
-  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, kFused, kQuad>;
+                               int num_sms) {
+  using C = K1PairCfg<BN>;
+  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, kFused>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(C::SMEM));
   if (e != cudaSuccess) return e;
   const int tiles = g.m_tiles * g.n_tiles;
-  int grid;
-  if constexpr (kQuad) {
-    if (tiles % 2 != 0 || quad_clusters < 1) return cudaErrorInvalidValue;
-    const int units = tiles / 2;
-    grid = 4 * (units < quad_clusters ? units : quad_clusters);
-  } else {
-    const int pairs = num_sms / 2;
-    grid = 2 * (tiles < pairs ? tiles : pairs);
-  }
+  const int pairs = num_sms / 2;
+  const int grid = 2 * (tiles < pairs ? tiles : pairs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -1163,7 +1158,7 @@ cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kQuad ? 4 : 2;
+  attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlaps the prep kernel
@@ -1171,33 +1166,6 @@ cudaError_t launch_gemm_pair_t(const GemmShape& g, const CUtensorMap& tmA, const
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, tmA, tmW, tmSF, g, a, nr);
-}
-
-// How many clusters of two pairs of this GEMM the device holds at once (0 on error).
-template <int BN, int kEpi>
-int quad_clusters_t(int num_sms) {
-  using C = K1PairCfg<BN, kEpi != kEpiHead>;
-  auto kern = qkv_gemm_mxf8_pair_kernel<BN, kEpi, false, true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(C::SMEM)) !=
-      cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(4 * (num_sms / 4)));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = C::SMEM;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 4;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 0;
-  }
-  return n;
 }
 
 }  // namespace

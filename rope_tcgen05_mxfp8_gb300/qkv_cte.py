@@ -39,7 +39,6 @@ QKV_CTE_FLAG_GEMM_CTA_PAIR = 0x8
 QKV_CTE_FLAG_GEMM_SINGLE_CTA = 0x10
 QKV_CTE_FLAG_NORM_IN_GEMM = 0x20
 QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE = 0x40
-QKV_CTE_FLAG_GEMM_A_MULTICAST = 0x80
 
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
             "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",
@@ -75,8 +74,6 @@ class qkv_cte_plan_info(ctypes.Structure):
         ("cta_pair", ctypes.c_int32),
         ("norm_in_gemm", ctypes.c_int32),
         ("workspace_bytes", ctypes.c_int64),
-        ("a_multicast", ctypes.c_int32),
-        ("a_multicast_ran", ctypes.c_int32),
     ]
 
 
@@ -345,7 +342,7 @@ class QkvCte:
         self.workspace = torch.zeros(max(self.workspace_bytes, 256), dtype=torch.uint8, device=dev)
 
     def plan_info(self) -> qkv_cte_plan_info:
-        """The plan's choices now (a_multicast_ran reflects the latest run)."""
+        """The plan's choices."""
         return qkv_cte_get_plan_info(self.plan)
 
     def __call__(self, A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, out=None,

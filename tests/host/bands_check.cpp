@@ -1,7 +1,5 @@
 // Host check of the GEMM's banded tile order (compiled and run by tests/test_host_logic.py).
-// Usage: bands_check T H I tile_n k_end band_tiles [quad]   -> prints "ok <n_bands>" or an error.
-// With quad = 1 (n_tiles even) every band must hold an even number of N tiles, so that
-// linear tiles 2u and 2u+1 share their row panel.
+// Usage: bands_check T H I tile_n k_end band_tiles   -> prints "ok <n_bands>" or an error.
 #include <cstdio>
 #include <cstdlib>
 #include <vector>
@@ -9,7 +7,7 @@
 #include "internal.h"
 
 int main(int argc, char** argv) {
-  if (argc != 7 && argc != 8) return 2;
+  if (argc != 7) return 2;
   qkvcte::GemmShape g{};
   g.T = atoi(argv[1]);
   g.H = atoi(argv[2]);
@@ -21,35 +19,26 @@ int main(int argc, char** argv) {
   g.n_tiles = (g.I + g.tile_n - 1) / g.tile_n;
   g.n_qk_tiles = (k_end + g.tile_n - 1) / g.tile_n;
   if (g.n_qk_tiles > g.n_tiles) g.n_qk_tiles = g.n_tiles;
-  g.quad = argc == 8 ? atoi(argv[7]) : 0;
-  if (g.quad && g.n_tiles % 2 != 0) { printf("quad needs an even tile count\n"); return 1; }
   qkvcte::make_bands(g, band_tiles);
   const int total = g.m_tiles * g.n_tiles;
   if (g.band_tile0[g.n_bands] != total) { printf("bad total %d vs %d\n", g.band_tile0[g.n_bands], total); return 1; }
   if (g.n_bands > qkvcte::kMaxBands) { printf("too many bands\n"); return 1; }
   std::vector<int> seen(total, 0);
   bool in_v = false;
-  int prev_m = -1;
   for (int t = 0; t < total; ++t) {
     int m, n;
     qkvcte::tile_coords(g, t, m, n);
     if (m < 0 || m >= g.m_tiles || n < 0 || n >= g.n_tiles) { printf("out of range at %d\n", t); return 1; }
     seen[m * g.n_tiles + n]++;
-    // with quad the Q/K run is rounded up to even: it may take in the first V-only tile
-    const bool qk = n < g.n_qk_tiles + (g.quad ? (g.n_qk_tiles & 1) : 0);
+    const bool qk = n < g.n_qk_tiles;
     if (in_v && qk) { printf("Q/K tile after a V tile at %d\n", t); return 1; }
     in_v = in_v || !qk;
-    if (g.quad && (t & 1) && m != prev_m) { printf("tiles %d and %d are in different row panels\n", t - 1, t); return 1; }
-    prev_m = m;
   }
-  if (g.quad)
-    for (int b = 0; b < g.n_bands; ++b)
-      if (g.band_nc[b] % 2 != 0) { printf("band %d holds an odd number of tiles\n", b); return 1; }
   for (int i = 0; i < total; ++i)
     if (seen[i] != 1) { printf("tile %d visited %d times\n", i, seen[i]); return 1; }
   const int v_tiles = g.n_tiles - g.n_qk_tiles;
   const int need = (v_tiles + band_tiles - 1) / band_tiles + (g.n_qk_tiles + band_tiles - 1) / band_tiles;
-  if (need <= qkvcte::kMaxBands && !g.quad) {  // otherwise bands are widened to fit the cap
+  if (need <= qkvcte::kMaxBands) {  // otherwise bands are widened to fit the cap
     for (int b = 0; b < g.n_bands; ++b)
       if (g.band_nc[b] > band_tiles) { printf("band %d too wide\n", b); return 1; }
   }

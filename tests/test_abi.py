@@ -40,7 +40,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_version():
-    assert pkg.qkv_cte_version() == 3
+    assert pkg.qkv_cte_version() == 4
 
 
 def _plan_code(**kw):
@@ -185,31 +185,6 @@ def test_plan_info_reports_the_choices():
     with pytest.raises(q.QkvCteError):
         q.qkv_cte_plan(q.make_desc(300, 512, 4, 4, 128,
                                    flags=q.QKV_CTE_FLAG_GEMM_CTA_PAIR | q.QKV_CTE_FLAG_GEMM_SINGLE_CTA))
-
-
-def test_plan_info_reports_when_two_pairs_share_a():
-    """The A-sharing cluster form runs on request (QKV_CTE_FLAG_GEMM_A_MULTICAST) and only
-    with the CTA-pair form, an even number of N tiles, the plain epilogue and the norm/RoPE
-    work outside the GEMM."""
-    A = q.QKV_CTE_FLAG_GEMM_A_MULTICAST
-    wan = dict(tokens=32760, hidden=5120, n_q_heads=40, n_kv_heads=40, d_head=128)
-    cases = [
-        (dict(wan), 0),                                                                  # default: off
-        (dict(wan, flags=A), 1),                                                         # 64 N tiles
-        (dict(tokens=32760, hidden=5120, n_q_heads=40, n_kv_heads=0, d_head=128, flags=A), 1),  # 22 tiles
-        (dict(tokens=256, hidden=512, n_q_heads=4, n_kv_heads=4, d_head=128, flags=A), 0),      # 7 tiles
-        (dict(tokens=100, hidden=512, n_q_heads=4, n_kv_heads=4, d_head=128, tile_n=128, flags=A), 0),  # one CTA
-        (dict(wan, norm=2, flags=A), 0),                                                 # per-head norm
-        (dict(wan, flags=A | q.QKV_CTE_FLAG_NORM_IN_GEMM), 0),                           # norm in the GEMM
-    ]
-    for kw, expect in cases:
-        plan, _ = q.qkv_cte_plan(q.make_desc(**kw))
-        try:
-            info = q.qkv_cte_get_plan_info(plan)
-            assert info.a_multicast == expect, kw
-            assert info.a_multicast_ran == -1, kw  # no run yet
-        finally:
-            q.qkv_cte_destroy(plan)
 
 
 def test_error_message_is_recorded():

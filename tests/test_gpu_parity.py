@@ -499,80 +499,3 @@ def test_independent_calls_on_two_streams():
     for c, inp, op, out, ss, s in zip(calls, inps, ops, outs, sss, streams):
         op.status(s)
         check_outputs(c, inp, out, ss, None, name=c.name)
-
-
-# --- two CTA pairs sharing each A tile (QKV_CTE_FLAG_GEMM_A_MULTICAST, on request) ---
-
-def _a_sharing_call(name):
-    if name == "ragged":  # 4 N tiles, last 256-row panel only partly filled
-        return wl.custom_call(name="share_ragged", tokens=300, hidden=1024, n_q_heads=3, n_kv_heads=2, d_head=128,
-                              seed=101, has_w_col_scale=True)
-    if name == "half_empty":  # T mod 256 in (0, 128]: the second CTA of each pair has no rows
-        return wl.custom_call(name="share_T129", tokens=129, hidden=512, n_q_heads=3, n_kv_heads=2, d_head=128,
-                              seed=103)
-    if name == "separate":  # one segment, 4 N tiles
-        return wl.custom_call(name="share_sep", tokens=333, hidden=512, n_q_heads=6, n_kv_heads=0, d_head=128,
-                              norm=1, rope=0, seed=107)
-    return wl.workload("short")[0]  # 64 N tiles, 16 row panels
-
-
-@pytest.mark.parametrize("name", ["ragged", "half_empty", "separate", "short"])
-@pytest.mark.parametrize("nbsd", [False, True])
-def test_a_sharing_clusters_match_oracle_and_plain_pairs(name, nbsd):
-    """With QKV_CTE_FLAG_GEMM_A_MULTICAST (and N tiles that pair up) the CTA-pair GEMM runs
-    in clusters of two pairs that compute neighbouring N tiles of one row panel and share
-    its A tile (each CTA loads half of its rows and multicasts them to both pairs). The
-    result matches the oracle and the default pair form: V bit for bit, Q/K to
-    rounding."""
-    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_A_MULTICAST
-
-    if nbsd and name == "short":
-        pytest.skip("the NBSd layout is covered on the small shapes")
-    call = _a_sharing_call(name)
-    inp = wl.make_inputs(call)
-    g = to_device(inp, DEV)
-    op_s, out_s, ss_s, inv_s = run_path(call, g, nbsd=nbsd, flags=QKV_CTE_FLAG_GEMM_A_MULTICAST)
-    op_p, out_p, ss_p, inv_p = run_path(call, g, nbsd=nbsd)
-    assert op_s.info.a_multicast == 1 and op_p.info.a_multicast == 0
-    # the cluster form really ran (not the pair form the run falls back to without room for it)
-    assert op_s.plan_info().a_multicast_ran == 1 and op_p.plan_info().a_multicast_ran == 0
-    op_s.status()
-    op_p.status()
-    check_outputs(call, inp, out_s, ss_s, inv_s, name=f"{call.name}_shared_a")
-    check_outputs(call, inp, out_p, ss_p, inv_p, name=f"{call.name}_plain_pairs")
-    assert_same_to_rounding(call, out_s, out_p, name=f"{call.name}_shared_vs_plain")
-
-
-def test_a_sharing_wan480p_sampled_and_repeatable():
-    """The Wan 480p shape in the A-sharing form: sampled rows against the oracle, and a
-    second run agreeing with the first to rounding."""
-    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_A_MULTICAST
-
-    call = wl.workload("wan480p")[0]
-    inp = wl.make_inputs(call)
-    g = to_device(inp, DEV)
-    op1, out1, ss1, inv1 = run_path(call, g, flags=QKV_CTE_FLAG_GEMM_A_MULTICAST)
-    assert op1.info.a_multicast == 1 and op1.plan_info().a_multicast_ran == 1
-    op1.status()
-    check_outputs(call, inp, out1, ss1, inv1, rows=sampled_rows(call), name="wan480p_shared_a")
-    op2, out2, _, _ = run_path(call, g, flags=QKV_CTE_FLAG_GEMM_A_MULTICAST)
-    op2.status()
-    assert_same_to_rounding(call, out1, out2, name="wan480p_shared_a_repeat")
-
-
-def test_a_sharing_bounded_wait_reports_timeout():
-    """A stalled load warp in the cluster form: every bounded wait of both pairs runs out,
-    the status reports it, and the next call on the same context is correct."""
-    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_GEMM_A_MULTICAST
-
-    call = _a_sharing_call("ragged")
-    inp = wl.make_inputs(call)
-    g = to_device(inp, DEV)
-    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_TEST_STALL | QKV_CTE_FLAG_GEMM_A_MULTICAST)
-    assert op.info.a_multicast == 1
-    with pytest.raises(QkvCteError) as ei:
-        op.status()
-    assert ei.value.code == QKV_CTE_ERR_DEVICE_TIMEOUT
-    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_GEMM_A_MULTICAST)
-    op.status()
-    check_outputs(call, inp, out, ss, inv, name="shared_a_after_timeout")

@@ -37,23 +37,6 @@ def test_banded_tile_order_covers_every_tile_once(bands_bin, T, H, I, tile_n, k_
     assert r.stdout.startswith("ok")
 
 
-@pytest.mark.parametrize("T,H,I,tile_n,k_end,band", [
-    (32760, 5120, 15360, 240, 10240, 23),   # Wan 480p: odd Q/K run (43 tiles) rounded up to 44
-    (32760, 5120, 15360, 240, 10240, 22),
-    (32760, 5120, 15360, 240, 10240, 1),    # bands of one tile widened to two
-    (4096, 5120, 5120, 240, 5120, 45),      # separate mode, 22 tiles
-    (300, 1024, 896, 240, 640, 3),          # 4 tiles, ragged rows
-    (75600, 5120, 15360, 256, 10240, 1),    # band cap with even widths
-])
-def test_paired_tile_order_keeps_each_pair_in_one_row_panel(bands_bin, T, H, I, tile_n, k_end, band):
-    """The A-sharing GEMM form runs linear tiles 2u and 2u+1 at once on two CTA pairs
-    that share the A tile: both must lie in the same row panel, in every band."""
-    r = subprocess.run([bands_bin, str(T), str(H), str(I), str(tile_n), str(k_end), str(band), "1"],
-                       capture_output=True, text=True)
-    assert r.returncode == 0, r.stdout + r.stderr
-    assert r.stdout.startswith("ok")
-
-
 def test_clock_samples_are_kept_only_inside_the_timed_region():
     """bench.py reports clocks from the nvidia-smi samples taken while the timed steps
     ran; idle samples before or after them must not enter the median."""
