@@ -35,7 +35,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused QKV-CTE FP8 TFLOP/s and % of dense FP8 peak at Wan 480p self-attn shape"
-NOMINAL_FP8_TFLOPS = 4500.0        # GB300 dense FP8 tensor peak, nominal
+# GB300 dense FP8 tensor peak per GPU: NVIDIA's GB300 NVL72 specifications give 720 PFLOPS
+# of FP8 for the 72-GPU rack with 2:4 sparsity, i.e. 10 PFLOPS sparse and 5 PFLOPS dense per
+# GPU. The HGX B300 board's figure (72 PFLOPS sparse for 8 GPUs: 4.5 dense per GPU) belongs
+# to the lower-power air-cooled part and is reported beside it for comparison only.
+NOMINAL_FP8_TFLOPS = 5000.0
+HGX_B300_FP8_TFLOPS = 4500.0
 FP8_PER_BF16 = 2.0                  # nominal dense FP8 / BF16 tensor rate ratio
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -65,6 +70,8 @@ def _args():
     p.add_argument("--no-flush", action="store_true", help="keep L2 warm between steps")
     p.add_argument("--cpu-rows", type=int, default=20480, help="oracle row sample for cpu_baseline")
     p.add_argument("--ref-rows", type=int, default=256, help="oracle row sample per reference step")
+    p.add_argument("--sustained-s", type=float, default=1.2,
+                   help="seconds of back-to-back steps for the sustained leg (0: skip)")
     return p.parse_args()
 
 
@@ -407,6 +414,44 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = per_s / 1e12
 
+    # Sustained leg: back-to-back steps for at least --sustained-s seconds (L2 flushed
+    # between steps as above), with their own clock record, so that the power cap the
+    # short timed region may not reach is in the number.
+    sustained = None
+    if args.sustained_s > 0:
+        n_sus = max(1, int(args.sustained_s / max(1e-4, statistics.median(step_ms) * 1e-3)) + 1)
+        sus_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_sus)]
+        sus_sampler = ClockSampler(gpu_uuid)
+        barrier()
+        sus_sampler.start()
+        time.sleep(0.3)
+        sus_sampler.mark_start()
+        for i in range(n_sus):
+            if not args.no_flush:
+                flush.zero_()
+            sus_ev[i][0].record(stream)
+            step()
+            sus_ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        sus_sampler.mark_end()
+        barrier()
+        sus_clocks = sus_sampler.stop()
+        op.status(stream)
+        sus_ms = [a.elapsed_time(b2) for a, b2 in sus_ev]
+        sus_per_s, sus_total = replica_throughput(sum(sus_ms), call.flops * n_sus, world, device=dev)
+        sus_value = sus_per_s / 1e12
+        _, bf16_b, bf16_s, _ = _peaks()
+        sus_peak = (bf16_s if bf16_s > 0 else bf16_b) * FP8_PER_BF16
+        sustained = {"value": sus_value, "unit": "TFLOP/s", "steps": n_sus, "seconds_of_steps": sus_total * 1e-3,
+                     "ms_per_step": sus_total / n_sus, "step_ms_spread": _spread(sus_ms),
+                     "pct_nominal_dense_fp8_peak": 100.0 * sus_value / (world * NOMINAL_FP8_TFLOPS),
+                     "frac_of_measured_sustained_fp8": sus_value / (world * sus_peak),
+                     "measured_sustained_fp8_peak": sus_peak,
+                     "clocks": sus_clocks,
+                     "how": "back-to-back steps (L2 flushed between them, outside the per-step events), "
+                            "per-step CUDA events, nvidia-smi clocks sampled every 20 ms inside the run; "
+                            "peak = measured sustained bf16 x nominal fp8/bf16 ratio"}
+
     prep_ms = statistics.mean(p[0] for p in passes)
     gemm_ms = statistics.mean(p[1] for p in passes)
     norm_span_ms = statistics.mean(p[2] for p in passes)
@@ -518,6 +563,10 @@ def run_ours(args):
         "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout, input_kind=args.input,
                           op_norm_in_gemm=bool(op.info.norm_in_gemm), gemm_form=gemm_form),
         "pct_nominal_dense_fp8_peak": 100.0 * value / (world * NOMINAL_FP8_TFLOPS),
+        "nominal_dense_fp8_peak": {"TFLOP/s": NOMINAL_FP8_TFLOPS,
+                                   "source": "NVIDIA GB300 NVL72 specifications: FP8 720 PFLOPS per 72 GPUs with "
+                                             "2:4 sparsity = 5 PFLOPS dense per GPU",
+                                   "pct_of_hgx_b300_4500": 100.0 * value / (world * HGX_B300_FP8_TFLOPS)},
         "pct_measured_fp8_peak": 100.0 * value / (world * fp8_peak),
         "passes_ms": {"prep": prep_ms, "gemm_epilogue": gemm_ms, "norm_rope_span": norm_span_ms,
                       "run": run_ms, "exposed_after_gemm": run_ms - prep_ms - gemm_ms,
@@ -536,6 +585,7 @@ def run_ours(args):
                      "peak_source": (f"{peak_src} bf16 {peak_kind} {bf16_used:.1f} TFLOP/s x nominal fp8/bf16 "
                                      f"ratio {FP8_PER_BF16:g}")},
         "step_ms_spread": _spread(step_ms),
+        "sustained": sustained,
         "clocks": clocks,
         "e2e": e2e,
         # prep + GEMM, the producer for a bf16 / packed input, and the norm/RoPE pass when

@@ -314,17 +314,29 @@ int qkv_cte_host_scratch_bytes(qkv_cte_plan_t plan, int32_t chunk_rows, size_t* 
  * 40+40 heads of 128) up to 640 tokens fit; so do the separate cross-attention K and
  * V calls on 512 context tokens.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * The array is part of the library's device code. CUDA maps code and array on a device
+ * the first time the library launches a kernel there (the first run of any entry point
+ * on that device), which is a one-time allocation by the driver; the first
+ * qkv_cte_run_noalloc on a device also looks up the array's address
+ * (cudaGetSymbolAddress). A caller that must not allocate at all therefore makes one
+ * call at start-up on each device it uses (this entry point or qkv_cte_run), before
+ * allocation is forbidden and before any stream capture; every later call allocates
+ * nothing.
  * Every call shares the one array and each call clears the parts that must start at
  * zero, so calls that overlap on the GPU (different streams, or other host threads)
  * race and corrupt each other's results: serialise them. Bounded-wait timeouts are
- * recorded in the array's status word, which this entry point does not report; use
- * qkv_cte_run with a workspace to read them with qkv_cte_status. */
+ * recorded in the array's status word: read it with qkv_cte_noalloc_status. */
 int qkv_cte_run_noalloc(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, const uint8_t* W,
                         const uint8_t* w_sf, const float* w_col_scale, const uint16_t* bias,
                         const uint16_t* gamma_q, const uint16_t* gamma_k, const float* cos_table,
                         const float* sin_table, uint16_t* O, float* sumsq, float* inv_rms, void* stream);
+
+/* qkv_cte_status for the array behind qkv_cte_run_noalloc on the current device: waits
+ * for `stream`, returns 0, or QKV_CTE_ERR_DEVICE_TIMEOUT (and clears the word) when a
+ * bounded wait of an earlier allocation-free call ran out, or -3 on a CUDA error.
+ * Allocates nothing. Like qkv_cte_run_noalloc it has no counterpart on the page this
+ * library follows. */
+int qkv_cte_noalloc_status(void* stream);
 
 /* Release a plan. NULL is a no-op. */
 void qkv_cte_destroy(qkv_cte_plan_t plan);

@@ -226,6 +226,10 @@ cudaError_t launch_gemm_fused(const GemmShape& g, const CUtensorMap& tmA, const 
 // K1 runs and take each row panel as soon as K1 marks it ready.
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap);
 
+// Device address (on the current device) of the allocation-free entry point's scratch
+// array (qkv_gemm_mxf8.cu); cudaGetSymbolAddress's status.
+cudaError_t noalloc_scratch_address(void** out);
+
 // dst |= src on the stream (qkv_gemm_mxf8.cu): the status of a run made of chunks.
 cudaError_t launch_status_or(const uint32_t* src, uint32_t* dst, cudaStream_t s);
 

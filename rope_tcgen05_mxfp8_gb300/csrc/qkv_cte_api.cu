@@ -872,10 +872,6 @@ extern "C" int qkv_cte_run_host(qkv_cte_plan_t plan, const void* A_host, const f
 
 namespace {
 
-// The scratch: QKV_CTE_NOALLOC_SCRATCH_BYTES on every GPU that loads the library,
-// held until the process exits.
-static __device__ __align__(256) uint8_t g_noalloc_scratch[QKV_CTE_NOALLOC_SCRATCH_BYTES];
-
 void* g_noalloc_ptr[kMaxDevices] = {};
 std::mutex g_noalloc_mu;
 
@@ -888,7 +884,7 @@ int noalloc_scratch(void** out) {
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
   if (g_noalloc_ptr[dev] == nullptr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = noalloc_scratch_address(&p);
     if (e != cudaSuccess || p == nullptr)
       return fail(QKV_CTE_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
     g_noalloc_ptr[dev] = p;
@@ -919,4 +915,11 @@ extern "C" int qkv_cte_run_noalloc(qkv_cte_plan_t plan, const uint8_t* A, const 
   // squares, panel counters) in its first kernel, on the same stream.
   return qkv_cte_run(plan, A, a_scale, W, w_sf, w_col_scale, bias, gamma_q, gamma_k, cos_table, sin_table, O,
                      sumsq, inv_rms, scratch, (size_t)QKV_CTE_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" int qkv_cte_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != QKV_CTE_OK) return rc;
+  return qkv_cte_status(scratch, stream);
 }

@@ -2,6 +2,7 @@
 // the scale repack / clear kernel, and the GEMM dispatch. The kernel templates and
 // their design notes are in qkv_gemm_mxf8.cuh.
 #include "qkv_gemm_mxf8.cuh"
+#include "qkv_cte.h"
 
 namespace qkvcte {
 
@@ -76,12 +77,21 @@ __global__ void __launch_bounds__(kPrepThreads) qkv_prep_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// The scratch of the allocation-free entry point: QKV_CTE_NOALLOC_SCRATCH_BYTES on every
+// GPU that loads the library, held until the process exits. It sits in the same
+// translation unit (one CUDA module) as the prep kernel, which every run launches
+// first: whatever call first runs on a device maps the module and the array together,
+// so a later lookup of the array's address maps nothing.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[QKV_CTE_NOALLOC_SCRATCH_BYTES];
+
 // dst |= src: one chunk's status word into the status word of a run made of chunks.
 __global__ void status_or_kernel(const uint32_t* __restrict__ src, uint32_t* __restrict__ dst) {
   if (threadIdx.x == 0) *dst |= *src;
 }
 
 }  // namespace
+
+cudaError_t noalloc_scratch_address(void** out) { return cudaGetSymbolAddress(out, g_noalloc_scratch); }
 
 cudaError_t launch_status_or(const uint32_t* src, uint32_t* dst, cudaStream_t s) {
   status_or_kernel<<<1, 32, 0, s>>>(src, dst);

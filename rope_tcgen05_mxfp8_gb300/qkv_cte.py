@@ -43,7 +43,7 @@ QKV_CTE_FLAG_HEAD_NORM_IN_EPILOGUE = 0x40
 EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times", "qkv_cte_destroy",
             "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",
             "qkv_cte_row_quantize", "qkv_cte_unpack_rows", "qkv_cte_interleaved_to_rotate_half",
-            "qkv_cte_run_host", "qkv_cte_host_scratch_bytes")
+            "qkv_cte_run_host", "qkv_cte_host_scratch_bytes", "qkv_cte_noalloc_status")
 QKV_CTE_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
@@ -108,6 +108,8 @@ def load() -> ctypes.CDLL:
     lib.qkv_cte_get_plan_info.restype = ctypes.c_int
     lib.qkv_cte_run_noalloc.argtypes = [P] * 15
     lib.qkv_cte_run_noalloc.restype = ctypes.c_int
+    lib.qkv_cte_noalloc_status.argtypes = [P]
+    lib.qkv_cte_noalloc_status.restype = ctypes.c_int
     lib.qkv_cte_row_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P, P]
     lib.qkv_cte_row_quantize.restype = ctypes.c_int
     lib.qkv_cte_unpack_rows.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
@@ -313,6 +315,14 @@ def qkv_cte_status(workspace, stream=None) -> int:
         stream = torch.cuda.current_stream()
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     return _check(load().qkv_cte_status(_ptr("workspace", workspace), ctypes.c_void_p(handle)))
+
+
+def qkv_cte_noalloc_status(stream=None) -> int:
+    """qkv_cte_status for the scratch array of qkv_cte_run_noalloc on the current device."""
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return _check(load().qkv_cte_noalloc_status(ctypes.c_void_p(handle)))
 
 
 def qkv_cte_pass_times(plan):

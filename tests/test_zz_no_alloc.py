@@ -8,9 +8,11 @@ same kernels with their scratch in a fixed array inside the library instead of a
 caller-provided workspace.
 
 These tests call it through the C ABI twice in a row and check each result against
-qkv_cte_run (the entry point with a workspace) and the float64 oracle, and check that
-a problem too large for the fixed array is refused before anything is launched. The
-file is named so that pytest collects it after every other test file.
+qkv_cte_run (the entry point with a workspace) and the float64 oracle; check that its
+first call after a warm-up run leaves the device's free memory unchanged; that a
+bounded-wait timeout in it is reported by qkv_cte_noalloc_status; and that a problem
+too large for the fixed array is refused before anything is launched. The file is
+named so that pytest collects it after every other test file.
 """
 import numpy as np
 import pytest
@@ -68,6 +70,69 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(name):
             check_outputs(call, inp, out, ss, inv, name=f"noalloc_{name}_{call_no}")
     finally:
         q.qkv_cte_destroy(plan)
+
+
+@pytest.mark.gpu
+def test_noalloc_first_call_after_warm_up_allocates_nothing():
+    """A caller that forbids allocation warms the library up once (any run on the
+    device maps its device code, the scratch array included); the first allocation-free
+    call after that must not change the device's free memory."""
+    call = _cases()["edge"]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, dev)
+    op, _, _, _ = run_path(call, g)  # warm-up through qkv_cte_run (its own workspace)
+    op.status()
+    desc = q.make_desc(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
+                       rope=call.rope, eps=call.eps)
+    plan, _ = q.qkv_cte_plan(desc)
+    out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=dev)
+    ss = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
+    inv = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
+    try:
+        torch.cuda.synchronize(dev)
+        free_before, _ = torch.cuda.mem_get_info(dev)
+        q.qkv_cte_run_noalloc(plan, g["A"], g["a_scale"], g["W"], g["w_sf"], g["w_col_scale"], g["bias"],
+                              g["gamma_q"], g["gamma_k"], g["cos"], g["sin"], out, ss, inv)
+        q.qkv_cte_noalloc_status()
+        torch.cuda.synchronize(dev)
+        free_after, _ = torch.cuda.mem_get_info(dev)
+        assert free_after == free_before, f"free device memory changed by {free_before - free_after} bytes"
+        check_outputs(call, inp, out, ss, inv, name="noalloc_after_warm_up")
+    finally:
+        q.qkv_cte_destroy(plan)
+
+
+@pytest.mark.gpu
+def test_noalloc_status_reports_a_stalled_call_and_the_next_call_is_correct():
+    """The test hook that stalls the GEMM's load warp makes every bounded wait of an
+    allocation-free call run out; qkv_cte_noalloc_status reports it (and clears the
+    word), and the next allocation-free call on the same context is correct."""
+    call = _cases()["edge"]
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, dev)
+    out = torch.empty(call.tokens, call.width, dtype=torch.bfloat16, device=dev)
+    ss = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
+    inv = torch.empty(call.tokens, 2, dtype=torch.float32, device=dev)
+    for flags, expect_timeout in ((q.QKV_CTE_FLAG_TEST_STALL, True), (0, False)):
+        plan, _ = q.qkv_cte_plan(q.make_desc(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head,
+                                             norm=call.norm, rope=call.rope, eps=call.eps, flags=flags))
+        try:
+            q.qkv_cte_run_noalloc(plan, g["A"], g["a_scale"], g["W"], g["w_sf"], g["w_col_scale"], g["bias"],
+                                  g["gamma_q"], g["gamma_k"], g["cos"], g["sin"], out, ss, inv)
+            if expect_timeout:
+                with pytest.raises(q.QkvCteError) as ei:
+                    q.qkv_cte_noalloc_status()
+                assert ei.value.code == q.QKV_CTE_ERR_DEVICE_TIMEOUT
+                q.qkv_cte_noalloc_status()  # cleared
+            else:
+                q.qkv_cte_noalloc_status()
+                check_outputs(call, inp, out, ss, inv, name="noalloc_after_stall")
+        finally:
+            q.qkv_cte_destroy(plan)
 
 
 def test_noalloc_refuses_a_problem_larger_than_its_scratch():
