@@ -53,6 +53,8 @@ def _args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="wan480p")
+    p.add_argument("--call", type=int, default=0,
+                   help="which call of a multi-call workload to time (cross: 0 = Q, 1 = K, 2 = V)")
     p.add_argument("--tile-n", type=int, default=0)
     p.add_argument("--gemm", choices=["auto", "pair", "single"], default="auto",
                    help="GEMM form: 256-row tiles on SM pairs, 128-row tiles on one SM, or the library's choice")
@@ -267,7 +269,7 @@ def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
         return 0
-    call = wl.workload(args.workload)[0]
+    call = wl.workload(args.workload)[args.call]
     inp = wl.make_inputs(call)
     rows = wl.sample_rows(call, args.ref_rows).numpy()
     flops = 2.0 * len(rows) * call.hidden * call.width
@@ -287,7 +289,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(call, 0, flushed=False),
+        "config": _config(call),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -302,22 +304,42 @@ _INPUT_NOTE = {
 }
 
 
-def _config(call, tile_n, flushed=True, layout="bsd", input_kind="fp8", op_norm_in_gemm=False, gemm_form=None):
+def _describe(call):
+    """What the timed call computes, with its sizes."""
+    if call.n_kv_heads == 0:
+        kind = "Wan2.2-style cross-attention single-segment projection (separate Q, K or V call)"
+    elif call.n_q_heads == 0:
+        kind = "Wan2.2-style cross-attention K|V projection of the context tokens in one call"
+    else:
+        kind = "Wan2.2-style fused QKV self-attention projection"
+    norm = {0: "no qk-norm", 1: "across-heads RMSNorm", 2: "per-head RMSNorm", 3: "per-head LayerNorm"}[call.norm]
+    rope = ("3D-grid rotate-half RoPE" if call.rope_grid else "1D rotate-half RoPE") if call.rope else "no RoPE"
+    return (f"{call.name}: {kind}, T={call.tokens} H={call.hidden} n_q={call.n_q_heads} n_kv={call.n_kv_heads} "
+            f"d_head={call.d_head} I={call.width}, {norm}, {rope}")
+
+
+def _config(call, layout="bsd", input_kind="fp8"):
+    """The workload: what is computed, on which shapes and data layouts. The same for
+    both arms (how our arm runs it, e.g. the GEMM form and the L2 flushing, is reported
+    beside it, under "implementation")."""
     return {
-        "workload": (f"{call.name}: Wan2.2-style fused QKV self-attention projection, T={call.tokens} "
-                     f"H={call.hidden} n_q={call.n_q_heads} n_kv={call.n_kv_heads} d_head={call.d_head} "
-                     f"I={call.width}, across-heads Q/K RMSNorm + 3D-grid rotate-half RoPE"),
+        "workload": _describe(call),
         "tokens": call.tokens, "hidden": call.hidden, "width": call.width,
         "n_q_heads": call.n_q_heads, "n_kv_heads": call.n_kv_heads, "d_head": call.d_head,
+        "output_layout": "NBSd [heads, T, d_head]" if layout == "nbsd" else "BSD [T, I]",
+        "qk_norm": {0: "none", 1: "across heads (RMS)", 2: "per head RMS", 3: "per head LayerNorm"}[call.norm],
+        "input": _INPUT_NOTE[input_kind],
+    }
+
+
+def _implementation(tile_n, flushed=True, op_norm_in_gemm=False, gemm_form=None, head_norm_in_epilogue=False):
+    return {
         "tile_n": tile_n,
         "gemm_form": gemm_form,
-        "output_layout": "NBSd [heads, T, d_head]" if layout == "nbsd" else "BSD [T, I]",
-        "norm_rope_work": "inside the GEMM's epilogue warps" if op_norm_in_gemm else "its own kernel, overlapped with the GEMM",
-        "qk_norm": {0: "none", 1: "across heads (RMS)", 2: "per head RMS, in the GEMM epilogue",
-                    3: "per head LayerNorm, in the GEMM epilogue"}[call.norm],
-        "input": _INPUT_NOTE[input_kind],
-        "l2": "flushed between timed steps (256 MB write, outside the step events)" if flushed
-        else "not flushed",
+        "norm_rope_work": ("inside the GEMM's epilogue" if head_norm_in_epilogue else
+                           "inside the GEMM's epilogue warps" if op_norm_in_gemm else
+                           "its own kernel, overlapped with the GEMM"),
+        "l2": "flushed between timed steps (256 MB write, outside the step events)" if flushed else "not flushed",
     }
 
 
@@ -348,11 +370,13 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    call = wl.workload(args.workload)[0]
+    call = wl.workload(args.workload)[args.call]
     if args.norm != "across":
         call = dataclasses.replace(call, norm={"head_rms": 2, "head_layer": 3}[args.norm])
     inp = wl.make_inputs(call)
     g = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    gq = g["gamma_q"] if call.norm else None  # gammas only where a segment is normalised
+    gk = g["gamma_k"] if call.norm else None
     gemm_flag = {"auto": 0, "pair": QKV_CTE_FLAG_GEMM_CTA_PAIR, "single": QKV_CTE_FLAG_GEMM_SINGLE_CTA}[args.gemm]
     if args.norm_in_gemm:
         from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_NORM_IN_GEMM
@@ -379,7 +403,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        op(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"],
+        op(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], gq, gk, g["cos"], g["sin"],
            out=out, sumsq=sumsq, stream=stream)
 
     for _ in range(max(args.warmup, 0)):
@@ -467,7 +491,7 @@ def run_ours(args):
     for i in range(max(3, min(args.steps, 10))):
         if not args.no_flush:
             flush.zero_()
-        serial(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"],
+        serial(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], gq, gk, g["cos"],
                g["sin"], out=out, sumsq=sumsq, stream=stream)
         ser.append(serial.pass_times())
     serial.status(stream)
@@ -506,7 +530,7 @@ def run_ours(args):
             if not args.no_flush:
                 flush.zero_()
             e0.record(stream)
-            op.run_host(A_h, s_h, g["W"], g["w_sf"], g["bias"], g["gamma_q"], g["gamma_k"], g["cos"], g["sin"], O_h,
+            op.run_host(A_h, s_h, g["W"], g["w_sf"], g["bias"], gq, gk, g["cos"], g["sin"], O_h,
                         w_col_scale=g["w_col_scale"], sumsq=sumsq, chunk_rows=args.e2e_chunk, stream=stream)
             e1.record(stream)
             if i >= args.warmup:
@@ -560,8 +584,9 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded; Wan2.2 480p shapes and distributions)",
-        "config": _config(call, tile_n, flushed=not args.no_flush, layout=args.layout, input_kind=args.input,
-                          op_norm_in_gemm=bool(op.info.norm_in_gemm), gemm_form=gemm_form),
+        "config": _config(call, layout=args.layout, input_kind=args.input),
+        "implementation": _implementation(tile_n, flushed=not args.no_flush, op_norm_in_gemm=bool(op.info.norm_in_gemm),
+                                          gemm_form=gemm_form),
         "pct_nominal_dense_fp8_peak": 100.0 * value / (world * NOMINAL_FP8_TFLOPS),
         "nominal_dense_fp8_peak": {"TFLOP/s": NOMINAL_FP8_TFLOPS,
                                    "source": "NVIDIA GB300 NVL72 specifications: FP8 720 PFLOPS per 72 GPUs with "

@@ -126,10 +126,13 @@ enum { QKV_CTE_INPUT_ROW_FP8 = 0, QKV_CTE_INPUT_PACKED = 1, QKV_CTE_INPUT_BF16 =
 typedef struct {
     int64_t tokens;        /* T = B*S rows; 0 is allowed (nothing is launched); <= INT32_MAX */
     int32_t hidden;        /* H, contraction length; multiple of 128 */
-    int32_t n_q_heads;     /* Q heads in this call (>= 1) */
+    int32_t n_q_heads;     /* Q heads in this call (>= 1; 0 in fused mode: a K|V call, e.g. the
+                              cross-attention K and V projections of the context tokens as one
+                              launch, W = [W_k; W_v], K normalised with gamma_k, V as projected) */
     int32_t n_kv_heads;    /* K/V heads; 0 for a single-segment (separate) call */
     int32_t d_head;        /* head dim; multiple of 16, of 32 when a norm or RoPE runs */
-    int32_t mode;          /* QKV_CTE_MODE_FUSED (n_kv >= 1) or QKV_CTE_MODE_SEPARATE (n_kv == 0) */
+    int32_t mode;          /* QKV_CTE_MODE_FUSED (n_kv >= 1, n_q >= 0) or QKV_CTE_MODE_SEPARATE
+                              (n_kv == 0, n_q >= 1) */
     int32_t norm;          /* QKV_CTE_NORM_*: 0 none, 1 across heads, 2 per-head RMS, 3 per-head LayerNorm */
     int32_t rope;          /* 1: rotate-half RoPE on Q (and K); needs cos/sin */
     int32_t output_layout; /* QKV_CTE_LAYOUT_BSD: O[T, I]; QKV_CTE_LAYOUT_NBSD: O[I/d_head, T, d_head]
@@ -176,8 +179,8 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info);
  * w_sf       : uint8  [I, H/32]   UE8M0 block scales, row-major; 4-byte aligned
  * w_col_scale: fp32   [I] or NULL per-output-channel multiplier ("weight_scales"); 16-byte aligned
  * bias       : bf16   [I] or NULL; 16-byte aligned
- * gamma_q    : bf16   Q gamma, required iff norm != NONE: [n_q*d_head] (across heads) or [d_head]
- *              (per head); 16-byte aligned
+ * gamma_q    : bf16   Q gamma, required iff norm != NONE and n_q > 0: [n_q*d_head] (across heads)
+ *              or [d_head] (per head), else NULL; 16-byte aligned
  * gamma_k    : bf16   K gamma, [n_kv*d_head] or [d_head]; required iff norm != NONE and n_kv > 0,
  *              else NULL
  * cos_table, sin_table: fp32 [T, d_head] rotate-half tables; required iff rope, else NULL;
@@ -185,9 +188,11 @@ int qkv_cte_get_plan_info(qkv_cte_plan_t plan, qkv_cte_plan_info* info);
  * O          : bf16 output, [T, I] (BSD) or [I/d_head, T, d_head] (NBSd: element (h, t, j)
  *              is column h*d_head + j of token t); 32-byte aligned; must not alias any input
  * sumsq      : fp32   [T, 2] or NULL: per-token sum of o^2 over the un-normalised Q and K
- *              segments ([qkv_cte] "Design" 1 step a; column 1 is 0 when n_kv == 0)
+ *              segments ([qkv_cte] "Design" 1 step a; column 1 is 0 when n_kv == 0, column 0
+ *              when n_q == 0)
  * inv_rms    : fp32   [T, 2] or NULL: the rsqrt factors of step b (written iff norm is
- *              ACROSS_HEADS; must be NULL with a per-head norm)
+ *              ACROSS_HEADS; must be NULL with a per-head norm; the column of an absent
+ *              segment is 0)
  * workspace  : device scratch of at least the planned size; 256-byte aligned
  * With tokens == 0 every tensor pointer may be NULL: no kernel is launched and only
  * the workspace's status word is reset (when a workspace is given).

@@ -158,7 +158,9 @@ def segments(n_q_heads: int, n_kv_heads: int, d_head: int):
     """Column ranges of the Q, K and V segments of O: I = (n_q + 2 n_kv) * d_head.
 
     With n_kv_heads == 0 there is one segment and it is treated as Q
-    ([qkv_cte] "Design" 5).
+    ([qkv_cte] "Design" 5). With n_q_heads == 0 (and n_kv_heads > 0) the Q segment is
+    empty: the call projects K and V only (the cross-attention K and V calls of
+    "Design" 5 run as one).
     """
     q = (0, n_q_heads * d_head)
     k = (q[1], q[1] + n_kv_heads * d_head)
@@ -186,10 +188,12 @@ def inv_rms(sumsq: np.ndarray, n_q_heads: int, n_kv_heads: int, d_head: int, eps
 
     [qkv_cte] "Design" 1, step b (reduce). With one GPU holding every head, tp = 1
     and the cross-rank AllReduce is the identity. The K column is 0 when the call
-    has no K segment (its rsqrt is skipped, "Design" 5).
+    has no K segment (its rsqrt is skipped, "Design" 5); likewise the Q column when
+    the call has no Q heads (a K|V call).
     """
     out = np.zeros_like(sumsq)
-    out[:, SEG_Q] = 1.0 / np.sqrt(sumsq[:, SEG_Q] / (n_q_heads * d_head * tp) + eps)
+    if n_q_heads > 0:
+        out[:, SEG_Q] = 1.0 / np.sqrt(sumsq[:, SEG_Q] / (n_q_heads * d_head * tp) + eps)
     if n_kv_heads > 0:
         out[:, SEG_K] = 1.0 / np.sqrt(sumsq[:, SEG_K] / (n_kv_heads * d_head * tp) + eps)
     return out
@@ -325,7 +329,7 @@ def qkv_cte(A, a_scale, W, w_sf, bias, gamma_q, gamma_k, cos, sin, *, n_q_heads:
     inv = inv_rms(ss, n_q_heads, n_kv_heads, d_head, eps) if across else np.zeros_like(ss)
     out = o.copy()
     q, k, _ = segments(n_q_heads, n_kv_heads, d_head)
-    parts = [(q, SEG_Q, gamma_q)] + ([(k, SEG_K, gamma_k)] if n_kv_heads > 0 else [])
+    parts = ([(q, SEG_Q, gamma_q)] if n_q_heads > 0 else []) + ([(k, SEG_K, gamma_k)] if n_kv_heads > 0 else [])
     for (c0, c1), seg, gamma in parts:
         x = o[:, c0:c1]
         if norm in (NORM_HEAD_RMS, NORM_HEAD_LAYER):

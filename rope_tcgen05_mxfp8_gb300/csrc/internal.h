@@ -192,6 +192,7 @@ struct NormRopeArgs {
   const float* head_stats;
   int stat_parts;
   int tile_n;
+  int head_group;            // heads per task of the standalone pass (set at its launch)
 };
 
 // Supported N tiles (compile-time instantiations of K1).

@@ -23,7 +23,17 @@ namespace qkvcte {
 namespace {
 
 constexpr int kThreads = 128;
-constexpr int kHeadGroup = 20;  // heads per warp task: small tasks keep the warps evenly loaded to the end
+// Heads per warp task: at most 20 (small tasks keep the warps evenly loaded to the
+// end); fewer when the problem is small, so that every warp of the grid gets a task
+// (the 512-token cross-attention K|V call: 4 heads per task, 640 tasks for 608 warps
+// instead of 128 tasks of 20 heads, which ran latency-bound on 32 blocks).
+constexpr int kHeadGroups[] = {20, 10, 5, 4, 2, 1};
+
+int head_group_for(const NormRopeArgs& a, long long warps) {
+  for (int g : kHeadGroups)
+    if (nrp::task_count(a, g) >= warps) return g;
+  return 1;
+}
 
 // Lane 0: hold back (bounded) while the K1 CTA on this SM occupies this warp's
 // sub-partition with its load or MMA warp and tasks remain.
@@ -50,7 +60,7 @@ template <bool kHeadStats, int kBatch>
 __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_constant__ NormRopeArgs p) {
   if (threadIdx.x == 0) atomicMin(&p.stamps[0], nrp::now_ns());
   const int lane = threadIdx.x & 31;
-  const long long tasks = nrp::task_count(p, kHeadGroup);
+  const long long tasks = nrp::task_count(p, p.head_group);
   if (p.claim && lane == 0) defer_while_busy(p, tasks);
   __syncwarp();
   // Read-once hand-off and write-once output: first out of L2, so the GEMM's
@@ -62,7 +72,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
     int ok = 1;
     if (lane == 0) {
       task = p.claim ? static_cast<long long>(atomicAdd(p.task_next, 1u)) : task + warps;
-      if (task < tasks) ok = nrp::wait_panel_ready(p.ready + nrp::task_panel(p, task, kHeadGroup), p.ready_target);
+      if (task < tasks) ok = nrp::wait_panel_ready(p.ready + nrp::task_panel(p, task, p.head_group), p.ready_target);
     }
     task = __shfl_sync(0xffffffffu, task, 0);
     if (task >= tasks) break;
@@ -71,7 +81,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
       if (lane == 0) atomicOr(p.status, kErrNormReadyWait);
       break;
     }
-    nrp::run_task<kHeadStats, kBatch>(p, task, kHeadGroup, once);
+    nrp::run_task<kHeadStats, kBatch>(p, task, p.head_group, once);
   }
   if (threadIdx.x == 0) atomicMax(&p.stamps[1], nrp::now_ns());
 }
@@ -81,8 +91,7 @@ __global__ void __launch_bounds__(kThreads) qk_norm_rope_kernel(const __grid_con
 cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms, bool overlap) {
   if (!a.norm && !a.rope) return cudaSuccess;
   if (a.d_head < 32 || a.d_head % 32 != 0) return cudaErrorInvalidValue;
-  const long long tasks = nrp::task_count(a, kHeadGroup);
-  if (tasks == 0) return cudaSuccess;
+  if (nrp::task_count(a, kHeadGroups[0]) == 0) return cudaSuccess;
   // Overlapped with the GEMM, the grid is kept to what fits beside each GEMM CTA
   // (registers are the limit) so every block finds its tasks as their panels
   // complete. That sizing only affects speed: the GEMM never waits for this kernel.
@@ -96,6 +105,9 @@ cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms,
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) == cudaSuccess && occ > per_sm)
       per_sm = occ;
   }
+  NormRopeArgs args = a;
+  args.head_group = head_group_for(a, static_cast<long long>(per_sm) * num_sms * (kThreads / 32));
+  const long long tasks = nrp::task_count(a, args.head_group);
   long long blocks = (tasks + kThreads / 32 - 1) / (kThreads / 32);
   if (blocks > static_cast<long long>(per_sm) * num_sms) blocks = static_cast<long long>(per_sm) * num_sms;
   cudaLaunchConfig_t cfg = {};
@@ -108,7 +120,6 @@ cudaError_t launch_norm_rope(const NormRopeArgs& a, cudaStream_t s, int num_sms,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap ? 1 : 0;
-  NormRopeArgs args = a;
   args.claim = overlap && a.head_kind == 0 ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, args);
 }

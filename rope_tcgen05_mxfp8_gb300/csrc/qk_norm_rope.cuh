@@ -255,7 +255,8 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
   const float inv_d = 1.0f / static_cast<float>(d);  // per-head norms
   float inv_q = 1.0f, inv_k = 1.0f;
   if (p.norm && !kHeadStats) {
-    inv_q = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr)] / static_cast<float>(p.n_q * d) + p.eps);
+    if (p.n_q > 0)
+      inv_q = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr)] / static_cast<float>(p.n_q * d) + p.eps);
     if (p.n_kv > 0)
       inv_k = 1.0f / sqrtf(p.sumsq[2 * static_cast<size_t>(tr) + 1] / static_cast<float>(p.n_kv * d) + p.eps);
   }
@@ -360,7 +361,7 @@ __device__ __forceinline__ void run_task(const NormRopeArgs& p, long long task, 
     }
   }
   if (!kHeadStats && c == 0 && grp == 0 && row_ok && p.norm && p.inv_rms != nullptr) {
-    p.inv_rms[2 * static_cast<size_t>(t)] = inv_q;
+    p.inv_rms[2 * static_cast<size_t>(t)] = p.n_q > 0 ? inv_q : 0.0f;
     p.inv_rms[2 * static_cast<size_t>(t) + 1] = p.n_kv > 0 ? inv_k : 0.0f;
   }
 }

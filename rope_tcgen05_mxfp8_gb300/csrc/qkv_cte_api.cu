@@ -191,7 +191,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   if (d.tokens > INT32_MAX) return fail(QKV_CTE_ERR_UNSUPPORTED, "tokens > INT32_MAX");
   if (d.hidden <= 0) return fail(QKV_CTE_ERR_INVALID, "hidden must be > 0");
   if (d.hidden % 128 != 0) return fail(QKV_CTE_ERR_UNSUPPORTED, "hidden %d is not a multiple of 128", d.hidden);
-  if (d.n_q_heads < 1) return fail(QKV_CTE_ERR_INVALID, "n_q_heads must be >= 1");
+  if (d.n_q_heads < 0) return fail(QKV_CTE_ERR_INVALID, "n_q_heads must be >= 0");
   if (d.n_kv_heads < 0) return fail(QKV_CTE_ERR_INVALID, "n_kv_heads must be >= 0");
   if (d.d_head <= 0) return fail(QKV_CTE_ERR_INVALID, "d_head must be > 0");
   if (d.d_head % 16 != 0) return fail(QKV_CTE_ERR_UNSUPPORTED, "d_head %d is not a multiple of 16", d.d_head);
@@ -199,6 +199,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
     if (d.n_kv_heads < 1) return fail(QKV_CTE_ERR_INVALID, "fused mode needs n_kv_heads >= 1");
   } else if (d.mode == QKV_CTE_MODE_SEPARATE) {
     if (d.n_kv_heads != 0) return fail(QKV_CTE_ERR_INVALID, "separate mode needs n_kv_heads == 0");
+    if (d.n_q_heads < 1) return fail(QKV_CTE_ERR_INVALID, "separate mode needs n_q_heads >= 1");
   } else {
     return fail(QKV_CTE_ERR_INVALID, "unknown mode %d", d.mode);
   }
@@ -359,11 +360,12 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   if (!produced && !a_scale) return fail(QKV_CTE_ERR_INVALID, "a_scale is required with separate FP8 rows");
   if (produced && a_scale)
     return fail(QKV_CTE_ERR_INVALID, "a_scale must be NULL with a packed or bf16 input (the scales come from it)");
-  if (d.norm && !gamma_q) return fail(QKV_CTE_ERR_INVALID, "norm needs gamma_q");
+  if (d.norm && d.n_q_heads > 0 && !gamma_q) return fail(QKV_CTE_ERR_INVALID, "norm with a Q segment needs gamma_q");
   if (d.norm && d.n_kv_heads > 0 && !gamma_k) return fail(QKV_CTE_ERR_INVALID, "norm with a K segment needs gamma_k");
   if (gamma_k && !(d.norm && d.n_kv_heads > 0))
     return fail(QKV_CTE_ERR_INVALID, "gamma_k given but the call has no normalised K segment");
-  if (gamma_q && !d.norm) return fail(QKV_CTE_ERR_INVALID, "gamma_q given but norm is off");
+  if (gamma_q && !(d.norm && d.n_q_heads > 0))
+    return fail(QKV_CTE_ERR_INVALID, "gamma_q given but the call has no normalised Q segment");
   if (inv_rms && per_head_norm(d))
     return fail(QKV_CTE_ERR_INVALID, "inv_rms is an output of the across-heads norm only (per-head norm: NULL)");
   if (d.rope && (!cos_table || !sin_table)) return fail(QKV_CTE_ERR_INVALID, "rope needs cos and sin tables");

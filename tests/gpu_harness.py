@@ -76,19 +76,24 @@ def check_outputs(call, inp, out, sumsq, inv, rows=None, name="case"):
                f"bad rows {len(np.unique(br))}, bad cols {len(np.unique(bc))} "
                f"(cols mod 128 {sorted(set((bc % 128).tolist()))[:8]}...)")
         raise AssertionError(msg + _diag(name, got, r, bad))
-    segs = [0] + ([1] if call.n_kv_heads > 0 else [])
+    # segments the call has (Q unless it is a K|V call, K unless it is a separate call);
+    # the columns of an absent segment must be exactly 0
+    segs = ([0] if call.n_q_heads > 0 else []) + ([1] if call.n_kv_heads > 0 else [])
+    absent = [c for c in (0, 1) if c not in segs]
     if sumsq is not None:
         s = sumsq.index_select(0, idx.to(sumsq.device)).cpu().double().numpy()
         for c in segs:
             rel = np.abs(s[:, c] - ref["sumsq"][:, c]) / np.maximum(np.abs(ref["sumsq"][:, c]), 1e-30)
             assert np.all(rel <= SS_REL), f"{name}: sumsq[{c}] max rel err {np.nanmax(rel):.3e}"
-        if call.n_kv_heads == 0:
-            assert np.all(s[:, 1] == 0), f"{name}: sumsq K column should be 0 without a K segment"
+        for c in absent:
+            assert np.all(s[:, c] == 0), f"{name}: sumsq column {c} should be 0 without that segment"
     if inv is not None and call.norm == 1:
         v = inv.index_select(0, idx.to(inv.device)).cpu().double().numpy()
         for c in segs:
             rel = np.abs(v[:, c] - ref["inv_rms"][:, c]) / np.abs(ref["inv_rms"][:, c])
             assert np.all(rel <= SS_REL), f"{name}: inv_rms[{c}] max rel err {np.nanmax(rel):.3e}"
+        for c in absent:
+            assert np.all(v[:, c] == 0), f"{name}: inv_rms column {c} should be 0 without that segment"
     return float(np.max(err)) if err.size else 0.0
 
 
@@ -105,7 +110,7 @@ def assert_same_to_rounding(call, a, b, name="runs"):
     rotation cancels."""
     assert a.shape == b.shape == (call.tokens, call.width)
     assert bool(torch.isfinite(a).all()) and bool(torch.isfinite(b).all()), f"{name}: non-finite output"
-    k_end = (call.n_q_heads + call.n_kv_heads) * call.d_head
+    k_end = (call.n_q_heads + call.n_kv_heads) * call.d_head  # the Q/K columns (and V after them)
     assert torch.equal(a[:, k_end:], b[:, k_end:]), f"{name}: V columns differ"
     fa, fb = a[:, :k_end].float(), b[:, :k_end].float()
     mag = torch.maximum(fa.abs(), fb.abs())

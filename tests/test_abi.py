@@ -68,7 +68,10 @@ def _plan_code(**kw):
     (dict(hidden=192), -2),
     (dict(d_head=0), -1),
     (dict(d_head=24), -2),
-    (dict(n_q_heads=0), -1),
+    (dict(n_q_heads=0), 0),                      # fused mode with no Q heads: a K|V call
+    (dict(n_q_heads=-1), -1),
+    (dict(n_q_heads=0, n_kv_heads=0, mode=1), -1),  # separate mode needs a Q segment
+    (dict(n_q_heads=0, n_kv_heads=0, mode=0), -1),
     (dict(n_kv_heads=-1), -1),
     (dict(n_kv_heads=0, mode=0), -1),
     (dict(n_kv_heads=2, mode=1), -1),

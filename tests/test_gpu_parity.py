@@ -5,6 +5,8 @@ and N tiles, with ragged tails); the full Wan shapes are compared on 4096 seeded
 sampled rows (rows are independent, so each sampled row is exact), in the same
 launch configuration the benchmark times.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -80,6 +82,50 @@ def test_cross_attention_calls():
     _case(q, rows=sampled_rows(q))
     _case(k)
     _case(v)
+
+
+@pytest.mark.parametrize("nbsd", [False, True])
+def test_cross_kv_call(nbsd):
+    """The cross-attention K and V projections of the 512 context tokens as one call (no
+    Q heads): every element against the oracle, BSD and NBSd."""
+    call = wl.workload("cross_kv")[0]
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, nbsd=nbsd)
+    op.status()
+    check_outputs(call, inp, out, ss, inv, name=f"cross_kv_{'nbsd' if nbsd else 'bsd'}")
+
+
+@pytest.mark.parametrize("T,rope", [(300, 0), (129, 1), (1, 0)])
+def test_kv_call_equals_separate_k_and_v_calls(T, rope):
+    """A K|V call against the oracle, and against the separate K call (normalised as its
+    only segment with gamma_k) and the separate plain V call on the same weights: V bit
+    for bit, K to rounding (its sums of squares are accumulated in a run-dependent order)."""
+    call = wl.custom_call(name=f"kv_{T}", tokens=T, hidden=1024, n_q_heads=0, n_kv_heads=3, d_head=128, norm=1,
+                          rope=rope, seed=71 + T, has_w_col_scale=True)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g)
+    op.status()
+    check_outputs(call, inp, out, ss, inv, name=call.name)
+    k = call.n_kv_heads * call.d_head
+    sep = wl.custom_call(name="sep", tokens=T, hidden=1024, n_q_heads=3, n_kv_heads=0, d_head=128, norm=1,
+                         rope=rope, seed=1)
+    gk = dict(g, W=g["W"][:k], w_sf=g["w_sf"][:k], bias=g["bias"][:k], w_col_scale=g["w_col_scale"][:k],
+              gamma_q=g["gamma_k"], gamma_k=None)
+    op_k, out_k, ss_k, _ = run_path(sep, gk)
+    op_k.status()
+    sep_v = dataclasses.replace(sep, norm=0, rope=0)
+    gv = dict(g, W=g["W"][k:], w_sf=g["w_sf"][k:], bias=g["bias"][k:], w_col_scale=g["w_col_scale"][k:],
+              gamma_q=None, gamma_k=None, cos=None, sin=None)
+    op_v, out_v, _, _ = run_path(sep_v, gv)
+    op_v.status()
+    assert torch.equal(out[:, k:], out_v), "V columns differ from the separate V call"
+    a, b = out[:, :k].float(), out_k.float()
+    mag = torch.maximum(a.abs(), b.abs())
+    tol = 2 ** -7 * mag + 2 ** -18 * mag.amax(dim=1, keepdim=True)
+    assert int(((a - b).abs() > tol).sum()) == 0, "K columns differ from the separate K call by more than rounding"
+    torch.testing.assert_close(ss[:, 1], ss_k[:, 0], rtol=1e-5, atol=0)
 
 
 def test_outputs_repeatable_on_side_stream():

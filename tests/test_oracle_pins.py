@@ -67,7 +67,7 @@ def _tiny_case(seed=0, T=3, H=96, nq=2, nkv=1, d=4, col_scale=True, distinct_hal
         w_sf=rng.integers(118, 136, size=(I, H // 32)).astype(np.uint8),
         w_col_scale=(rng.uniform(0.5, 2.0, size=I).astype(np.float32) if col_scale else None),
         bias=_rand_bf16_bits(rng, I, 0.0, 0.5),
-        gamma_q=_rand_bf16_bits(rng, nq * d, 1.0, 0.3),
+        gamma_q=_rand_bf16_bits(rng, nq * d, 1.0, 0.3) if nq else None,
         gamma_k=_rand_bf16_bits(rng, nkv * d, 1.0, 0.3) if nkv else None,
     )
     ang = rng.uniform(-math.pi, math.pi, size=(T, d))
@@ -109,14 +109,16 @@ def _brute_force(c, nq, nkv, d, norm, rope, eps):
             acc += Fraction(float(bias[i]))
             row.append(acc)
         o.append(row)
-    segs = [(0, nq * d, _torch_bf16(c["gamma_q"]), nq)]
+    segs = []
+    if nq:
+        segs.append((0, 0, nq * d, _torch_bf16(c["gamma_q"]), nq))
     if nkv:
-        segs.append((nq * d, (nq + nkv) * d, _torch_bf16(c["gamma_k"]), nkv))
+        segs.append((1, nq * d, (nq + nkv) * d, _torch_bf16(c["gamma_k"]), nkv))
     out = [[float(v) for v in row] for row in o]
     ss = [[0.0, 0.0] for _ in range(T)]
     inv = [[0.0, 0.0] for _ in range(T)]
     for t in range(T):
-        for s_idx, (lo, hi, gamma, nh) in enumerate(segs):
+        for s_idx, lo, hi, gamma, nh in segs:
             exact = sum((o[t][i] ** 2 for i in range(lo, hi)), Fraction(0))
             ss[t][s_idx] = float(exact)
             r = 1.0 / math.sqrt(float(exact / (nh * d)) + eps) if norm else 0.0
@@ -220,6 +222,38 @@ def pin_separate_bruteforce():
     _close(res["O"], out, what="separate O")
     _close(res["sumsq"], ss, what="separate sumsq")
     _close(res["inv_rms"], inv, what="separate inv")
+
+
+def pin_kv_call_bruteforce():
+    """A call with no Q heads (the K|V form): K normalised across its heads, V as projected."""
+    for seed, rope in ((13, 0), (14, 1)):
+        c, shape = _tiny_case(seed=seed, nq=0, nkv=2, d=4)
+        res = _run(c, shape, norm=1, rope=rope)
+        out, ss, inv = _brute_force(c, 0, 2, 4, 1, rope, 1e-6)
+        _close(res["O"], out, what=f"K|V O rope={rope}")
+        _close(res["sumsq"], ss, what="K|V sumsq")
+        _close(res["inv_rms"], inv, what="K|V inv")
+        assert np.all(res["sumsq"][:, 0] == 0) and np.all(res["inv_rms"][:, 0] == 0)
+
+
+def pin_kv_call_equals_separate_k_and_v_calls():
+    """The K|V call on W = [W_k; W_v] gives the separate K call (normalised as its only
+    segment, gamma_k as its gamma) on the K columns and the separate plain V call on the
+    V columns, as the cross-attention's three separate calls would."""
+    c, shape = _tiny_case(seed=15, T=3, H=64, nq=0, nkv=2, d=8)
+    kv = _run(c, shape, norm=1, rope=0)
+    k = 16
+    sep_k = dict(c, W=c["W"][:k], w_sf=c["w_sf"][:k], bias=c["bias"][:k], w_col_scale=c["w_col_scale"][:k],
+                 gamma_q=c["gamma_k"], gamma_k=None)
+    sep_v = dict(c, W=c["W"][k:], w_sf=c["w_sf"][k:], bias=c["bias"][k:], w_col_scale=c["w_col_scale"][k:],
+                 gamma_q=None, gamma_k=None)
+    one = dict(n_q_heads=2, n_kv_heads=0, d_head=8)
+    rk = _run(sep_k, one, norm=1, rope=0)
+    rv = _run(sep_v, one, norm=0, rope=0)
+    _close(kv["O"][:, :k], rk["O"], rel=1e-14, what="K|V vs separate K")
+    _close(kv["O"][:, k:], rv["O"], rel=0, what="K|V vs separate V")
+    _close(kv["inv_rms"][:, 1], rk["inv_rms"][:, 0], rel=1e-14, what="K|V inv vs separate K")
+    _close(kv["sumsq"][:, 1], rk["sumsq"][:, 0], rel=1e-14, what="K|V sumsq vs separate K")
 
 
 def pin_hand_example():
@@ -580,7 +614,8 @@ PINS = [pin_head_norm_vs_torch, pin_head_norm_invariants, pin_rope_interleaved_c
         pin_row_quantise_exact_power_of_two, pin_row_quantise_vs_torch_route, pin_packed_rows_layout, pin_e4m3_exhaustive, pin_e4m3_spec_values, pin_ue8m0_exhaustive, pin_bf16_exhaustive,
         pin_full_bruteforce, pin_separate_bruteforce, pin_hand_example, pin_norm_vs_torch_rms_norm,
         pin_rope_complex_closed_form, pin_unit_rms_invariant, pin_pair_norm_invariant,
-        pin_v_is_plain_projection, pin_separate_equals_fused_slice, pin_rows_subset]
+        pin_v_is_plain_projection, pin_separate_equals_fused_slice, pin_rows_subset,
+        pin_kv_call_bruteforce, pin_kv_call_equals_separate_k_and_v_calls]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)

@@ -82,6 +82,10 @@ WORKLOADS: Dict[str, List[Call]] = {
         Call("cross_v", 512, 5120, 40, 0, 128, norm=0, rope=0, rope_grid=None,
              outlier_frac=0.0, seed=300),
     ],
+    # the cross-attention K and V projections of the 512 context tokens as one call:
+    # no Q heads, W = [W_k; W_v], K normalised across heads, V as projected
+    "cross_kv": [Call("cross_kv", 512, 5120, 0, 40, 128, norm=1, rope=0, rope_grid=None,
+                      outlier_frac=0.0, seed=400)],
 }
 
 
@@ -216,8 +220,8 @@ def make_inputs(call: Call) -> Dict[str, Optional[torch.Tensor]]:
 
     Keys: A (uint8 [T,H] e4m3 codes), a_scale (float32 [T]), W (uint8 [I,H] e4m3
     codes, K-major), w_sf (uint8 [I,H/32] UE8M0), w_col_scale (float32 [I] or None),
-    bias (bfloat16 [I]), gamma_q (bfloat16 [n_q*d]), gamma_k (bfloat16 [n_kv*d] or
-    None), cos/sin (float32 [T,d] or None).
+    bias (bfloat16 [I]), gamma_q (bfloat16 [n_q*d], or None without Q heads), gamma_k
+    (bfloat16 [n_kv*d] or None), cos/sin (float32 [T,d] or None).
     """
     T, H, I, d = call.tokens, call.hidden, call.width, call.d_head
     s = call.seed
@@ -232,9 +236,11 @@ def make_inputs(call: Call) -> Dict[str, Optional[torch.Tensor]]:
     nq = call.n_q_heads * d
     nk = call.n_kv_heads * d
     if call.norm in (2, 3):  # per-head norms: one [d_head] gamma per segment
-        g = torch.cat([g[:d], g[nq:nq + d]])
-        nq, nk = d, (d if call.n_kv_heads > 0 else 0)
-    gamma_q = _bf16_bits(g[:nq])
+        gq = g[:d] if call.n_q_heads > 0 else g[:0]
+        gk = g[nq:nq + d] if call.n_kv_heads > 0 else g[:0]
+        g = torch.cat([gq, gk])
+        nq, nk = gq.numel(), gk.numel()
+    gamma_q = _bf16_bits(g[:nq]) if nq > 0 else None
     gamma_k = _bf16_bits(g[nq:nq + nk]) if nk > 0 else None
     w_col_scale = None
     if call.has_w_col_scale:
