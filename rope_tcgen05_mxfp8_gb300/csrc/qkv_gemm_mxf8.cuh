@@ -1017,23 +1017,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const int halves = g.k_stages - ks * C::KW < C::KW ? g.k_stages - ks * C::KW : C::KW;
           const uint32_t sf_smem = smem_u32(sSFB + stage * C::SFB_BYTES);
-          // the block scales of both K blocks first, then their eight MMAs back to back
-          for (int h = 0; h < halves; ++h) {
+          const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
+          const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
+          // The block scales of the stage's K blocks first, then their MMAs back to back,
+          // as straight-line code: the tensor pipe idles whenever the issue stream stalls.
+          if (g.k_stages - ks * C::KW >= C::KW) {
+#pragma unroll
+            for (int h = 0; h < C::KW; ++h)
+#pragma unroll
+              for (int c = 0; c < C::SF_CHUNKS; ++c)
+                tc_copy_32x128b_x4_pair(sfb_t + 4 * (h * C::SF_CHUNKS + c),
+                                        smem_desc_plain(sf_smem + h * C::SF_HALF + 512 * c));
+#pragma unroll
+            for (int h = 0; h < C::KW; ++h)
+#pragma unroll
+              for (int k = 0; k < kBK / 32; ++k)
+                mma_mxf8_pair(d_t, ad + (h * C::A_HALF >> 4) + 2 * k, bd + (h * C::B_HALF >> 4) + 2 * k,
+                              idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t + 4 * h * C::SF_CHUNKS,
+                              (ks | h | k) != 0 ? 1u : 0u);
+          } else {  // the last stage of an odd number of 128-byte K blocks: one block
 #pragma unroll
             for (int c = 0; c < C::SF_CHUNKS; ++c)
-              tc_copy_32x128b_x4_pair(sfb_t + 4 * (h * C::SF_CHUNKS + c),
-                                      smem_desc_plain(sf_smem + h * C::SF_HALF + 512 * c));
-          }
-          for (int h = 0; h < halves; ++h) {
-            const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES + h * C::A_HALF));
-            const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES + h * C::B_HALF));
-            const uint32_t sfb_h = sfb_t + static_cast<uint32_t>(4 * h * C::SF_CHUNKS);
+              tc_copy_32x128b_x4_pair(sfb_t + 4 * c, smem_desc_plain(sf_smem + 512 * c));
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k)
-              mma_mxf8_pair(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_h,
-                            (ks | h | k) != 0 ? 1u : 0u);
+              mma_mxf8_pair(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t,
+                            (ks | k) != 0 ? 1u : 0u);
           }
           // the stage is free once every CTA that wrote into it sees this pair done
           tc_commit_pair_multicast(smem_u32(&empty[stage]), static_cast<uint16_t>(0x3u << lead));
