@@ -50,6 +50,17 @@ def test_head_norm_ragged(T, norm, rope, form):
     _case(call, name=f"head_T{T}_n{norm}_r{rope}_{form}", form=form)
 
 
+@pytest.mark.parametrize("form", ["stats", "epilogue"])
+@pytest.mark.parametrize("norm,rope", [(RMS, 0), (LAYER, 1)])
+@pytest.mark.parametrize("T", [129, 300])
+def test_head_norm_kv_call(T, norm, rope, form):
+    """A K|V call (no Q heads) with a per-head norm: K normalised per head with its
+    [d_head] gamma, V as projected."""
+    call = wl.custom_call(name=f"head_kv{T}", tokens=T, hidden=512, n_q_heads=0, n_kv_heads=3, d_head=128,
+                          norm=norm, rope=rope, seed=61 + T + norm, has_w_col_scale=True)
+    _case(call, name=f"head_kv_T{T}_n{norm}_r{rope}_{form}", form=form)
+
+
 @pytest.mark.parametrize("norm,tile_n,form", [(RMS, 0, "epilogue"), (LAYER, 0, "epilogue"), (RMS, 128, "epilogue"),
                                              (LAYER, 256, "epilogue"), (RMS, 0, "stats"), (LAYER, 0, "stats"),
                                              (LAYER, 192, "stats"), (RMS, 128, "stats")])
