@@ -198,6 +198,11 @@ struct NormRopeArgs {
 // Supported N tiles (compile-time instantiations of K1).
 bool gemm_tile_supported(int tile_n);
 int gemm_sf_chunks(int tile_n);
+// Bytes of the repacked scales of one N tile for one 128-byte K block, and the row
+// size in which the scale tensor map addresses them (a box row holds at most 256
+// uint32).
+constexpr int kSfBlockBytesPerChunk = 2048;
+constexpr int kSfRowBytes = 1024;
 size_t gemm_smem_bytes(int tile_n);
 
 // Launchers. Each returns cudaSuccess or the launch error.
@@ -206,8 +211,8 @@ cudaError_t launch_prep(const GemmShape& g, const uint8_t* w_sf, uint8_t* sf_pac
                         unsigned long long* stamps,
                         uint32_t* task_next, float* zero_extra, size_t zero_extra_count, cudaStream_t s,
                         int num_sms, bool after_producer);
-// K1. tmSF: the repacked scales as a uint32 [n_tiles * k_stages, sf_chunks * 128] map
-// with one-row boxes (used by the CTA-pair kernel). With `fused` (CTA-pair form only)
+// K1. tmSF: the repacked scales as a uint32 map of kSfRowBytes-byte rows, one K block's
+// image (sf_chunks * 2048 bytes) per box (used by the CTA-pair kernel). With `fused` (CTA-pair form only)
 // the epilogue warps also run the norm/RoPE tasks of `*fused` between tiles, and no
 // separate pass is launched.
 cudaError_t launch_gemm(const GemmShape& g, const CUtensorMap& tmA, const CUtensorMap& tmW,

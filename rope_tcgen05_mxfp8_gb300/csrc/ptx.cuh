@@ -190,6 +190,28 @@ __device__ __forceinline__ void tc_copy_32x128b_x4(uint32_t taddr, uint64_t s_de
   asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
+// A matrix of 8-row x 16-byte core matrices without swizzle: `lbo` bytes from one core
+// matrix to the next along a row (the leading byte offset), `sbo` bytes from one group
+// of 8 rows to the next (the stride byte offset).
+__device__ __forceinline__ uint64_t smem_desc_plain_lbo_sbo(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// 128 rows of 256 (or 128) bits into 128 TMEM lanes: row r to lane r, 8 (or 4)
+// consecutive 32-bit columns.
+__device__ __forceinline__ void tc_copy_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+__device__ __forceinline__ void tc_copy_128x128b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
   asm volatile(
@@ -321,6 +343,14 @@ __device__ __forceinline__ void mma_mxf8_pair(uint32_t d_tmem, uint64_t a_desc, 
 
 __device__ __forceinline__ void tc_copy_32x128b_x4_pair(uint32_t taddr, uint64_t s_desc) {
   asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+__device__ __forceinline__ void tc_copy_128x256b_pair(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
+__device__ __forceinline__ void tc_copy_128x128b_pair(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
 
 // Arrive once on the mbarrier at this offset in every CTA of `cta_mask` when the

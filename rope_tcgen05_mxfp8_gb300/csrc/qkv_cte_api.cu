@@ -117,15 +117,16 @@ int encode_operand(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
   return QKV_CTE_OK;
 }
 
-// The repacked scales as uint32 [n_tiles * k_stages rows, sf_chunks * 128 words]:
-// one row (one N tile's scales for one K stage) per TMA box.
+// The repacked scales as uint32 rows of kSfRowBytes: one N tile's image for one
+// 128-byte K block (sf_chunks * kSfBlockBytesPerChunk bytes, whole rows) per TMA box.
 int encode_scales(CUtensorMap* m, void* base, const GemmShape& g) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return fail(QKV_CTE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
-  const cuuint32_t words = (cuuint32_t)g.sf_chunks * 128u;
-  cuuint64_t dims[2] = {words, (cuuint64_t)g.n_tiles * (cuuint64_t)g.k_stages};
-  cuuint64_t strides[1] = {(cuuint64_t)words * 4u};
-  cuuint32_t box[2] = {words, 1u};
+  const cuuint32_t words = kSfRowBytes / 4;
+  const cuuint32_t rows_per_block = (cuuint32_t)(g.sf_chunks * kSfBlockBytesPerChunk / kSfRowBytes);
+  cuuint64_t dims[2] = {words, (cuuint64_t)g.n_tiles * (cuuint64_t)g.k_stages * rows_per_block};
+  cuuint64_t strides[1] = {(cuuint64_t)kSfRowBytes};
+  cuuint32_t box[2] = {words, rows_per_block};
   cuuint32_t estr[2] = {1u, 1u};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -272,7 +273,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   w.status_off = 0;
   w.sumsq_off = 256;
   w.sf_off = w.sumsq_off + align_up((size_t)g.T * 2 * sizeof(float), 256);
-  w.ready_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * 512, 256);
+  w.ready_off = w.sf_off + align_up((size_t)g.n_tiles * g.k_stages * g.sf_chunks * kSfBlockBytesPerChunk, 256);
   w.sm_busy_off = w.ready_off + align_up((size_t)g.blocks128 * sizeof(uint32_t), 256);
   w.qk_off = w.sm_busy_off + align_up((size_t)kSmTable * sizeof(uint32_t), 256);
   const size_t hand_rows = second_pass ? (size_t)g.blocks128 * 128 : 0;

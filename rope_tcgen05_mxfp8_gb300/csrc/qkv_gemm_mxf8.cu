@@ -8,12 +8,12 @@ namespace qkvcte {
 
 namespace {
 
-// Repack W's UE8M0 scales [I, H/32] into, per (N tile, K stage), SF_CHUNKS blocks of
-// 512 bytes: byte 16*r + 4*c + kb of block `chunk` is the scale of output column
-// n = tile*tile_n + 128*chunk + 32*c + r for K block 4*stage + kb. That is the
-// 32-row x 16-byte shared-memory image tcgen05.cp 32x128b.warpx4 turns into the
-// TMEM scale-factor layout of an M=128 block-scaled MMA. Columns past I (or past
-// the tile) get 127.
+// Repack W's UE8M0 scales [I, H/32] into, per (N tile, 128-byte K block), the image
+// one tcgen05.cp turns into the TMEM scale-factor layout of an M=128 block-scaled MMA
+// (sf_chunks * 2048 bytes; qkv_gemm_mxf8.cuh describes it): byte kb of word c of
+// image row l = 32*q + r, chunk j is the scale of output column
+// n = tile*tile_n + 128*j + 32*c + r for K element group 4*block + kb, for each of the
+// four lane quarters q. Columns past I (or past the tile) get 127.
 //
 // The first n_tiles * stage_groups blocks each repack one N tile for up to
 // kPrepStages K stages: they read the tile's rows of w_sf (consecutive threads,
@@ -46,13 +46,15 @@ __global__ void __launch_bounds__(kPrepThreads) qkv_prep_kernel(
 #pragma unroll
     for (int k = 0; k < kPrepStages; ++k) rows[i][k] = (live && k < n_st) ? __ldg(src + k) : 0x7F7F7F7Fu;
     __syncthreads();
-    const int per_stage = sf_chunks * 128;
+    const int per_stage = sf_chunks * (kSfBlockBytesPerChunk / 4);
     uint32_t* dst = packed + (static_cast<size_t>(nt) * k_stages + kst0) * per_stage;
     for (int w = threadIdx.x; w < n_st * per_stage; w += kPrepThreads) {
       const int ks = w / per_stage;
       const int rem = w - ks * per_stage;
-      const int within = rem & 127;
-      const int n_local = (rem >> 7) * 128 + (within & 3) * 32 + (within >> 2);
+      const int core = rem >> 5;              // 8-row x 16-byte core matrix: (group, chunk)
+      const int chunk = core % sf_chunks;
+      const int lane = (core / sf_chunks) * 8 + ((rem >> 2) & 7);
+      const int n_local = chunk * 128 + (rem & 3) * 32 + (lane & 31);
       dst[w] = n_local < 256 ? rows[n_local][ks] : 0x7F7F7F7Fu;
     }
   }

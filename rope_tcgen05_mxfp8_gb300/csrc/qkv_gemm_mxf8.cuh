@@ -57,12 +57,39 @@ constexpr int kThreads = 192;  // producer warp, MMA warp, 4 epilogue warps
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint32_t kFlagTestStall = 0x1u;
 
+// W's block scales for one 128-byte K block as the GEMM copies them into TMEM: 128 rows
+// (TMEM lanes) x 16 bytes (4 columns) per 128-column chunk of the N tile, lane q*32 + r,
+// column c holding the four K-scales of tile column 128*chunk + 32*c + r (the scale
+// layout of an M = 128 block-scaled MMA, which wants the same 32 rows in each lane
+// quarter, so the image holds them four times). Stored as 8-row x 16-byte core
+// matrices, the chunks of one 8-row group side by side: core matrix (group g, chunk j)
+// at byte 128 * (g * SF_CHUNKS + j). Every read of a descriptor over this image stays
+// inside it whichever way its two offsets are taken.
+static_assert(kSfBlockBytesPerChunk == 128 * 16, "128 lanes x 4 scale columns per chunk");
+
+// One tcgen05.cp of one K block's scales (the image above) into TMEM columns
+// taddr + 4 * chunk. One copy per K block rather than one quarter-replicating copy per
+// chunk: with 256-byte K stages, four 32x128b.warpx4 copies after each full-barrier
+// wait cost about a tenth of the tensor pipe's time; two 128x256b copies cost nothing
+// measurable.
+template <int SF_CHUNKS, bool kPair>
+__device__ __forceinline__ void copy_block_scales(uint32_t taddr, uint32_t sf_smem) {
+  static_assert(SF_CHUNKS == 1 || SF_CHUNKS == 2, "one or two 128-column chunks");
+  if constexpr (SF_CHUNKS == 2) {
+    const uint64_t d = smem_desc_plain_lbo_sbo(sf_smem, 128, 256);
+    if constexpr (kPair) tc_copy_128x256b_pair(taddr, d); else tc_copy_128x256b(taddr, d);
+  } else {
+    const uint64_t d = smem_desc_plain_lbo_sbo(sf_smem, 128, 128);
+    if constexpr (kPair) tc_copy_128x128b_pair(taddr, d); else tc_copy_128x128b(taddr, d);
+  }
+}
+
 template <int BN>
 struct K1Cfg {
   static constexpr int SF_CHUNKS = (BN + 127) / 128;
   static constexpr int A_BYTES = kBM * kBK;
   static constexpr int B_BYTES = BN * kBK;
-  static constexpr int SFB_BYTES = SF_CHUNKS * 512;
+  static constexpr int SFB_BYTES = SF_CHUNKS * kSfBlockBytesPerChunk;
   static constexpr int SFB_COLS = SF_CHUNKS * 4;
   static constexpr int ACC_STAGES = (2 * BN + 4 + SFB_COLS <= 512) ? 2 : 1;
   static constexpr int SFA_COL = ACC_STAGES * BN;
@@ -632,10 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sf_smem = smem_u32(sSFB + stage * C::SFB_BYTES);
-#pragma unroll
-          for (int c = 0; c < C::SF_CHUNKS; ++c)
-            tc_copy_32x128b_x4(sfb_t + 4 * c, smem_desc_plain(sf_smem + 512 * c));
+          copy_block_scales<C::SF_CHUNKS, false>(sfb_t, smem_u32(sSFB + stage * C::SFB_BYTES));
           const uint64_t ad = smem_desc_sw128(smem_u32(sA + stage * C::A_BYTES));
           const uint64_t bd = smem_desc_sw128(smem_u32(sB + stage * C::B_BYTES));
 #pragma unroll
@@ -740,7 +764,7 @@ struct K1PairCfg {
   static constexpr int KW = 2;                           // 128-byte K blocks per stage
   static constexpr int A_HALF = kBM * kBK;               // one 128-byte K block of A
   static constexpr int B_HALF = HALF_N * kBK;            // ... of this CTA's half of W
-  static constexpr int SF_HALF = SF_CHUNKS * 512;        // ... of the tile's scales
+  static constexpr int SF_HALF = SF_CHUNKS * kSfBlockBytesPerChunk;  // ... of the tile's scales
   static constexpr int A_BYTES = KW * A_HALF;
   static constexpr int B_BYTES = KW * B_HALF;
   static constexpr int SFB_BYTES = KW * SF_HALF;
@@ -960,7 +984,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d_pair(smem_u32(sB + stage * C::B_BYTES + h * C::B_HALF), &tmW, kb * kBK,
                              n_blk * BN + static_cast<int>(rank) * C::HALF_N, fb, pol_keep);
             tma_load_2d_pair(smem_u32(sSFB + stage * C::SFB_BYTES + h * C::SF_HALF), &tmSF, 0,
-                             n_blk * g.k_stages + kb, fb, pol_keep);
+                             (n_blk * g.k_stages + kb) * (C::SF_HALF / kSfRowBytes), fb, pol_keep);
           }
           ++issued;
           if (++stage == C::STAGES) {
@@ -1025,10 +1049,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g.k_stages - ks * C::KW >= C::KW) {
 #pragma unroll
             for (int h = 0; h < C::KW; ++h)
-#pragma unroll
-              for (int c = 0; c < C::SF_CHUNKS; ++c)
-                tc_copy_32x128b_x4_pair(sfb_t + 4 * (h * C::SF_CHUNKS + c),
-                                        smem_desc_plain(sf_smem + h * C::SF_HALF + 512 * c));
+              copy_block_scales<C::SF_CHUNKS, true>(sfb_t + 4 * h * C::SF_CHUNKS, sf_smem + h * C::SF_HALF);
 #pragma unroll
             for (int h = 0; h < C::KW; ++h)
 #pragma unroll
@@ -1037,9 +1058,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                               idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t + 4 * h * C::SF_CHUNKS,
                               (ks | h | k) != 0 ? 1u : 0u);
           } else {  // the last stage of an odd number of 128-byte K blocks: one block
-#pragma unroll
-            for (int c = 0; c < C::SF_CHUNKS; ++c)
-              tc_copy_32x128b_x4_pair(sfb_t + 4 * c, smem_desc_plain(sf_smem + 512 * c));
+            copy_block_scales<C::SF_CHUNKS, true>(sfb_t, sf_smem);
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k)
               mma_mxf8_pair(d_t, ad + 2 * k, bd + 2 * k, idesc_with_sf_id(idesc, 0, k), sfa_t, sfb_t,

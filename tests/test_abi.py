@@ -207,7 +207,7 @@ def test_workspace_size_formula(input_layout):
         q.qkv_cte_destroy(plan)
         I = (nq + 2 * nkv) * 128
         n_tiles = -(-I // tile)
-        sf = n_tiles * (5120 // 128) * (-(-tile // 128)) * 512
+        sf = n_tiles * (5120 // 128) * (-(-tile // 128)) * 2048  # 4 lane-quarter copies of 512 B
         ss = -(-(T * 8) // 256) * 256
         rows = -(-T // 128) * 128
         kq = (nq + nkv) * 128
