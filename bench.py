@@ -438,6 +438,40 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = per_s / 1e12
 
+    # Side measurement (outside the timed region, before the sustained leg so that both
+    # forms see the clocks of a short run): the same step with the two passes serialised,
+    # alternating with the overlapped step. The serialised runs time the norm/RoPE pass on
+    # its own (its bandwidth roofline) and the GEMM alone; the pairs give the overlapped
+    # step's cost against the GEMM alone under the same conditions.
+    serial = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
+                    rope=call.rope, eps=call.eps, tile_n=args.tile_n,
+                    flags=QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES | gemm_flag, device=dev,
+                    output_layout=layout, input_layout=input_layout)
+    ser, ovl = [], []
+    for i in range(max(3, min(args.steps, 10))):
+        if not args.no_flush:
+            flush.zero_()
+        serial(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], gq, gk, g["cos"],
+               g["sin"], out=out, sumsq=sumsq, stream=stream)
+        ser.append(serial.pass_times())
+        if not args.no_flush:
+            flush.zero_()
+        step()
+        ovl.append(op.pass_times())
+    serial.status(stream)
+    op.status(stream)
+    serial.close()
+    norm_ms = statistics.mean(p[2] for p in ser[1:])
+    serial_gemm_ms = statistics.mean(p[1] for p in ser[1:])
+    serial_run_ms = statistics.mean(p[3] for p in ser[1:])
+    ovl_gemm_ms = statistics.mean(p[1] for p in ovl[1:])
+    ovl_run_ms = statistics.mean(p[3] for p in ovl[1:])
+    drag = {"gemm_alone_ms": serial_gemm_ms, "gemm_in_step_ms": ovl_gemm_ms, "step_ms": ovl_run_ms,
+            "step_over_gemm_alone": ovl_run_ms / serial_gemm_ms,
+            "gemm_in_step_over_alone": ovl_gemm_ms / serial_gemm_ms, "pairs": len(ser) - 1,
+            "how": "alternating serialised and overlapped steps (L2 flushed before each); GEMM spans from the "
+                   "kernels' %globaltimer stamps, the step from CUDA events around prep + GEMM + norm/RoPE"}
+
     # Sustained leg: back-to-back steps for at least --sustained-s seconds (L2 flushed
     # between steps as above), with their own clock record, so that the power cap the
     # short timed region may not reach is in the number.
@@ -481,24 +515,6 @@ def run_ours(args):
     norm_span_ms = statistics.mean(p[2] for p in passes)
     run_ms = statistics.mean(p[3] for p in passes)
 
-    # Side measurement (outside the timed region): the same step with the two passes
-    # serialised, to time the norm/RoPE pass on its own for its bandwidth roofline.
-    serial = QkvCte(call.tokens, call.hidden, call.n_q_heads, call.n_kv_heads, call.d_head, norm=call.norm,
-                    rope=call.rope, eps=call.eps, tile_n=args.tile_n,
-                    flags=QKV_CTE_FLAG_PROFILE | QKV_CTE_FLAG_SERIAL_PASSES | gemm_flag, device=dev,
-                    output_layout=layout, input_layout=input_layout)
-    ser = []
-    for i in range(max(3, min(args.steps, 10))):
-        if not args.no_flush:
-            flush.zero_()
-        serial(a_in, a_scale_in, g["W"], g["w_sf"], g["bias"], gq, gk, g["cos"],
-               g["sin"], out=out, sumsq=sumsq, stream=stream)
-        ser.append(serial.pass_times())
-    serial.status(stream)
-    serial.close()
-    norm_ms = statistics.mean(p[2] for p in ser[1:])
-    serial_gemm_ms = statistics.mean(p[1] for p in ser[1:])
-    serial_run_ms = statistics.mean(p[3] for p in ser[1:])
     hbm_gbs, bf16, bf16_sus, peak_src = _peaks()
     # The tensor-peak denominator: the burst figure, or the sustained one when the power
     # cap was active during the timed steps (the kernel then ran at the clocks a long
@@ -596,6 +612,7 @@ def run_ours(args):
         "passes_ms": {"prep": prep_ms, "gemm_epilogue": gemm_ms, "norm_rope_span": norm_span_ms,
                       "run": run_ms, "exposed_after_gemm": run_ms - prep_ms - gemm_ms,
                       "serial": {"gemm_epilogue": serial_gemm_ms, "norm_rope": norm_ms, "run": serial_run_ms},
+                      "overlap_vs_gemm_alone": drag,
                       "how": "prep and run: CUDA events on the launching stream; gemm_epilogue and "
                              "norm_rope: first-block start to last-block end from %globaltimer stamps "
                              "written by the kernels. In the timed steps the norm/RoPE pass overlaps the "
