@@ -835,6 +835,14 @@ __device__ __forceinline__ bool fused_try(const NormRopeArgs& nr, FusedWork& w, 
   return true;
 }
 
+// Lane 0's value of `v`, for a decision the whole warp takes together: the task
+// helpers use full-warp shuffles, so no lane may leave a loop the others stay in (a
+// lane that read the abort flag before lane 0 had set it would otherwise wait in a
+// shuffle for lanes that have left).
+__device__ __forceinline__ bool warp_uniform(bool v) {
+  return __shfl_sync(0xffffffffu, v ? 1 : 0, 0) != 0;
+}
+
 // Wait (bounded) for the accumulator barrier, running norm tasks meanwhile.
 __device__ __forceinline__ bool fused_wait_acc(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                                const NormRopeArgs& nr, long long n_tasks, FusedWork& w,
@@ -845,14 +853,14 @@ __device__ __forceinline__ bool fused_wait_acc(uint32_t bar, uint32_t parity, vo
     if ((threadIdx.x & 31) == 0) ready = mbar_test_wait(bar, parity) ? 1 : 0;
     ready = __shfl_sync(0xffffffffu, ready, 0);
     if (ready) return mbar_wait_bounded(bar, parity, abort_flag, kWaitLimitNs);  // completes at once, per lane
-    if (*abort_flag) return false;
+    if (warp_uniform(*abort_flag != 0)) return false;
     bool ran = false;
     if (!w.done) {
       if (w.pending < 0) fused_claim(nr, n_tasks, w);
       if (w.pending >= 0) ran = fused_try(nr, w, once);
     }
     if (!ran) {
-      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (warp_uniform(globaltimer_ns() - t0 > kWaitLimitNs)) return false;
       __nanosleep(64);
     }
   }
@@ -862,7 +870,7 @@ __device__ __forceinline__ bool fused_wait_acc(uint32_t bar, uint32_t parity, vo
 __device__ __forceinline__ void fused_finish(const NormRopeArgs& nr, long long n_tasks, FusedWork& w,
                                              volatile int* abort_flag, uint32_t* status, uint64_t once) {
   uint64_t t0 = globaltimer_ns();
-  while (!w.done && !*abort_flag) {
+  while (!w.done && !warp_uniform(*abort_flag != 0)) {
     if (w.pending < 0) {
       fused_claim(nr, n_tasks, w);
       if (w.done) break;
@@ -871,7 +879,7 @@ __device__ __forceinline__ void fused_finish(const NormRopeArgs& nr, long long n
       t0 = globaltimer_ns();
       continue;
     }
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (warp_uniform(globaltimer_ns() - t0 > kWaitLimitNs)) {
       if ((threadIdx.x & 31) == 0) atomicOr(status, kErrNormReadyWait);
       break;
     }
