@@ -46,16 +46,23 @@ __global__ void __launch_bounds__(kPrepThreads) qkv_prep_kernel(
 #pragma unroll
     for (int k = 0; k < kPrepStages; ++k) rows[i][k] = (live && k < n_st) ? __ldg(src + k) : 0x7F7F7F7Fu;
     __syncthreads();
-    const int per_stage = sf_chunks * (kSfBlockBytesPerChunk / 4);
-    uint32_t* dst = packed + (static_cast<size_t>(nt) * k_stages + kst0) * per_stage;
-    for (int w = threadIdx.x; w < n_st * per_stage; w += kPrepThreads) {
-      const int ks = w / per_stage;
-      const int rem = w - ks * per_stage;
-      const int core = rem >> 5;              // 8-row x 16-byte core matrix: (group, chunk)
+    // The image's four lane quarters are the same 32-row block (sf_chunks * 512 bytes):
+    // each thread builds one 16-byte row of a core matrix of that block and stores it
+    // four times.
+    const int per_stage = sf_chunks * (kSfBlockBytesPerChunk / 4);  // words per K block
+    const int quarter16 = per_stage / 16;                          // 16-byte rows per lane quarter
+    uint4* dst = reinterpret_cast<uint4*>(packed + (static_cast<size_t>(nt) * k_stages + kst0) * per_stage);
+    for (int v = threadIdx.x; v < n_st * quarter16; v += kPrepThreads) {
+      const int ks = v / quarter16;
+      const int row16 = v - ks * quarter16;
+      const int core = row16 >> 3;  // 8-row x 16-byte core matrix: (row group, chunk)
       const int chunk = core % sf_chunks;
-      const int lane = (core / sf_chunks) * 8 + ((rem >> 2) & 7);
-      const int n_local = chunk * 128 + (rem & 3) * 32 + (lane & 31);
-      dst[w] = n_local < 256 ? rows[n_local][ks] : 0x7F7F7F7Fu;
+      const int lane = (core / sf_chunks) * 8 + (row16 & 7);  // TMEM lane within the quarter
+      const int n0 = chunk * 128 + lane;                      // word c holds column n0 + 32 c
+      const uint4 q = make_uint4(rows[n0][ks], rows[n0 + 32][ks], rows[n0 + 64][ks], rows[n0 + 96][ks]);
+      uint4* d = dst + static_cast<size_t>(ks) * (per_stage / 4) + row16;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) d[r * quarter16] = q;
     }
   }
   const size_t stride = static_cast<size_t>(gridDim.x) * blockDim.x;
