@@ -744,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // memory and the scale-factor copies per FLOP.
 // ---------------------------------------------------------------------------
 // Stage depth. A ring stage holds two 128-byte K blocks (K = 256 per stage: eight MMAs
-// and one scale-factor copy group per barrier wait). The tensor pipe runs the MMAs of
+// and two scale-factor copies per barrier wait). The tensor pipe runs the MMAs of
 // a continuously fed issue stream at the full rate, but every stage boundary (the
 // wait for the stage's operands and the copy of its block scales into TMEM, which is
 // ordered against the MMAs in flight) opens a bubble. Measured on GB300 with the
@@ -753,7 +753,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // boundaries at all), so the boundaries are made half as frequent. A K length that
 // is an odd number of 128-byte blocks ends on a half stage.
 //
-// Ring depth: as many stages as fit (three at tile_n 192 to 256: 192 KB). Measured at
+// Ring depth: as many stages as fit (three at tile_n 192 to 256: 192 to 216 KB). Measured at
 // the Wan 480p shape with the norm/RoPE pass overlapped: 1.616 ms per step with three
 // 256-byte stages against 2.094 ms with two (which left more L1 for the pass beside
 // the GEMM, but cannot cover the load latency).
