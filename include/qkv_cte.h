@@ -301,9 +301,9 @@ int qkv_cte_run_host(qkv_cte_plan_t plan, const void* A_host, const float* a_sca
  * empty problem). Host only (creates the per-chunk plans). Returns 0 or -1/-2. */
 int qkv_cte_host_scratch_bytes(qkv_cte_plan_t plan, int32_t chunk_rows, size_t* bytes);
 
-/* Size of the scratch array behind qkv_cte_run_noalloc: 16 MiB on every GPU that
+/* Size of the scratch array behind qkv_cte_run_noalloc: 24 MiB on every GPU that
  * loads the library, held until the process exits. */
-#define QKV_CTE_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define QKV_CTE_NOALLOC_SCRATCH_BYTES (24u << 20)
 
 /* qkv_cte_run without a workspace, for callers that cannot allocate device memory
  * when they run the projection (a server that forbids allocation after start-up, a

@@ -44,7 +44,7 @@ EXPORTED = ("qkv_cte_plan", "qkv_cte_run", "qkv_cte_status", "qkv_cte_pass_times
             "qkv_cte_last_error", "qkv_cte_version", "qkv_cte_run_noalloc", "qkv_cte_get_plan_info",
             "qkv_cte_row_quantize", "qkv_cte_unpack_rows", "qkv_cte_interleaved_to_rotate_half",
             "qkv_cte_run_host", "qkv_cte_host_scratch_bytes", "qkv_cte_noalloc_status")
-QKV_CTE_NOALLOC_SCRATCH_BYTES = 16 << 20
+QKV_CTE_NOALLOC_SCRATCH_BYTES = 24 << 20
 
 
 class qkv_cte_desc(ctypes.Structure):

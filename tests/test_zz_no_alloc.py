@@ -147,3 +147,13 @@ def test_noalloc_refuses_a_problem_larger_than_its_scratch():
         assert "scratch" in msg and str(q.QKV_CTE_NOALLOC_SCRATCH_BYTES) in msg
     finally:
         q.qkv_cte_destroy(plan)
+
+
+def test_noalloc_scratch_holds_the_documented_problems():
+    """The header promises that 640 tokens of the fused Wan layout and the 512-token
+    cross-attention K, V and K|V calls fit the fixed array (planning only, no GPU)."""
+    cases = [(640, 40, 40, 1), (512, 40, 0, 0), (512, 0, 40, 0)]
+    for tokens, nq, nkv, rope in cases:
+        plan, ws_bytes = q.qkv_cte_plan(q.make_desc(tokens, 5120, nq, nkv, 128, rope=rope))
+        q.qkv_cte_destroy(plan)
+        assert ws_bytes <= q.QKV_CTE_NOALLOC_SCRATCH_BYTES, (tokens, nq, nkv, ws_bytes)
