@@ -75,10 +75,11 @@ struct GemmShape {
   int m_tiles, n_tiles, k_stages;
   int sf_chunks;    // 128-column scale-factor chunks per N tile
   int n_qk_tiles;   // N tiles holding at least one Q or K column: [0, n_qk_tiles)
-  int n_bands;
-  int band_n0[kMaxBands];          // first N tile of each band
-  int band_nc[kMaxBands];          // N tiles in each band
-  int band_tile0[kMaxBands + 1];   // linear index of each band's first tile
+  int n_bands;                     // segments: a band's N tiles over a range of row panels
+  int band_n0[kMaxBands];          // first N tile of each segment
+  int band_nc[kMaxBands];          // N tiles in each segment
+  int band_m0[kMaxBands];          // first row panel (m) of each segment
+  int band_tile0[kMaxBands + 1];   // linear index of each segment's first tile
 };
 
 // (m, n) of linear tile `tile` in the banded order.
@@ -87,12 +88,16 @@ __host__ __device__ inline void tile_coords(const GemmShape& g, int tile, int& m
   while (b + 1 < g.n_bands && tile >= g.band_tile0[b + 1]) ++b;
   const int local = tile - g.band_tile0[b];
   const int nc = g.band_nc[b];
-  m = local / nc;
-  n = g.band_n0[b] + (local - m * nc);
+  const int ml = local / nc;
+  m = g.band_m0[b] + ml;
+  n = g.band_n0[b] + (local - ml * nc);
 }
 
-// Cut [0, n_tiles) into bands of at most `band_tiles` N tiles, Q/K tiles first.
-inline void make_bands(GemmShape& g, int band_tiles) {
+// Cut [0, n_tiles) into bands of at most `band_tiles` N tiles, Q/K tiles first. With
+// m_chunks > 1 the Q/K bands take turns over m_chunks ranges of row panels (every Q/K
+// band over the first range, then over the next, ...), so row panels complete from
+// early on; the V bands follow over all row panels.
+inline void make_bands(GemmShape& g, int band_tiles, int m_chunks = 1) {
   if (band_tiles < 1) band_tiles = 1;
   const int qk_run = g.n_qk_tiles;
   const int runs[2][2] = {{0, qk_run}, {qk_run, g.n_tiles - qk_run}};
@@ -103,18 +108,28 @@ inline void make_bands(GemmShape& g, int band_tiles) {
     need = 0;
     for (const auto& r : runs) need += (r[1] + band_tiles - 1) / band_tiles;
   }
+  const int qk_bands = (qk_run + band_tiles - 1) / band_tiles;
+  if (m_chunks > g.m_tiles) m_chunks = g.m_tiles;
+  while (m_chunks > 1 && need - qk_bands + qk_bands * m_chunks > kMaxBands) --m_chunks;
+  if (m_chunks < 1 || qk_bands == 0) m_chunks = 1;
+  const int per_chunk = (g.m_tiles + m_chunks - 1) / m_chunks;
   g.n_bands = 0;
   int tile0 = 0;
-  for (const auto& r : runs) {
-    for (int n0 = r[0]; n0 < r[0] + r[1]; n0 += band_tiles) {
-      const int nc = (r[0] + r[1] - n0) < band_tiles ? (r[0] + r[1] - n0) : band_tiles;
-      g.band_n0[g.n_bands] = n0;
-      g.band_nc[g.n_bands] = nc;
-      g.band_tile0[g.n_bands] = tile0;
-      tile0 += nc * g.m_tiles;
-      ++g.n_bands;
-    }
+  auto add = [&](int n0, int nc, int m0, int mc) {
+    if (nc <= 0 || mc <= 0) return;
+    g.band_n0[g.n_bands] = n0;
+    g.band_nc[g.n_bands] = nc;
+    g.band_m0[g.n_bands] = m0;
+    g.band_tile0[g.n_bands] = tile0;
+    tile0 += nc * mc;
+    ++g.n_bands;
+  };
+  for (int m0 = 0; m0 < g.m_tiles; m0 += per_chunk) {
+    const int mc = g.m_tiles - m0 < per_chunk ? g.m_tiles - m0 : per_chunk;
+    for (int n0 = 0; n0 < qk_run; n0 += band_tiles) add(n0, qk_run - n0 < band_tiles ? qk_run - n0 : band_tiles, m0, mc);
   }
+  for (int n0 = qk_run; n0 < g.n_tiles; n0 += band_tiles)
+    add(n0, g.n_tiles - n0 < band_tiles ? g.n_tiles - n0 : band_tiles, 0, g.m_tiles);
   g.band_tile0[g.n_bands] = tile0;
 }
 

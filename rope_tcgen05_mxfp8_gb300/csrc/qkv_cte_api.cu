@@ -149,6 +149,17 @@ int band_tiles(const GemmShape& g) {
   return n < 1 ? 1 : n;
 }
 
+// Row-panel ranges the Q/K bands take turns over (1: each Q/K band over all panels).
+// QKV_CTE_M_CHUNKS overrides it (for tuning sweeps).
+int band_m_chunks() {
+  int c = 1;
+  if (const char* e = getenv("QKV_CTE_M_CHUNKS")) {
+    const int v = atoi(e);
+    if (v > 0) c = v;
+  }
+  return c;
+}
+
 bool per_head_norm(const qkv_cte_desc& d) {
   return d.norm == QKV_CTE_NORM_HEAD_RMS || d.norm == QKV_CTE_NORM_HEAD_LAYER;
 }
@@ -268,7 +279,7 @@ int qkv_cte_plan(qkv_cte_plan_t* out, const qkv_cte_desc* desc, size_t* workspac
   p->second_pass = second_pass;
   p->fused_norm = second_pass && g.cta_pair && !per_head_norm(d) && (d.flags & QKV_CTE_FLAG_NORM_IN_GEMM) &&
                   !(d.flags & QKV_CTE_FLAG_SERIAL_PASSES);
-  make_bands(g, band_tiles(g));
+  make_bands(g, band_tiles(g), band_m_chunks());
   WorkspaceLayout& w = p->ws;
   w.status_off = 0;
   w.sumsq_off = 256;

@@ -21,17 +21,21 @@ def bands_bin(tmp_path_factory):
     return out
 
 
-@pytest.mark.parametrize("T,H,I,tile_n,k_end,band", [
-    (32760, 5120, 15360, 240, 10240, 45),   # Wan 480p: one V band, one Q/K band
-    (32760, 5120, 15360, 240, 10240, 10),
-    (75600, 5120, 15360, 256, 10240, 1),    # one N tile per band: capped at 16 bands
-    (256, 512, 1536, 240, 1024, 3),
-    (1, 256, 640, 128, 512, 2),
-    (4096, 5120, 5120, 240, 5120, 45),      # separate mode: every tile is Q
-    (129, 384, 576, 192, 448, 1000),
+@pytest.mark.parametrize("T,H,I,tile_n,k_end,band,chunks", [
+    (32760, 5120, 15360, 240, 10240, 45, 1),   # Wan 480p: one V band, one Q/K band
+    (32760, 5120, 15360, 240, 10240, 10, 1),
+    (32760, 5120, 15360, 240, 10240, 23, 4),   # 28 MB bands, Q/K bands over four row-panel ranges
+    (32760, 5120, 15360, 240, 10240, 23, 20),  # more chunks than the segment cap allows
+    (75600, 5120, 15360, 256, 10240, 1, 1),    # one N tile per band: capped at 16 bands
+    (256, 512, 1536, 240, 1024, 3, 1),
+    (256, 512, 1536, 240, 1024, 3, 3),         # more chunks than row panels
+    (1, 256, 640, 128, 512, 2, 2),
+    (4096, 5120, 5120, 240, 5120, 45, 1),      # separate mode: every tile is Q
+    (4096, 5120, 5120, 240, 5120, 45, 5),
+    (129, 384, 576, 192, 448, 1000, 1),
 ])
-def test_banded_tile_order_covers_every_tile_once(bands_bin, T, H, I, tile_n, k_end, band):
-    r = subprocess.run([bands_bin, str(T), str(H), str(I), str(tile_n), str(k_end), str(band)],
+def test_banded_tile_order_covers_every_tile_once(bands_bin, T, H, I, tile_n, k_end, band, chunks):
+    r = subprocess.run([bands_bin, str(T), str(H), str(I), str(tile_n), str(k_end), str(band), str(chunks)],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.startswith("ok")
