@@ -12,8 +12,9 @@
 //
 // GB300 design (not the page's Trainium schedule):
 //   * persistent grid, one CTA per SM, tiles of 128 rows x tile_n columns, walked in
-//     bands of N tiles (V-only tiles first), row-panel-major inside a band, so the
-//     band's slab of W stays resident in L2 while A streams;
+//     bands of N tiles (those holding Q or K columns first, V-only tiles last),
+//     row-panel-major inside a band, so the band's slab of W stays resident in L2
+//     while A streams;
 //   * warp 0: TMA producer. Per K stage it loads a 128x128-byte A tile and a
 //     tile_n x 128-byte W tile (128-byte swizzle) plus the stage's repacked UE8M0
 //     block scales, all counted on one mbarrier;
