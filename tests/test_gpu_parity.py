@@ -202,6 +202,21 @@ def test_serial_and_overlapped_passes_agree(name):
     assert float(diff.max()) <= 2 ** -6 * float(out_a.float().abs().max())
 
 
+@pytest.mark.parametrize("d_head,nq,nkv", [(64, 5, 2), (96, 3, 2), (256, 2, 1)])
+def test_serial_pass_other_head_sizes(d_head, nq, nkv):
+    """The stand-alone norm/RoPE pass (serial flag: a full grid, two heads' loads in
+    flight per lane) with 16, 8 (and 8 idle lanes) and 4 rows per warp task."""
+    from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_SERIAL_PASSES
+
+    call = wl.custom_call(name=f"serial_d{d_head}", tokens=333, hidden=512, n_q_heads=nq, n_kv_heads=nkv,
+                          d_head=d_head, seed=140 + d_head, has_w_col_scale=True)
+    inp = wl.make_inputs(call)
+    g = to_device(inp, DEV)
+    op, out, ss, inv = run_path(call, g, flags=QKV_CTE_FLAG_SERIAL_PASSES)
+    op.status()
+    check_outputs(call, inp, out, ss, inv, name=call.name)
+
+
 def test_pass_times_reported():
     from rope_tcgen05_mxfp8_gb300 import QKV_CTE_FLAG_PROFILE
 
