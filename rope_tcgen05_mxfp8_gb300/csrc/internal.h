@@ -17,13 +17,15 @@ enum : uint32_t {
   kErrEpilogueTmemFullWait = 1u << 3,
   kErrDrainWait = 1u << 4,
   kErrNormReadyWait = 1u << 5,
+  kErrTileIdWait = 1u << 6,
 };
 
 // Workspace layout (all offsets 256-byte aligned):
 //   [0, 256)                 status word (offset 0); at kStampOffset four uint64
 //                            %globaltimer stamps: K1 first start, K1 last end, norm/RoPE
 //                            first start, norm/RoPE last end; at kTaskCounterOffset the
-//                            counter the norm/RoPE tasks are claimed from
+//                            counter the norm/RoPE tasks are claimed from, and after it
+//                            the counter the CTA-pair GEMM claims its tiles from
 //   [256, 256 + ss_bytes)    fp32 [T, 2] sum-of-squares accumulator (used when the
 //                            caller passes no sumsq buffer)
 //   [.., + sf_bytes)         W's UE8M0 scales repacked per (N tile, K stage) in the
@@ -48,6 +50,8 @@ enum : uint32_t {
 //                            fp32 row scales [T] the producer step writes for the GEMM
 constexpr size_t kStampOffset = 64;
 constexpr size_t kTaskCounterOffset = 128;  // uint32: the next unclaimed norm/RoPE task
+constexpr size_t kTileCounterOffset = 132;  // uint32: the next unclaimed CTA-pair GEMM tile
+static_assert(kTileCounterOffset == kTaskCounterOffset + 4, "prep clears both counters as one pair of words");
 constexpr int kSmTable = 1024;              // entries of the per-SM sub-partition table
 
 struct WorkspaceLayout {
@@ -58,6 +62,9 @@ struct WorkspaceLayout {
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 constexpr int kMaxBands = 16;
+
+// The CTA-pair GEMM takes its last kClaimedWaves waves of tiles from a counter.
+constexpr int kClaimedWaves = 6;
 
 // GEMM (kernel K1) configuration chosen at plan time.
 //
@@ -145,6 +152,7 @@ struct GemmArgs {
   uint32_t* ready;           // per-panel completion counters (K2 overlaps K1 on them)
   uint32_t* sm_busy;         // [kSmTable] sub-partitions of this kernel's load and MMA warps, per SM
   unsigned long long* stamps;  // [0] first CTA start (min), [1] last CTA end (max)
+  uint32_t* tile_next;       // the CTA-pair form's tile counter (zeroed by prep)
   uint32_t* status;
   int q_end, k_end;          // Q = [0, q_end), K = [q_end, k_end), V = [k_end, I)
   int d_head;
@@ -201,6 +209,10 @@ struct NormRopeArgs {
   unsigned long long* stamps;  // [0] first block start (min), [1] last block end (max)
   uint32_t* status;
   uint32_t* task_next;       // next unclaimed task (claimed by K2's warps, or by the fused GEMM's epilogue warps)
+  // The CTA-pair GEMM's claimed-tile counter and the count at which every pair has
+  // reached the claimed tail: from then on no warp of the pass holds back (or null).
+  const uint32_t* gemm_claims;
+  uint32_t release_at;
   // per-head norm (norm 2 RMS / 3 LayerNorm) from the GEMM's per-(row, head)
   // statistics (see GemmArgs); 0: the across-heads norm or none
   int head_kind;

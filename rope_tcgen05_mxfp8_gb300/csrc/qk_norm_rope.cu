@@ -10,9 +10,11 @@
 //
 // Beside K1, warps claim tasks in order from a counter. A warp that shares its SM
 // sub-partition with the TMA-load or MMA-issue warp of the K1 CTA on its SM (K1
-// publishes them per SM) holds back until that CTA has finished, then joins for the
-// tasks left: sharing those schedulers slows the GEMM about twice as much per unit of
-// this work as running on the other two sub-partitions. The per-head norms' tasks are
+// publishes them per SM) holds back until that CTA has finished, or until every GEMM
+// pair has reached the claimed tail of its tile sequence (the GEMM then balances the
+// pairs itself, and the pass must not be left with a backlog when it ends), then joins
+// for the tasks left: sharing those schedulers slows the GEMM about twice as much per
+// unit of this work as running on the other two sub-partitions. The per-head norms' tasks are
 // heavier (the statistics of every head): with fewer warps they would fall behind the
 // GEMM, so there, as when the pass runs alone, every warp takes every gridDim-th task
 // (no counter on the critical path).
@@ -47,6 +49,7 @@ __device__ __forceinline__ void defer_while_busy(const NormRopeArgs& p, long lon
     __nanosleep(2000);
     if (!(nrp::ld_relaxed(busy) & bit)) return;
     if (static_cast<long long>(nrp::ld_relaxed(p.task_next)) >= tasks) return;
+    if (p.gemm_claims != nullptr && nrp::ld_relaxed(p.gemm_claims) >= p.release_at) return;
     if (nrp::now_ns() - t0 > nrp::kWaitLimitNs) return;  // a hint only: go ahead
   }
 }

@@ -7,6 +7,7 @@
 #include <cstdarg>
 #include <cstdlib>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -468,6 +469,7 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   ga.ready = ready;
   ga.sm_busy = sm_busy;
   ga.stamps = stamps;
+  ga.tile_next = reinterpret_cast<uint32_t*>(ws + kTileCounterOffset);
   ga.status = status;
   ga.q_end = plan->q_end;
   ga.k_end = plan->k_end;
@@ -509,6 +511,14 @@ int qkv_cte_run(qkv_cte_plan_t plan, const uint8_t* A, const float* a_scale, con
   na.status = status;
   na.stamps = stamps + 2;
   na.task_next = task_next;
+  {
+    // every pair has claimed its first tail tile: the pass's held-back warps join in
+    const long long tiles = (long long)g.m_tiles * g.n_tiles;
+    const long long pairs = std::min<long long>(tiles, dev.sms / 2);
+    const bool tail = g.cta_pair && pairs > 0 && tiles / pairs > kClaimedWaves;
+    na.gemm_claims = tail ? ga.tile_next : nullptr;
+    na.release_at = tail ? (uint32_t)pairs : 0xFFFFFFFFu;
+  }
   na.head_kind = head_stats ? d.norm : 0;
   na.head_stats = stats;
   na.stat_parts = stat_parts(d.d_head, g.tile_n);
@@ -543,7 +553,7 @@ int qkv_cte_status(void* workspace, void* stream) {
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
   if (word == 0) return ok();
   const uint32_t known = kErrProducerEmptyWait | kErrMmaFullWait | kErrMmaTmemEmptyWait |
-                         kErrEpilogueTmemFullWait | kErrDrainWait | kErrNormReadyWait;
+                         kErrEpilogueTmemFullWait | kErrDrainWait | kErrNormReadyWait | kErrTileIdWait;
   if (word & ~known)
     return fail(QKV_CTE_ERR_INVALID,
                 "workspace status word holds 0x%x, which no run wrote: zero the workspace before its first use",
@@ -553,13 +563,14 @@ int qkv_cte_status(void* workspace, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return fail(QKV_CTE_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
   return fail(QKV_CTE_ERR_DEVICE_TIMEOUT,
-              "device wait ran out (status 0x%x:%s%s%s%s%s%s)", word,
+              "device wait ran out (status 0x%x:%s%s%s%s%s%s%s)", word,
               (word & kErrProducerEmptyWait) ? " load-stage-free" : "",
               (word & kErrMmaFullWait) ? " mma-operands-ready" : "",
               (word & kErrMmaTmemEmptyWait) ? " mma-accumulator-free" : "",
               (word & kErrEpilogueTmemFullWait) ? " epilogue-accumulator-ready" : "",
               (word & kErrDrainWait) ? " drain" : "",
-              (word & kErrNormReadyWait) ? " norm-panel-ready" : "");
+              (word & kErrNormReadyWait) ? " norm-panel-ready" : "",
+              (word & kErrTileIdWait) ? " tile-id" : "");
 }
 
 namespace {

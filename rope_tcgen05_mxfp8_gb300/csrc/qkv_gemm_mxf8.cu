@@ -78,7 +78,8 @@ __global__ void __launch_bounds__(kPrepThreads) qkv_prep_kernel(
   for (size_t i = first; i < static_cast<size_t>(kSmTable); i += stride) sm_busy[i] = 0u;
   if (first == 0) {
     status[0] = 0u;
-    *task_next = 0u;
+    task_next[0] = 0u;  // norm/RoPE tasks
+    task_next[1] = 0u;  // CTA-pair GEMM tiles (kTileCounterOffset)
     stamps[0] = stamps[2] = ~0ull;
     stamps[1] = stamps[3] = 0ull;
   }

@@ -758,6 +758,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the Wan 480p shape with the norm/RoPE pass overlapped: 1.616 ms per step with three
 // 256-byte stages against 2.094 ms with two (which left more L1 for the pass beside
 // the GEMM, but cannot cover the load latency).
+// The CTA-pair form's tile sequence: whole waves first, pair p taking tiles p, p + P,
+// p + 2P, ... (P pairs), then the last kClaimedWaves waves' worth from a counter, so
+// that pairs slowed by other work on their SMs (the norm/RoPE pass beside the GEMM)
+// take fewer of them instead of finishing last. Claiming every tile cost about 4 % of
+// the GEMM's cycles at the Wan 480p shape; claiming the last six waves only keeps that
+// to the tail. Once every pair has claimed a tile the norm/RoPE pass stops holding its
+// warps back (the counter is its signal), so that it ends with the now even tail.
+//
+// A claimed tile is claimed by the leader's load thread one tile ahead (the atomic's
+// latency hides behind the current tile's loads) and published to both CTAs through a
+// ring of kTileRing slots with one mbarrier each (one arrival per publication; -1 ends
+// the sequence). A slot is rewritten kTileRing tiles later; by then every reader has
+// read it: the load thread publishes tile s only after it has loaded tile s - 1, which
+// needs the MMA issuer to have finished tile s - 1 - STAGES, which needs the epilogue to
+// have drained tile s - 1 - STAGES - ACC_STAGES.
+constexpr int kTileRing = 8;
+
+struct PairSchedule {
+  int pair, pairs, n_static, dyn_base, num_tiles;
+
+  __device__ __forceinline__ PairSchedule(int num_tiles_, int pair_, int pairs_)
+      : pair(pair_), pairs(pairs_), num_tiles(num_tiles_) {
+    const int waves = num_tiles_ / pairs_;
+    n_static = waves > kClaimedWaves ? waves - kClaimedWaves : 0;
+    dyn_base = n_static * pairs_;
+  }
+  __device__ __forceinline__ bool is_static(int seq) const { return seq < n_static; }
+  __device__ __forceinline__ int static_tile(int seq) const { return pair + seq * pairs; }
+};
+
+struct PairTileRing {
+  int* ids;        // [kTileRing]
+  uint64_t* full;  // [kTileRing]
+
+  // Leader's load thread: claimed tile (or -1) number `d` of the pair (counted from
+  // the pair's first claimed tile), to both CTAs.
+  __device__ __forceinline__ void publish(int d, int tile, uint32_t peer) const {
+    const int r = d & (kTileRing - 1);
+    ids[r] = tile;
+    st_shared_cluster_s32(mapa_shared(smem_u32(&ids[r]), peer), tile);
+    mbar_arrive(smem_u32(&full[r]));
+    mbar_arrive_cluster(mapa_shared(smem_u32(&full[r]), peer));
+  }
+
+  // Any reader: claimed tile number `d` (false if the bounded wait ran out, or if the
+  // slot holds neither a tile below num_tiles nor -1).
+  __device__ __forceinline__ bool fetch(int d, int& tile, const volatile int* abort, int num_tiles) const {
+    const int r = d & (kTileRing - 1);
+    if (!mbar_wait_bounded_cluster(smem_u32(&full[r]), static_cast<uint32_t>(d / kTileRing) & 1u, abort,
+                                   kWaitLimitNs))
+      return false;
+    tile = ids[r];
+    return tile >= -1 && tile < num_tiles;
+  }
+};
+
 template <int BN>
 struct K1PairCfg {
   static constexpr int HALF_N = BN / 2;
@@ -909,15 +965,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint32_t* busy_slot = tmem_slot + 2;  // [2]: sub-partition bits of the load and MMA warps
+  const PairTileRing ring{reinterpret_cast<int*>(busy_slot + 2), reinterpret_cast<uint64_t*>(busy_slot + 2 + kTileRing)};
+  static_assert((2 * C::STAGES + 5) * 8 + 16 + kTileRing * (4 + 8) <= 256, "barrier area");
+  static_assert(C::STAGES + C::ACC_STAGES + 1 < kTileRing, "a tile-id slot is reread only after every reader");
+  const PairSchedule sched(g.m_tiles * g.n_tiles, static_cast<int>(blockIdx.x >> 1), static_cast<int>(gridDim.x >> 1));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();  // rank in the pair
   constexpr uint32_t lead = 0u;             // cluster rank of the pair's leader
   const bool leader = rank == 0;
-  // Tiles of this pair: tile_first, tile_first + tile_step, ...
-  const int tile_first = static_cast<int>(blockIdx.x >> 1);
-  const int tile_step = static_cast<int>(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -929,6 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&tempty[s]), 8);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int r = 0; r < kTileRing; ++r) mbar_init(smem_u32(&ring.full[r]), 1);
     *abort_flag = 0;
     fence_barrier_init();
     prefetch_tmap(&tmA);
@@ -969,9 +1027,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
-      bool ok = (a.flags & kFlagTestStall) == 0;
+      // test hook: hand out the first tile, then load nothing (every wait downstream runs out)
+      const bool stall = (a.flags & kFlagTestStall) != 0;
+      bool ok = true;
       const int n_stages = (g.k_stages + C::KW - 1) / C::KW;
-      for (int tile = tile_first; ok && tile < num_tiles; tile += tile_step) {
+      uint32_t claimed = (leader && sched.n_static == 0) ? atomicAdd(a.tile_next, 1u) : 0u;
+      for (int seq = 0; ok; ++seq) {
+        int tile;
+        if (sched.is_static(seq)) {
+          tile = sched.static_tile(seq);
+          if (leader && seq + 1 == sched.n_static) claimed = atomicAdd(a.tile_next, 1u);  // the first claimed
+        } else if (leader) {
+          const long long t = static_cast<long long>(sched.dyn_base) + claimed;
+          tile = t < num_tiles ? static_cast<int>(t) : -1;
+          ring.publish(seq - sched.n_static, tile, lead ^ 1u);
+          if (tile >= 0) claimed = atomicAdd(a.tile_next, 1u);
+        } else if (!ring.fetch(seq - sched.n_static, tile, abort_flag, num_tiles)) {
+          record_failure(a.status, abort_flag, kErrTileIdWait);
+          break;
+        }
+        if (tile < 0 || stall) break;
         int m_blk, n_blk;
         tile_coords(g, tile, m_blk, n_blk);
         for (int ks = 0; ks < n_stages; ++ks) {
@@ -1036,7 +1111,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = tile_first; ok && tile < num_tiles; tile += tile_step) {
+      for (int seq = 0; ok; ++seq) {
+        int tile;
+        if (sched.is_static(seq)) {
+          tile = sched.static_tile(seq);
+        } else if (!ring.fetch(seq - sched.n_static, tile, abort_flag, num_tiles)) {
+          record_failure(a.status, abort_flag, kErrTileIdWait);
+          break;
+        }
+        if (tile < 0) break;
         if (!mbar_wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1u, abort_flag, kWaitLimitNs)) {
           record_failure(a.status, abort_flag, kErrMmaTmemEmptyWait);
           break;
@@ -1103,7 +1186,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     FusedWork fw;
     const long long n_tasks = kFused ? nrp::task_count(nr, kFusedHeadGroup) : 0;
     const uint64_t once = kFused ? nrp::evict_first_policy() : 0;
-    for (int tile = tile_first; tile < num_tiles; tile += tile_step) {
+    for (int seq = 0;; ++seq) {
+      int tile = -1, got = 1;
+      if (sched.is_static(seq)) {
+        tile = sched.static_tile(seq);
+      } else {
+        if (lane == 0) got = ring.fetch(seq - sched.n_static, tile, abort_flag, num_tiles) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        tile = __shfl_sync(0xffffffffu, tile, 0);
+      }
+      if (!got) {
+        if (lane == 0) record_failure(a.status, abort_flag, kErrTileIdWait);
+        break;
+      }
+      if (tile < 0) break;
       int m_blk, n_blk;
       tile_coords(g, tile, m_blk, n_blk);
       bool ok;
