@@ -66,6 +66,22 @@ constexpr int kMaxBands = 16;
 // The CTA-pair GEMM takes its last kClaimedWaves waves of tiles from a counter.
 constexpr int kClaimedWaves = 6;
 
+// The static part of a CTA pair's tile sequence: its tile number seq < n_static is
+// pair + seq * pairs; the tiles from dyn_base on are claimed from the counter
+// (dyn_base + the counter's value, while below num_tiles).
+struct PairSchedule {
+  int pair, pairs, n_static, dyn_base, num_tiles;
+
+  __host__ __device__ PairSchedule(int num_tiles_, int pair_, int pairs_)
+      : pair(pair_), pairs(pairs_), num_tiles(num_tiles_) {
+    const int waves = num_tiles_ / pairs_;
+    n_static = waves > kClaimedWaves ? waves - kClaimedWaves : 0;
+    dyn_base = n_static * pairs_;
+  }
+  __host__ __device__ bool is_static(int seq) const { return seq < n_static; }
+  __host__ __device__ int static_tile(int seq) const { return pair + seq * pairs; }
+};
+
 // GEMM (kernel K1) configuration chosen at plan time.
 //
 // Tile order: the N tiles are cut into bands (contiguous runs of N tiles). The

@@ -775,18 +775,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // have drained tile s - 1 - STAGES - ACC_STAGES.
 constexpr int kTileRing = 8;
 
-struct PairSchedule {
-  int pair, pairs, n_static, dyn_base, num_tiles;
-
-  __device__ __forceinline__ PairSchedule(int num_tiles_, int pair_, int pairs_)
-      : pair(pair_), pairs(pairs_), num_tiles(num_tiles_) {
-    const int waves = num_tiles_ / pairs_;
-    n_static = waves > kClaimedWaves ? waves - kClaimedWaves : 0;
-    dyn_base = n_static * pairs_;
-  }
-  __device__ __forceinline__ bool is_static(int seq) const { return seq < n_static; }
-  __device__ __forceinline__ int static_tile(int seq) const { return pair + seq * pairs; }
-};
 
 struct PairTileRing {
   int* ids;        // [kTileRing]

@@ -41,6 +41,33 @@ def test_banded_tile_order_covers_every_tile_once(bands_bin, T, H, I, tile_n, k_
     assert r.stdout.startswith("ok")
 
 
+@pytest.fixture(scope="module")
+def schedule_bin(tmp_path_factory):
+    gxx = shutil.which("g++")
+    if gxx is None:
+        pytest.skip("no g++")
+    out = str(tmp_path_factory.mktemp("host") / "schedule_check")
+    cmd = [gxx, "-std=c++17", "-O1", "-I", CSRC, "-I", "/usr/local/cuda/include",
+           os.path.join(ROOT, "tests", "host", "schedule_check.cpp"), "-o", out]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+@pytest.mark.parametrize("num_tiles,pairs,seed", [
+    (8192, 76, 1),    # Wan 480p: 107 full waves, the last six and the partial one claimed
+    (8192, 76, 7),
+    (1024, 76, 3),    # 4096 tokens: 13 waves
+    (88, 76, 5),      # the K|V call: one wave and a bit, all claimed
+    (7, 7, 2),        # fewer tiles than pairs (the grid shrinks to the tiles)
+    (456, 76, 4),     # exactly six waves: nothing static
+    (532, 76, 9),     # exactly seven waves: one static
+])
+def test_pair_schedule_covers_every_tile_once(schedule_bin, num_tiles, pairs, seed):
+    r = subprocess.run([schedule_bin, str(num_tiles), str(pairs), str(seed)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.startswith("ok")
+
+
 def test_clock_samples_are_kept_only_inside_the_timed_region():
     """bench.py reports clocks from the nvidia-smi samples taken while the timed steps
     ran; idle samples before or after them must not enter the median."""
